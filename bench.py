@@ -1,0 +1,408 @@
+"""Benchmark of the NVFP4 W4A4 MoE expert forward on GB300.
+
+One step = one moe_expert_forward call (route, permute + amax + quantise,
+FC1 + SwiGLU + requantise, FC2 + router-weighted scatter, unpermute reduce)
+over the Qwen3-30B-A3B-shaped layer (T = 65536 tokens = 16 x 4096, d = 2048,
+E = 128, top-8, d_ff = 768, uniform router logits), inputs resident in HBM.
+Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...    # the CPU oracle as the reference arm
+
+Multi-GPU (torchrun, one rank per GPU): token data parallelism, each rank
+runs its own batch of T tokens with replicated weights; no collective on the
+data path; timing is the max over ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 MoE expert-forward tokens/s at 1 GB300; % FP4 tensor peak, % HBM BW"
+UNIT = "tokens/s"
+# Dense FP4 (NVFP4 block-scaled) tensor peak derived from the measured bf16
+# cuBLAS peak times the nominal fp4:bf16 ratio (13.5 / 2.25 = 6).
+FP4_PER_BF16 = 6.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed to the kernel source it was taken on; it is
+# reported only while that source is unchanged.  Filled from
+# profiles/*.md summaries.
+NCU_TRAFFIC = {}
+
+
+def src_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "nvfp4_w4a4_moe_top_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------
+# distributed harness (testable on CPU with gloo)
+# --------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_seed(base_seed, rank):
+    """Each rank draws its own token batch (data parallel); weights are
+    shared (seeded by the base seed only)."""
+    return base_seed + 1000003 * rank
+
+
+def max_over_ranks(value, world, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank_step, steps, world, seconds_max):
+    """Whole-job throughput: all ranks' tokens over the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / seconds_max
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "moe_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# workload
+# --------------------------------------------------------------------------
+def make_inputs(lay, seed_rank):
+    import synth
+    rank_lay = synth.layer(lay.name, seed=seed_rank)
+    return rank_lay.x(), rank_lay.logits()
+
+
+def algorithmic(lay):
+    """Algorithmic work of one forward: routed rows only (no pad rows), the
+    method's own dataflow (x read once, codes written k times)."""
+    T, d, E, k, F = lay.T, lay.d, lay.E, lay.k, lay.d_ff
+    R = T * k
+    fc1_flops = 2.0 * R * d * 2 * F
+    fc2_flops = 2.0 * R * F * d
+    fp4 = lambda rows, K: rows * (K / 2 + K / 16)            # codes + block scales
+    w1 = fp4(E * 2 * F, d) + E * 2 * F * 4
+    w2 = fp4(E * d, F) + E * d * 4
+    bytes_fc1 = fp4(R, d) + R * 4 + w1 + fp4(R, F) + R * 4       # A in, W1 in, h out
+    bytes_fc2 = fp4(R, F) + R * 4 + w2 + R * d * 2               # h in, W2 in, slots out
+    bytes_reduce = R * d * 2 + T * d * 2
+    bytes_quant = T * d * 2 + fp4(R, d) + R * 4                  # x in once, k copies out
+    bytes_route = T * E * 4 + R * 12
+    return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, bytes_fc1=bytes_fc1, bytes_fc2=bytes_fc2,
+                bytes_reduce=bytes_reduce, bytes_quant=bytes_quant, bytes_route=bytes_route)
+
+
+def native(args):
+    import numpy as np
+    import torch
+
+    import nvfp4_w4a4_moe_top_gb300 as M
+    import synth
+    from nvfp4_w4a4_moe_top_gb300 import build as B
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    lay = synth.layer(args.workload, seed=args.seed)
+    T, E, k, d, F = lay.T, lay.E, lay.k, lay.d, lay.d_ff
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    W1 = torch.stack([to_dev(lay.w1_expert(e)) for e in range(E)])
+    W2 = torch.stack([to_dev(lay.w2_expert(e)) for e in range(E)])
+    w1q, w2q = M.quantize_weights(W1), M.quantize_weights(W2)
+    del W1, W2
+    x_np, lg_np = make_inputs(lay, shard_seed(args.seed, rank))
+    x, lg = to_dev(x_np), to_dev(lg_np)
+    out = torch.empty((T, d), dtype=torch.int16, device=dev)
+    ws = M.forward_workspace(T, E, k, d, F, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        M.moe_expert_forward(x, lg, T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"], w2q["sf"],
+                             w2q["g"], out, ws, status, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %#x" % int(status.item()))
+
+    # ---- headline: K forwards on resident inputs, device-timed ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    sec = ev0.elapsed_time(ev1) / 1e3
+    sec_max = max_over_ranks(sec, world, dev)
+    value = aggregate(T, args.steps, world, sec_max)
+    clocks = clk.summary()
+
+    # ---- per-kernel durations of the dominant kernels (same stream, same
+    # inputs, events around the one launch each entry point makes) ----
+    v = M.forward_views(ws, T, E, k, d, F)
+    mc = v["m_cap"]
+    f1ws = ws[M.forward_workspace_layout(T, E, k, d, F)["fc1_staging"]:]
+    hq = M.empty_quantized(mc, F, dev)
+    reps = max(5, min(args.steps, 50))
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    t_fc1 = timed(lambda: M.nvfp4_grouped_gemm_fc1_swiglu(
+        v["x_codes"], v["x_sf"], v["x_g"], v["offsets"], E, mc, d, F, w1q["codes"], w1q["sf"], w1q["g"],
+        hq["codes"], hq["sf"], hq["g"], None, None, f1ws, status, stream))
+    slots2 = v["slots"]
+    t_fc2r = timed(lambda: M.nvfp4_grouped_gemm_fc2_unpermute(
+        v["h_codes"], v["h_sf"], v["h_g"], v["offsets"], E, mc, F, d, w2q["codes"], w2q["sf"], w2q["g"],
+        v["row_to_token"], v["token_slot_row"], v["topk_w"], T, k, slots2, out, None, status, stream))
+
+    peaks, peak_kind = load_peaks()
+    alg = algorithmic(lay)
+    fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
+    fc1_tflops = alg["fc1_flops"] / t_fc1 / 1e12
+    sha = src_sha("gemm.cu", "common.cuh")
+    tr = NCU_TRAFFIC.get("fc1")
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == sha else None
+    roofline = {"kernel": "fc1_swiglu_kernel", "bound": "tensor", "achieved": round(fc1_tflops, 1),
+                "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(fc1_tflops / fp4_peak, 4),
+                "traffic": traffic, "ms_per_launch": round(t_fc1 * 1e3, 4),
+                "peak_source": "%s bf16 burst x %g (nominal fp4:bf16)" % (peak_kind, FP4_PER_BF16)}
+    fc2_gbs = (alg["bytes_fc2"] + alg["bytes_reduce"]) / t_fc2r / 1e9
+    roofline_hbm = {"kernel": "fc2_scatter_kernel + unpermute_reduce_kernel", "bound": "hbm",
+                    "achieved": round(fc2_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(fc2_gbs / peaks["hbm_gbs"], 4), "ms_per_launch": round(t_fc2r * 1e3, 4),
+                    "peak_source": peak_kind}
+
+    # ---- end to end through the public call with host buffers ----
+    xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+    lgh = torch.from_numpy(lg_np).pin_memory()
+    outh = torch.empty((T, d), dtype=torch.int16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        lg.copy_(lgh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    e2e = {"value": round(aggregate(T, e2e_steps, world, e2e_sec), 1), "unit": UNIT,
+           "h2d_bytes_per_step": int(xh.numel() * 2 + lgh.numel() * 4), "d2h_bytes_per_step": int(outh.numel() * 2)}
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %#x" % int(status.item()))
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec_max / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate, bf16 out)",
+            "data": "synthetic (seeded; shapes and distributions of the Qwen3-30B-A3B expert layer)",
+            "config": {"workload": args.workload, "T": T, "d": d, "E": E, "k": k, "d_ff": F,
+                       "parallelism": "token data parallel x%d" % world, "l2": "inputs larger than L2 (no flush)"},
+            "gpu_launches": 7 * args.steps, "roofline": roofline, "roofline_hbm": roofline_hbm,
+            "clocks": clocks, "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(lay, args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores
+# --------------------------------------------------------------------------
+def oracle_weights(lay):
+    import numpy as np
+    import oracle
+    w1 = [oracle.quantize_weights(lay.w1_expert(e)[None]) for e in range(lay.E)]
+    w2 = [oracle.quantize_weights(lay.w2_expert(e)[None]) for e in range(lay.E)]
+    cat = lambda qs: (np.concatenate([q[0] for q in qs]), np.concatenate([q[1] for q in qs]),
+                      np.concatenate([q[2] for q in qs]))
+    return cat(w1), cat(w2)
+
+
+def cpu_baseline(lay, args, tokens=None):
+    import oracle
+    tokens = tokens or args.cpu_tokens
+    w1q, w2q = oracle_weights(lay)
+    x = lay.x_rows(range(tokens))
+    lg = lay.logits_rows(range(tokens))
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, lg, w1q, w2q, lay.k, lay.d_ff)
+    sec = time.perf_counter() - t0
+    return {"value": round(tokens / sec, 2), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "first %d tokens of the %s workload, one oracle forward (weights quantised beforehand)"
+                      % (tokens, args.workload)}
+
+
+def reference(args):
+    """The oracle as the reference arm: W untimed + K timed steps, each step a
+    bounded sample (args.ref_tokens consecutive tokens) of the same workload."""
+    import oracle
+    import synth
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    lay = synth.layer(args.workload, seed=args.seed)
+    w1q, w2q = oracle_weights(lay)
+    n = args.ref_tokens
+
+    def step(i):
+        t0 = (i * n) % lay.T
+        toks = [(t0 + j) % lay.T for j in range(n)]
+        oracle.moe_forward(lay.x_rows(toks), lay.logits_rows(toks), w1q, w2q, lay.k, lay.d_ff)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    sec = time.perf_counter() - t0
+    value = n * args.steps / sec
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (oracle)",
+            "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "T": lay.T, "d": lay.d, "E": lay.E, "k": lay.k, "d_ff": lay.d_ff},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": "%d tokens per step" % n},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="qwen64k")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--ref-tokens", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,236 @@
+/*
+ * moe_nvfp4.h -- C ABI of libmoe_nvfp4.so: the native NVFP4 W4A4
+ * Mixture-of-Experts expert forward on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation and its sources (page title, section):
+ *   - NVFP4 format: E2M1 elements, one E4M3 block scale per 16 elements, an
+ *     FP32 outer scale; decode x^ = g * s_b * c.  "miniTE Technical Report:
+ *     Stable and Efficient Reinforcement Learning with Native NVFP4", section
+ *     2.2, and the paper.rainbus.top summary, prerequisites ("NVFP4 format").
+ *   - Block scale s_b = Q_E4M3(a_b / (6 g)), element code Q_E2M1(x / (g s_b)):
+ *     Technical Report section 5.1, equation.
+ *   - Outer scale g = amax / (6*448), per token for activations and per output
+ *     row for weights: Technical Report section 4.3 table ("miniTE
+ *     per-token"), rainbus summary, method step 4.
+ *   - Quantiser writes packed codes, block scales and outer scales straight
+ *     into the contiguous buffers the grouped GEMM consumes; per-token amax is
+ *     gathered during permutation; expert offsets live on the device: AI
+ *     summary ("miniTE: Diagnosing and Bridging the Execution Gap in Native
+ *     NVFP4 Reinforcement Learning"), "Methodology in Plain English" and "Key
+ *     Contributions" item 4; rainbus summary, method step 6.
+ *   - Grouped GEMM U_e = MMA_NVFP4(X_e, W_e^T) with the FP32 epilogue that
+ *     multiplies by g_x g_w and casts to BF16: rainbus summary, core method.
+ *   - Router top-k and the FC1 -> SwiGLU -> FC2 expert, uneven and empty
+ *     groups: rainbus summary, prerequisites ("MoE and grouped GEMM").
+ *
+ * Execution specification (MOE-NVFP4-SPEC-1), fixed here:
+ *   route: top-k by (FP32 logit desc, expert id asc); slot j = j-th selected
+ *     expert in ascending id; weights = softmax over the selected logits.
+ *   permute: groups padded to 128 rows; rows of a group in ascending token
+ *     order; pad rows are all-zero rows.
+ *   quantise: g = amax/2688; s_b = E4M3_RNE_satfinite(a_b/(6g));
+ *     S_b = g*s_b; c = E2M1_RNE_satfinite(v/S_b) (true division); amax = 0
+ *     gives g = 0 and zero codes; codes two per byte, even element in the low
+ *     nibble; sign of a zero code = sign of the quotient.
+ *   FC1: y = acc*(g_x*g_w) in FP32, u = BF16(y); gate = columns [0,d_ff),
+ *     up = [d_ff, 2 d_ff); h = BF16(silu(gate)*up); h requantised per row.
+ *   FC2: y2 = acc*(g_h*g_w2) in FP32; z = BF16(w_{t,e}*y2) stored at slot
+ *     (t, j); out[t] = BF16(sum_j FP32(z_j)) in ascending j.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned
+ *     (TMA and 128-bit accesses).  The library never allocates, frees or
+ *     synchronises; every call is enqueued on `stream` (a cudaStream_t passed
+ *     as void*, NULL = legacy default stream) and returns before the GPU work
+ *     completes.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code, detected on the host
+ *     before anything is enqueued (except MOE_ERR_CUDA, reported from
+ *     cudaGetLastError after the launches).
+ *   - `status` (optional device int*, may be NULL) receives MOE_STATUS_* bits
+ *     OR-ed in by the kernels when they see data faults (non-finite inputs,
+ *     invalid routing replay) or give up a bounded wait.  The kernels finish
+ *     in all cases; nothing traps.  The caller zeroes it.
+ *   - Results are deterministic bit for bit for given inputs.
+ *   - Block-scale buffers ("sf") use the 128x4 tile layout: logical byte
+ *     (r, c) of a [rows][K/16] matrix lives at
+ *     ((r/128)*(K/64) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4,
+ *     nvfp4_sf_bytes(rows, K) bytes in total.
+ *
+ * Shape limits: 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T = 0 is a no-op),
+ * d % 128 == 0, d_ff % 128 == 0, 128 <= d, d_ff <= 4096; row counts < 2^31.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_NVFP4_ABI_VERSION 1
+
+/* return codes */
+#define MOE_OK              0
+#define MOE_ERR_POINTER    -1   /* required pointer NULL or not 16-byte aligned */
+#define MOE_ERR_SHAPE      -2   /* shape outside the limits above */
+#define MOE_ERR_WORKSPACE  -3   /* workspace smaller than the *_workspace_bytes helper */
+#define MOE_ERR_CUDA       -4   /* CUDA runtime or launch error */
+#define MOE_ERR_DEVICE     -5   /* current device is not compute capability 10.3 */
+
+/* device status bits */
+#define MOE_STATUS_NONFINITE_X       0x01  /* NaN/Inf in activations (x or h) */
+#define MOE_STATUS_NONFINITE_LOGITS  0x02  /* NaN/Inf in router logits */
+#define MOE_STATUS_NONFINITE_WEIGHT  0x04  /* NaN/Inf in weights being quantised */
+#define MOE_STATUS_BAD_ROUTING       0x08  /* replayed ids out of range or not strictly ascending */
+#define MOE_STATUS_TIMEOUT           0x10  /* a GEMM gave up a bounded wait; its outputs are invalid */
+
+/* ---------------------------------------------------------------------- */
+/* Helpers (host only, no CUDA calls).                                      */
+/* ---------------------------------------------------------------------- */
+int         moe_abi_version(void);
+const char* moe_status_string(int code);
+
+/* Rows of the padded routed-row buffers: T*k + 127*min(E, T*k), rounded up to
+ * a multiple of 128.  Every per-row buffer below has this many rows. */
+int64_t moe_m_cap(int T, int E, int k);
+
+/* Bytes of a block-scale buffer for `rows` rows of K elements (K % 64 == 0). */
+size_t nvfp4_sf_bytes(int64_t rows, int K);
+
+/* Workspace of moe_permute_amax (chunk histograms). */
+size_t moe_permute_workspace_bytes(int T, int E);
+
+/* Workspace of nvfp4_grouped_gemm_fc1_swiglu (per-CTA h staging). */
+size_t nvfp4_fc1_workspace_bytes(int d_ff);
+
+/* Workspace of moe_expert_forward (all intermediates of one forward). */
+size_t moe_expert_forward_workspace_bytes(int T, int E, int k, int d, int d_ff);
+
+/* Byte offsets of the intermediates inside moe_expert_forward's workspace,
+ * for inspection after a call (index order: 0 topk_ids i32[T][k],
+ * 1 topk_w f32[T][k], 2 token_slot_row i32[T][k], 3 counts i32[E],
+ * 4 offsets i32[E+1], 5 row_to_token i32[M_cap], 6 amax_tok f32[T],
+ * 7 x_codes u8[M_cap][d/2], 8 x_sf, 9 x_g f32[M_cap], 10 h_codes
+ * u8[M_cap][d_ff/2], 11 h_sf, 12 h_g f32[M_cap], 13 slots bf16[T][k][d],
+ * 14 chunk histograms, 15 FC1 staging).  Writes 16 entries; returns 0. */
+int moe_expert_forward_workspace_layout(int T, int E, int k, int d, int d_ff,
+                                        size_t offsets_out[16]);
+
+/* ---------------------------------------------------------------------- */
+/* Entry points.                                                            */
+/* ---------------------------------------------------------------------- */
+
+/* Per-output-row NVFP4 quantisation of expert weights (Technical Report
+ * section 4.3 table: one outer scale per row of the flattened expert
+ * weights; section 5.1 equation for the block scales and codes).
+ *   W      bf16 [E][N][K], row-major.
+ *   codes  u8   [E][N][K/2]       (out)
+ *   sf     u8   nvfp4_sf_bytes(E*N, K), the E*N rows as one matrix (out)
+ *   g      f32  [E][N]            (out)
+ * Needs N % 128 == 0, K % 64 == 0, 64 <= K <= 4096.  Called for W1
+ * (N = 2 d_ff, K = d) and W2 (N = d, K = d_ff). */
+int moe_nvfp4_quantize_weights(const uint16_t* W, int E, int N, int K,
+                               uint8_t* codes, uint8_t* sf, float* g,
+                               int* status, void* stream);
+
+/* Route, permute, pad, expert offsets, and per-token amax gathered in the
+ * same pass (rainbus summary, method step 6: sort fused with the amax scan,
+ * padding carries the statistics; AI summary methodology: no separate amax
+ * scan).
+ *   logits        f32 [T][E], or NULL to replay routing from ext_ids/ext_w
+ *   ext_ids/ext_w i32/f32 [T][k]: replayed routing (ids strictly ascending per
+ *                 token), used only when logits == NULL
+ *   x             bf16 [T][d], or NULL to skip amax (then d is ignored and
+ *                 amax_tok/amax_row may be NULL)
+ *   topk_ids      i32 [T][k] (out) ascending expert ids = slot order
+ *   topk_w        f32 [T][k] (out) renormalised router weights
+ *   counts        i32 [E]    (out) routed rows per expert
+ *   offsets       i32 [E+1]  (out) padded exclusive prefix; offsets[E] = M_pad
+ *   row_to_token  i32 [M_cap](out) token of each row, -1 on pad rows and on
+ *                 rows >= M_pad
+ *   token_slot_row i32 [T][k](out) row of slot (t, j)
+ *   amax_tok      f32 [T]    (out) max |x_t|
+ *   amax_row      f32 [M_cap](out) amax_tok of the row's token, 0 on pad rows
+ *   ws            device scratch of moe_permute_workspace_bytes(T, E) bytes */
+int moe_permute_amax(const float* logits, const int32_t* ext_ids,
+                     const float* ext_w, const uint16_t* x, int T, int E,
+                     int k, int d, int32_t* topk_ids, float* topk_w,
+                     int32_t* counts, int32_t* offsets, int32_t* row_to_token,
+                     int32_t* token_slot_row, float* amax_tok, float* amax_row,
+                     void* ws, size_t ws_bytes, int* status, void* stream);
+
+/* Quantise rows into the GEMM's buffers (Technical Report section 5.1
+ * equation; AI summary methodology: codes, block scales and outer scales are
+ * written straight into the contiguous buffers the GEMM consumes).
+ *   src      bf16 [src_rows][K]
+ *   row_map  i32 [dst_rows]: destination row r takes source row row_map[r];
+ *            a negative entry writes an all-zero row; NULL = identity
+ *   amax     f32 [src_rows] outer-scale arguments, NULL = computed per row
+ *   codes    u8 [dst_rows][K/2], sf nvfp4_sf_bytes(dst_rows, K), g f32
+ *            [dst_rows] (out)
+ * Needs K % 64 == 0, 64 <= K <= 4096. */
+int nvfp4_quantize_rows(const uint16_t* src, int src_rows, int K,
+                        const int32_t* row_map, const float* amax,
+                        int dst_rows, uint8_t* codes, uint8_t* sf, float* g,
+                        int* status, void* stream);
+
+/* Grouped FC1 with fused SwiGLU and requantisation (rainbus summary, core
+ * method: native block-scaled MMA, FP32 epilogue broadcast of g_x g_w, BF16
+ * cast; prerequisites: FC1 -> SwiGLU -> FC2).  Groups are the 128-row
+ * aligned ranges [offsets[e], offsets[e+1]) read on the device; empty groups
+ * are skipped.
+ *   a_codes/a_sf/a_g  quantised activations, M_cap rows of K = d
+ *   w1_codes/w1_sf/w1_g  from moe_nvfp4_quantize_weights(W1, E, 2 d_ff, d)
+ *   h_codes/h_sf/h_g  quantised h, M_cap rows of K = d_ff (out; rows >=
+ *                     offsets[E] untouched)
+ *   dbg_u_f32  f32 [M_cap][2 d_ff] pre-cast FC1 outputs, or NULL
+ *   dbg_h      bf16 [M_cap][d_ff] h before requantisation, or NULL
+ *   ws         nvfp4_fc1_workspace_bytes(d_ff) bytes of device scratch */
+int nvfp4_grouped_gemm_fc1_swiglu(
+    const uint8_t* a_codes, const uint8_t* a_sf, const float* a_g,
+    const int32_t* offsets, int E, int64_t M_cap, int d, int d_ff,
+    const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g,
+    uint8_t* h_codes, uint8_t* h_sf, float* h_g, float* dbg_u_f32,
+    uint16_t* dbg_h, void* ws, size_t ws_bytes, int* status, void* stream);
+
+/* Grouped FC2 with the router-weighted scatter epilogue, then the unpermute
+ * reduce (two launches).  z = BF16(topk_w[t][j] * (acc * (g_h * g_w2))) goes
+ * to slots[t][j][:], then out[t] = BF16(sum_j FP32(slots[t][j])) in ascending
+ * j (= ascending expert id).
+ *   h_codes/h_sf/h_g  M_cap rows of K = d_ff
+ *   w2_codes/w2_sf/w2_g from moe_nvfp4_quantize_weights(W2, E, d, d_ff)
+ *   row_to_token, token_slot_row, topk_w from moe_permute_amax
+ *   slots      bf16 [T][k][d] (workspace, also an output)
+ *   out        bf16 [T][d] (out)
+ *   dbg_y_f32  f32 [M_cap][d] pre-weighting expert outputs y2, or NULL */
+int nvfp4_grouped_gemm_fc2_unpermute(
+    const uint8_t* h_codes, const uint8_t* h_sf, const float* h_g,
+    const int32_t* offsets, int E, int64_t M_cap, int d_ff, int d,
+    const uint8_t* w2_codes, const uint8_t* w2_sf, const float* w2_g,
+    const int32_t* row_to_token, const int32_t* token_slot_row,
+    const float* topk_w, int T, int k, uint16_t* slots, uint16_t* out,
+    float* dbg_y_f32, int* status, void* stream);
+
+/* The whole expert forward: route, permute + amax + quantise (x read once),
+ * FC1 + SwiGLU + requantise, FC2 + router-weighted scatter, unpermute
+ * reduce.  Six launches on `stream`, no host synchronisation (capturable in
+ * a CUDA graph).
+ *   x       bf16 [T][d];  logits f32 [T][E]
+ *   w1_*, w2_* quantised weights as above
+ *   out     bf16 [T][d] (out)
+ *   ws      moe_expert_forward_workspace_bytes(...) bytes of device scratch;
+ *           the intermediates stay there (see ..._workspace_layout) */
+int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E,
+                       int k, int d, int d_ff, const uint8_t* w1_codes,
+                       const uint8_t* w1_sf, const float* w1_g,
+                       const uint8_t* w2_codes, const uint8_t* w2_sf,
+                       const float* w2_g, uint16_t* out, void* ws,
+                       size_t ws_bytes, int* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_NVFP4_H */

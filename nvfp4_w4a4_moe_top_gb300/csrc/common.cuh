@@ -1,0 +1,197 @@
+// Device helpers shared by the kernels of libmoe_nvfp4.so (sm_103a only).
+//
+// Codecs here are bit-level encoders of the NVFP4 element/scale formats
+// (E2M1 elements, E4M3 block scales: miniTE Technical Report section 2.2 and
+// section 5.1 equation).  They are written for the GPU from the format
+// definitions and share nothing with the CPU oracle; parity tests compare the
+// two over every float input.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda.h>
+#include <stdint.h>
+
+#include "../../include/moe_nvfp4.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------------------
+// scalar helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// FP32 -> BF16 bits, round to nearest even (hardware cvt.rn.bf16.f32).
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+// Two FP32 -> packed BF16x2 (lo in bits 0..15).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+}
+
+// E2M1 encoder, round to nearest with ties to the even code, saturating at 6.
+// The code of |q| is the number of decision boundaries it has crossed; at
+// 0.25, 1.25, 2.5 and 5 the tie stays on the lower (even) code, at 0.75,
+// 1.75 and 3.5 it moves up to the even code.  Sign bit = sign bit of q.
+__device__ __forceinline__ uint32_t e2m1_encode(float q) {
+  const float a = fabsf(q);
+  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) +
+               (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+  return c | ((__float_as_uint(q) >> 28) & 8u);
+}
+
+// E4M3 (OCP "FN") decoder for a non-negative scale byte 0x00..0x7E.
+__device__ __forceinline__ float e4m3_decode(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  if (e == 0) return (float)m * 0.001953125f;  // m * 2^-9
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// E4M3 encoder for t >= 0: round to nearest even, saturate at 448 (0x7E).
+// Below 2^-6 the grid is m * 2^-9 (m = 0..8), so the code is rint(t * 512);
+// above it, rounding the float's exponent+mantissa field to 3 mantissa bits
+// with an integer round-half-even carries into the exponent as needed, and
+// the biased exponents differ by 127 - 7.
+__device__ __forceinline__ uint32_t e4m3_encode(float t) {
+  if (!(t < 448.0f)) return 0x7Eu;  // also +inf (NaN is flagged by callers)
+  if (t < 0.015625f) return (uint32_t)__float2int_rn(t * 512.0f);
+  const uint32_t u = __float_as_uint(t);
+  const uint32_t r = (u + 0x7FFFFu + ((u >> 20) & 1u)) >> 20;
+  return r - (120u << 3);
+}
+
+// Byte offset of logical block scale (row, col) of a [rows][K/16] matrix in
+// the 128x4 tile layout (tiles row-group-major, 512 bytes each).
+__device__ __forceinline__ int64_t sf_tile_offset(int64_t row, int col, int kgroups) {
+  return ((row >> 7) * kgroups + (col >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (col & 3);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void set_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ bool is_finite_f32(float v) { return (__float_as_uint(v) & 0x7F800000u) != 0x7F800000u; }
+__device__ __forceinline__ bool bf16x2_finite(uint32_t p) {
+  return ((p & 0x7F80u) != 0x7F80u) && ((p & 0x7F800000u) != 0x7F800000u);
+}
+
+// ---------------------------------------------------------------------------
+// Quantise 8 consecutive BF16 values (one uint4) that form half of a
+// 16-element block whose other half sits in lane (lane ^ 1).  Returns the 8
+// packed E2M1 codes (4 bytes, even element in the low nibble) and the block
+// scale byte.  g and den = 6*g are the row's outer scale and its divisor.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t quant_half_block(const uint4 v, float g, float den,
+                                                     uint32_t* sb_out) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+  uint32_t sb = 0, packed = 0;
+  if (g != 0.0f) {
+    sb = e4m3_encode(__fdiv_rn(a, den));
+    const float S = __fmul_rn(g, e4m3_decode(sb));
+    if (S != 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c0 = e2m1_encode(__fdiv_rn(bf16_lo(w[i]), S));
+        const uint32_t c1 = e2m1_encode(__fdiv_rn(bf16_hi(w[i]), S));
+        packed |= (c0 | (c1 << 4)) << (8 * i);
+      }
+    }
+  }
+  *sb_out = sb;
+  return packed;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: mbarrier, TMA, tcgen05
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// 2D tiled TMA load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand staged by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;             // leading byte offset (unused when swizzled), 16 B
+  d |= (uint64_t)(1024u >> 4) << 32;   // stride byte offset: next 8-row group
+  d |= (uint64_t)1u << 46;             // descriptor version for tcgen05
+  d |= (uint64_t)2u << 61;             // 128-byte swizzle
+  return d;
+}
+// Descriptor of a 32-row x 16-byte block-scale tile (no swizzle, rows
+// contiguous, 8-row groups 128 bytes apart) for tcgen05.cp 32x128b.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  return d;
+}
+
+}  // namespace moe

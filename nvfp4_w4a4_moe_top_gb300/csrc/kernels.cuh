@@ -1,0 +1,80 @@
+// Host-side launch functions of the kernels (internal to libmoe_nvfp4.so).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kRouteChunk = 256;  // tokens per routing chunk (one CTA)
+
+int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,
+                         const float* amax, int64_t dst_rows, uint8_t* codes, uint8_t* sf, float* g,
+                         int* status, int nonfinite_bit, cudaStream_t stream);
+
+// Routing: top-k, weights, in-chunk ranks (into token_slot_row) and chunk
+// histograms hist[C][E].
+int launch_route(const float* logits, const int32_t* ext_ids, const float* ext_w, int T, int E, int k,
+                 int32_t* topk_ids, float* topk_w, int32_t* token_slot_row, int32_t* hist, int* status,
+                 cudaStream_t stream);
+
+// Chunk histograms -> exclusive chunk bases (in place), counts, padded offsets.
+int launch_scan(int32_t* hist, int C, int E, int32_t* counts, int32_t* offsets, cudaStream_t stream);
+
+// Final rows of the slots, row_to_token, and (when x != NULL) per-token amax
+// gathered in the same pass.
+int launch_permute_amax(const int32_t* topk_ids, int32_t* token_slot_row, const int32_t* hist, const int32_t* offsets,
+                        int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
+                        float* amax_row, int* status, cudaStream_t stream);
+
+// Pad rows of every group (and rows >= M_pad up to m_cap): row_to_token = -1,
+// amax_row = 0, and when codes != NULL zero codes / block scales / g.
+int launch_pad_rows(const int32_t* offsets, const int32_t* counts, int E, int64_t m_cap, int32_t* row_to_token,
+                    float* amax_row, uint8_t* codes, int K, uint8_t* sf, float* g, cudaStream_t stream);
+
+// Fused permute + amax + quantise of the forward: x read once, codes written
+// into the k destination rows of each token.
+int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const int32_t* hist, const int32_t* offsets,
+                         int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
+                         uint8_t* codes, uint8_t* sf, float* g, int* status, cudaStream_t stream);
+
+int launch_unpermute_reduce(const uint16_t* slots, int T, int k, int d, uint16_t* out, cudaStream_t stream);
+
+struct Fc1Args {
+  CUtensorMap tmap_a, tmap_b;
+  const uint8_t* a_sf;
+  const float* a_g;
+  const uint8_t* w_sf;
+  const float* w_g;
+  const int32_t* offsets;
+  int E, d, d_ff;
+  uint8_t* h_codes;
+  uint8_t* h_sf;
+  float* h_g;
+  float* dbg_u;
+  uint16_t* dbg_h;
+  uint16_t* scratch;
+  int* status;
+};
+struct Fc2Args {
+  CUtensorMap tmap_a, tmap_b;
+  const uint8_t* a_sf;
+  const float* a_g;
+  const uint8_t* w_sf;
+  const float* w_g;
+  const int32_t* offsets;
+  int E, d_ff, d, k;
+  const int32_t* row_to_token;
+  const int32_t* token_slot_row;
+  const float* topk_w;
+  uint16_t* slots;
+  float* dbg_y;
+  int* status;
+};
+
+int gemm_num_ctas();  // persistent grid size on the current device
+int launch_fc1(const Fc1Args& a, cudaStream_t stream);
+int launch_fc2(const Fc2Args& a, cudaStream_t stream);
+constexpr int kMaxGemmCtas = 256;
+
+}  // namespace moe

@@ -1,0 +1,415 @@
+// Routing, permutation, padding and expert offsets with per-token amax
+// gathered in the same pass (rainbus summary, prerequisites "MoE and grouped
+// GEMM": router top-k, permutation, padding, expert offsets, uneven and empty
+// groups; method step 6: sort fused with the amax scan, padding carries the
+// statistics, device-side expert offsets).
+//
+// The permutation is a deterministic stable counting sort with no
+// arrival-order atomics: per 256-token chunk, a bitmask per expert records
+// which tokens chose it (atomicOr is order-independent), a token's rank in
+// its expert is a popcount of the lower bits, chunk histograms are scanned
+// once, and a row is offsets[e] + chunk base + rank.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kChunk = kRouteChunk;
+
+__device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
+  return va > vb || (va == vb && ea < eb);
+}
+
+// One CTA per chunk of 256 tokens, one warp per token at a time.
+template <int NPL>
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits,
+                                                   const int32_t* __restrict__ ext_ids,
+                                                   const float* __restrict__ ext_w, int T, int E, int k,
+                                                   int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                                   int32_t* __restrict__ rank_out, int32_t* __restrict__ hist,
+                                                   int* status) {
+  extern __shared__ uint32_t mask[];  // [E][kChunk/32]
+  constexpr int W = kChunk / 32;
+  const int c = blockIdx.x;
+  const int t0 = c * kChunk;
+  for (int i = threadIdx.x; i < E * W; i += blockDim.x) mask[i] = 0u;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float NEG_INF = __uint_as_float(0xFF800000u);
+  for (int tl = warp; tl < kChunk; tl += blockDim.x / 32) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    int my_id = 0x7FFFFFFF;
+    float my_w = 0.0f;
+    if (logits) {
+      float v[NPL];
+      bool fin = true;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e = i * 32 + lane;
+        v[i] = NEG_INF;
+        if (e < E) {
+          const float x = __ldg(logits + (int64_t)t * E + e);
+          if (is_finite_f32(x)) v[i] = x; else fin = false;
+        }
+      }
+      if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, MOE_STATUS_NONFINITE_LOGITS);
+      uint32_t taken = 0u;
+      float my_v = NEG_INF, vmax = NEG_INF;
+      for (int j = 0; j < k; ++j) {
+        float bv = NEG_INF;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+          const int e = i * 32 + lane;
+          if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, be)) { bv = v[i]; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+          const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+          if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == j) { my_id = be; my_v = bv; }
+        if (j == 0) vmax = bv;
+      }
+      // softmax over the selected logits (FP32)
+      float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;
+      float den = ex;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+      my_w = (lane < k) ? __fdiv_rn(ex, den) : 0.0f;
+    } else {
+      // routing replay: ids must lie in [0, E) and be strictly ascending
+      if (lane < k) {
+        my_id = ext_ids[(int64_t)t * k + lane];
+        my_w = ext_w[(int64_t)t * k + lane];
+      }
+      const int prev = __shfl_up_sync(0xFFFFFFFFu, my_id, 1);
+      const bool bad = lane < k && (my_id < 0 || my_id >= E || (lane > 0 && prev >= my_id));
+      if (__any_sync(0xFFFFFFFFu, bad)) {
+        if (lane == 0) set_status(status, MOE_STATUS_BAD_ROUTING);
+        if (lane < k) my_id = min(max(my_id, 0), E - 1);  // stay in bounds
+      }
+    }
+    // slot order = ascending expert id
+    int pos = 0;
+    for (int i = 0; i < k; ++i) pos += (__shfl_sync(0xFFFFFFFFu, my_id, i) < my_id) ? 1 : 0;
+    if (lane < k) {
+      topk_ids[(int64_t)t * k + pos] = my_id;
+      topk_w[(int64_t)t * k + pos] = my_w;
+      atomicOr(&mask[my_id * W + (tl >> 5)], 1u << (tl & 31));
+    }
+  }
+  __syncthreads();
+  // in-chunk rank of each (token, slot): tokens of the chunk that chose the
+  // same expert and come earlier
+  for (int tl = threadIdx.x; tl < kChunk; tl += blockDim.x) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_ids[(int64_t)t * k + j];
+      int rank = __popc(mask[e * W + (tl >> 5)] & ((1u << (tl & 31)) - 1u));
+      for (int w = 0; w < (tl >> 5); ++w) rank += __popc(mask[e * W + w]);
+      rank_out[(int64_t)t * k + j] = rank;
+    }
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int h = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) h += __popc(mask[e * W + w]);
+    hist[(int64_t)c * E + e] = h;
+  }
+}
+
+int launch_route(const float* logits, const int32_t* ext_ids, const float* ext_w, int T, int E, int k,
+                 int32_t* topk_ids, float* topk_w, int32_t* token_slot_row, int32_t* hist, int* status,
+                 cudaStream_t stream) {
+  const int C = (T + kChunk - 1) / kChunk;
+  if (C == 0) return 0;
+  const size_t smem = (size_t)E * (kChunk / 32) * sizeof(uint32_t);
+  const int npl = (E + 31) / 32;
+#define MOE_ROUTE(N)                                                                                 \
+  route_kernel<N><<<C, 256, smem, stream>>>(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, \
+                                           token_slot_row, hist, status)
+  if (npl <= 1) MOE_ROUTE(1);
+  else if (npl <= 2) MOE_ROUTE(2);
+  else if (npl <= 4) MOE_ROUTE(4);
+  else if (npl <= 8) MOE_ROUTE(8);
+  else if (npl <= 16) MOE_ROUTE(16);
+  else MOE_ROUTE(32);
+#undef MOE_ROUTE
+  return 0;
+}
+
+// One CTA of 1024 threads: G = 1024/E threads per expert sum the expert's
+// chunk counts, write exclusive chunk bases in place, then a block scan of
+// the 128-padded counts gives the offsets.
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int C, int E,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int part[1024];
+  __shared__ int scan_a[1024], scan_b[1024];
+  const int G = max(1, 1024 / E);
+  const int e = threadIdx.x / G, gi = threadIdx.x % G;
+  const int per = (C + G - 1) / G;
+  const int c0 = min(C, gi * per), c1 = min(C, c0 + per);
+  int s = 0;
+  if (e < E)
+    for (int c = c0; c < c1; ++c) s += hist[(int64_t)c * E + e];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  if (e < E) {
+    int run = 0;
+    for (int g2 = 0; g2 < gi; ++g2) run += part[e * G + g2];
+    for (int c = c0; c < c1; ++c) {
+      const int h = hist[(int64_t)c * E + e];
+      hist[(int64_t)c * E + e] = run;
+      run += h;
+    }
+  }
+  // padded counts, inclusive scan over experts (Hillis-Steele)
+  const int x = threadIdx.x;
+  int tot = 0;
+  if (x < E) {
+    for (int g2 = 0; g2 < G; ++g2) tot += part[x * G + g2];
+    counts[x] = tot;
+  }
+  scan_a[x] = (x < E) ? ((tot + 127) & ~127) : 0;
+  __syncthreads();
+  int* in = scan_a;
+  int* out = scan_b;
+  for (int o = 1; o < 1024; o <<= 1) {
+    out[x] = in[x] + (x >= o ? in[x - o] : 0);
+    __syncthreads();
+    int* tmp = in; in = out; out = tmp;
+  }
+  if (x < E) offsets[x + 1] = in[x];
+  if (x == 0) offsets[0] = 0;
+}
+
+int launch_scan(int32_t* hist, int C, int E, int32_t* counts, int32_t* offsets, cudaStream_t stream) {
+  scan_kernel<<<1, 1024, 0, stream>>>(hist, C, E, counts, offsets);
+  return 0;
+}
+
+__device__ __forceinline__ int slot_row(int e, int t, int rank, const int32_t* __restrict__ hist,
+                                        const int32_t* __restrict__ offsets, int E) {
+  return offsets[e] + hist[(int64_t)(t / kChunk) * E + e] + rank;
+}
+
+// One warp per token: final rows of its slots, and per-token amax of x read
+// with 128-bit loads and a warp-shuffle max.
+__global__ void __launch_bounds__(256) permute_amax_kernel(
+    const int32_t* __restrict__ topk_ids, int32_t* __restrict__ tsr, const int32_t* __restrict__ hist,
+    const int32_t* __restrict__ offsets, int T, int E, int k, const uint16_t* __restrict__ x, int d,
+    int32_t* __restrict__ row_to_token, float* __restrict__ amax_tok, float* __restrict__ amax_row, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int row = -1;
+  if (lane < k) {
+    const int64_t i = (int64_t)t * k + lane;
+    row = slot_row(topk_ids[i], t, tsr[i], hist, offsets, E);
+    tsr[i] = row;
+    row_to_token[row] = t;
+  }
+  if (x) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
+    float a = 0.0f;
+    bool fin = true;
+    for (int i = lane; i < d / 8; i += 32) {
+      const uint4 v = __ldg(xr + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        fin = fin && bf16x2_finite(w[q]);
+        a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+      }
+    }
+    if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, MOE_STATUS_NONFINITE_X);
+    a = warp_max(a);
+    if (lane == 0 && amax_tok) amax_tok[t] = a;
+    if (lane < k && amax_row) amax_row[row] = a;
+  }
+}
+
+int launch_permute_amax(const int32_t* topk_ids, int32_t* token_slot_row, const int32_t* hist, const int32_t* offsets,
+                        int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
+                        float* amax_row, int* status, cudaStream_t stream) {
+  if (T == 0) return 0;
+  permute_amax_kernel<<<(T + 7) / 8, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d,
+                                                      row_to_token, amax_tok, amax_row, status);
+  return 0;
+}
+
+// Blocks [0, E): the pad rows of group e (fewer than 128); blocks >= E: rows
+// from the padded total up to m_cap (maps only; the GEMMs never read them).
+__global__ void __launch_bounds__(128) pad_rows_kernel(const int32_t* __restrict__ offsets,
+                                                       const int32_t* __restrict__ counts, int E, int64_t m_cap,
+                                                       int32_t* __restrict__ row_to_token, float* __restrict__ amax_row,
+                                                       uint8_t* __restrict__ codes, int K, uint8_t* __restrict__ sf,
+                                                       float* __restrict__ g) {
+  if ((int)blockIdx.x < E) {
+    const int e = blockIdx.x;
+    const int64_t r = (int64_t)offsets[e] + counts[e] + threadIdx.x;
+    if (r >= offsets[e + 1]) return;
+    row_to_token[r] = -1;
+    if (amax_row) amax_row[r] = 0.0f;
+    if (codes) {
+      uint4* cr = reinterpret_cast<uint4*>(codes + r * (K / 2));
+      for (int i = 0; i < K / 32; ++i) cr[i] = make_uint4(0u, 0u, 0u, 0u);
+      const int kg = K / 64;
+      for (int c4 = 0; c4 < kg; ++c4)
+        *reinterpret_cast<uint32_t*>(sf + ((r >> 7) * kg + c4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) = 0u;
+      g[r] = 0.0f;
+    }
+  } else {
+    const int64_t start = offsets[E];
+    for (int64_t r = start + (int64_t)(blockIdx.x - E) * blockDim.x + threadIdx.x; r < m_cap;
+         r += (int64_t)(gridDim.x - E) * blockDim.x) {
+      row_to_token[r] = -1;
+      if (amax_row) amax_row[r] = 0.0f;
+    }
+  }
+}
+
+int launch_pad_rows(const int32_t* offsets, const int32_t* counts, int E, int64_t m_cap, int32_t* row_to_token,
+                    float* amax_row, uint8_t* codes, int K, uint8_t* sf, float* g, cudaStream_t stream) {
+  pad_rows_kernel<<<E + 64, 128, 0, stream>>>(offsets, counts, E, m_cap, row_to_token, amax_row, codes, K, sf, g);
+  return 0;
+}
+
+// One warp per token: rows of its k slots, amax of x (read once into
+// registers), quantisation, and the same codes / block scales / outer scale
+// written into each of the k destination rows.
+template <int MAXCH>
+__global__ void __launch_bounds__(256) permute_quant_kernel(
+    const int32_t* __restrict__ topk_ids, int32_t* __restrict__ tsr, const int32_t* __restrict__ hist,
+    const int32_t* __restrict__ offsets, int T, int E, int k, const uint16_t* __restrict__ x, int d,
+    int32_t* __restrict__ row_to_token, float* __restrict__ amax_tok, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, float* __restrict__ gout, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int row = -1;
+  if (lane < k) {
+    const int64_t i = (int64_t)t * k + lane;
+    row = slot_row(topk_ids[i], t, tsr[i], hist, offsets, E);
+    tsr[i] = row;
+    row_to_token[row] = t;
+  }
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
+  const int n8 = d / 8;
+  uint4 v[MAXCH];
+  float a = 0.0f;
+  bool fin = true;
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int e8 = i * 32 + lane;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (e8 < n8) {
+      v[i] = __ldg(xr + e8);
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        fin = fin && bf16x2_finite(w[q]);
+        a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+      }
+    }
+  }
+  if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, MOE_STATUS_NONFINITE_X);
+  a = warp_max(a);
+  if (lane == 0 && amax_tok) amax_tok[t] = a;
+  const float g = __fdiv_rn(a, 2688.0f);
+  const float den = __fmul_rn(6.0f, g);
+  const int kg = d / 64;
+  uint32_t packed[MAXCH], sfw[MAXCH];
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    packed[i] = 0u;
+    sfw[i] = 0u;
+    if (i * 32 < n8) {
+      uint32_t sb;
+      packed[i] = quant_half_block(v[i], g, den, &sb);
+      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
+      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
+      sfw[i] = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+  }
+  for (int j = 0; j < k; ++j) {
+    const int64_t r = __shfl_sync(0xFFFFFFFFu, row, j);
+    uint32_t* crow = reinterpret_cast<uint32_t*>(codes + r * (d / 2));
+#pragma unroll
+    for (int i = 0; i < MAXCH; ++i) {
+      const int e8 = i * 32 + lane;
+      if (e8 < n8) {
+        crow[e8] = packed[i];
+        if ((lane & 7) == 0)
+          *reinterpret_cast<uint32_t*>(sf + ((r >> 7) * kg + (e8 >> 3)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) = sfw[i];
+      }
+    }
+    if (lane == 0) gout[r] = g;
+  }
+}
+
+int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const int32_t* hist, const int32_t* offsets,
+                         int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
+                         uint8_t* codes, uint8_t* sf, float* g, int* status, cudaStream_t stream) {
+  if (T == 0) return 0;
+  const int nch = (d / 8 + 31) / 32;
+  const dim3 grid((T + 7) / 8);
+  if (nch <= 4)
+    permute_quant_kernel<4><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d,
+                                                     row_to_token, amax_tok, codes, sf, g, status);
+  else if (nch <= 8)
+    permute_quant_kernel<8><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d,
+                                                     row_to_token, amax_tok, codes, sf, g, status);
+  else
+    permute_quant_kernel<16><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d,
+                                                      row_to_token, amax_tok, codes, sf, g, status);
+  return 0;
+}
+
+// out[t] = BF16(sum_j FP32(slots[t][j])), j ascending; 8 columns per thread.
+__global__ void __launch_bounds__(256) unpermute_reduce_kernel(const uint16_t* __restrict__ slots, int T, int k,
+                                                               int d, uint16_t* __restrict__ out) {
+  const int c8n = d / 8;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)T * c8n) return;
+  const int64_t t = idx / c8n;
+  const int c8 = (int)(idx - t * c8n);
+  const uint4* base = reinterpret_cast<const uint4*>(slots + t * k * (int64_t)d) + c8;
+  float s[8];
+  {
+    const uint4 v = __ldg(base);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) { s[2 * q] = bf16_lo(w[q]); s[2 * q + 1] = bf16_hi(w[q]); }
+  }
+  for (int j = 1; j < k; ++j) {
+    const uint4 v = __ldg(base + (int64_t)j * c8n);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      s[2 * q] = __fadd_rn(s[2 * q], bf16_lo(w[q]));
+      s[2 * q + 1] = __fadd_rn(s[2 * q + 1], bf16_hi(w[q]));
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(s[0], s[1]);
+  o.y = pack_bf16x2(s[2], s[3]);
+  o.z = pack_bf16x2(s[4], s[5]);
+  o.w = pack_bf16x2(s[6], s[7]);
+  reinterpret_cast<uint4*>(out + t * (int64_t)d)[c8] = o;
+}
+
+int launch_unpermute_reduce(const uint16_t* slots, int T, int k, int d, uint16_t* out, cudaStream_t stream) {
+  const int64_t n = (int64_t)T * (d / 8);
+  if (n == 0) return 0;
+  unpermute_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(slots, T, k, d, out);
+  return 0;
+}
+
+}  // namespace moe

@@ -1,0 +1,144 @@
+"""Parity of the tcgen05 grouped GEMMs with the oracle.
+
+Inputs come from the oracle (routing, permutation, quantised activations and
+weights).  Checks, per the specification's tolerance rules:
+  FC1: pre-cast FP32 outputs (dbg_u) within rel-L2 1e-5 of the oracle's
+       sequential-FP32 GEMM; h equal to the oracle SwiGLU of the GPU's u up
+       to rare 1-ulp BF16 flips; h codes / scales / g bit-exact with the
+       oracle's quantisation of the GPU's h.
+  FC2: pre-weighting expert outputs y2 (dbg_y) within rel-L2 1e-5 and BF16
+       max-abs 2e-3 of the oracle; slots bit-exact with the oracle's
+       weighting of the GPU's y2; out bit-exact with the oracle's reduce of
+       the GPU's slots.
+"""
+import numpy as np
+import pytest
+
+import nvfp4_w4a4_moe_top_gb300 as M
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from nvfp4_w4a4_moe_top_gb300 import build
+    build.build()
+
+
+def make_case(orc, lay, T=None):
+    x, lg, W1, W2 = lay.x(), lay.logits(), lay.w1(), lay.w2()
+    if T is not None:
+        x, lg = x[:T], lg[:T]
+    T = x.shape[0]
+    ids, w = orc.route(lg, lay.k)
+    perm = orc.permute(ids, lay.E)
+    am = orc.amax_rows(x)
+    mc = perm["m_cap"]
+    xq = orc.quantize_rows(x, perm["row_to_token"], am, mc)
+    return dict(T=T, x=x, ids=ids, w=w, perm=perm, xq=xq, mc=mc,
+                w1q=orc.quantize_weights(W1), w2q=orc.quantize_weights(W2))
+
+
+def run_fc1(lay, c):
+    import torch
+    from gpu_util import dev, host
+    mc, d, dff, E = c["mc"], lay.d, lay.d_ff, lay.E
+    hq = M.empty_quantized(mc, dff)
+    dbg_u = torch.full((mc, 2 * dff), float("nan"), dtype=torch.float32, device="cuda")
+    dbg_h = torch.zeros((mc, dff), dtype=torch.int16, device="cuda")
+    ws = torch.empty(M.fc1_workspace_bytes(dff), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    xc, xs, xg = c["xq"]
+    w1c, w1s, w1g = c["w1q"]
+    M.nvfp4_grouped_gemm_fc1_swiglu(dev(xc), dev(xs), dev(xg), dev(c["perm"]["offsets"]), E, mc, d, dff,
+                                    dev(w1c), dev(w1s), dev(w1g), hq["codes"], hq["sf"], hq["g"], dbg_u, dbg_h,
+                                    ws, st)
+    torch.cuda.synchronize()
+    return dict(status=int(st.item()), h_codes=host(hq["codes"]), h_sf=host(hq["sf"]), h_g=host(hq["g"]),
+                u=host(dbg_u), h=host(dbg_h, np.uint16))
+
+
+CASES = [("tiny", None), ("small", None), ("custom_d128", None), ("custom_skew", None)]
+
+
+def layer_of(name):
+    if name == "custom_d128":
+        return synth.custom(T=300, d=128, E=3, k=2, d_ff=256, seed=4)
+    if name == "custom_skew":
+        return synth.custom(T=700, d=384, E=16, k=3, d_ff=384, seed=5, logits="bias", bias_std=3.0,
+                            n_forced_empty=5)
+    return synth.layer(name)
+
+
+@pytest.mark.parametrize("name,T", CASES)
+def test_fc1_parity(orc, name, T):
+    from gpu_util import rel_l2
+    lay = layer_of(name)
+    c = make_case(orc, lay, T)
+    g = run_fc1(lay, c)
+    assert g["status"] == 0
+    mp = c["perm"]["m_pad"]
+    xc, xs, xg = c["xq"]
+    y1 = orc.grouped_gemm(xc, xs, xg, c["perm"]["offsets"], *c["w1q"], lay.d, 2 * lay.d_ff)
+    assert rel_l2(g["u"][:mp], y1[:mp]) <= 1e-5
+    # per-row: every row within 1e-5 relative (rows with a nonzero reference)
+    nr = np.linalg.norm(y1[:mp], axis=1)
+    rows = nr > 0
+    assert np.all(np.linalg.norm(g["u"][:mp] - y1[:mp], axis=1)[rows] <= 1e-5 * nr[rows])
+    # SwiGLU of the GPU's own FC1 output: equal up to rare one-ulp flips
+    _, h_ref = orc.swiglu(g["u"][:mp], lay.d_ff)
+    diff = g["h"][:mp].astype(np.int32) - h_ref.astype(np.int32)
+    assert np.abs(diff).max() <= 1
+    assert (diff != 0).mean() <= 2e-3
+    # requantisation of the GPU's h: bit-exact
+    hc, hs, hg = orc.quantize_rows(g["h"][:mp])
+    assert np.array_equal(g["h_codes"][:mp], hc)
+    assert np.array_equal(g["h_g"][:mp].view(np.uint32), hg.view(np.uint32))
+    assert np.array_equal(orc.unswizzle_sf(g["h_sf"], mp, lay.d_ff), orc.unswizzle_sf(hs, mp, lay.d_ff))
+    # pad rows come out as zero rows
+    pad = c["perm"]["row_to_token"][:mp] < 0
+    assert not g["h_codes"][:mp][pad].any() and not g["h_g"][:mp][pad].any()
+
+
+def run_fc2(lay, c, hq):
+    import torch
+    from gpu_util import dev, host
+    mc, d, dff, E, T, k = c["mc"], lay.d, lay.d_ff, lay.E, c["T"], lay.k
+    slots = torch.zeros((T, k, d), dtype=torch.int16, device="cuda")
+    out = torch.zeros((T, d), dtype=torch.int16, device="cuda")
+    dbg_y = torch.full((mc, d), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w2c, w2s, w2g = c["w2q"]
+    M.nvfp4_grouped_gemm_fc2_unpermute(dev(hq[0]), dev(hq[1]), dev(hq[2]), dev(c["perm"]["offsets"]), E, mc, dff,
+                                       d, dev(w2c), dev(w2s), dev(w2g), dev(c["perm"]["row_to_token"]),
+                                       dev(c["perm"]["token_slot_row"]), dev(c["w"]), T, k, slots, out, dbg_y, st)
+    torch.cuda.synchronize()
+    return dict(status=int(st.item()), slots=host(slots, np.uint16), out=host(out, np.uint16), y=host(dbg_y))
+
+
+@pytest.mark.parametrize("name,T", CASES)
+def test_fc2_parity(orc, name, T):
+    from gpu_util import rel_l2, f32_of_bf16
+    lay = layer_of(name)
+    c = make_case(orc, lay, T)
+    mp, mc = c["perm"]["m_pad"], c["mc"]
+    # FC2 operand: the oracle's own FC1 -> SwiGLU -> requantisation
+    xc, xs, xg = c["xq"]
+    y1 = orc.grouped_gemm(xc, xs, xg, c["perm"]["offsets"], *c["w1q"], lay.d, 2 * lay.d_ff)
+    _, h = orc.swiglu(y1, lay.d_ff)
+    hq = orc.quantize_rows(h)
+    g = run_fc2(lay, c, hq)
+    assert g["status"] == 0
+    y2 = orc.grouped_gemm(hq[0], hq[1], hq[2], c["perm"]["offsets"], *c["w2q"], lay.d_ff, lay.d)
+    real = c["perm"]["row_to_token"][:mp] >= 0
+    gy, ey = g["y"][:mp][real], y2[:mp][real]
+    assert rel_l2(gy, ey) <= 1e-5
+    from helpers import torch_bf16
+    assert np.abs(f32_of_bf16(torch_bf16(gy)) - f32_of_bf16(torch_bf16(ey))).max() <= 2e-3
+    # router-weighted BF16 scatter of the GPU's y2, and the reduce: bit-exact
+    y_full = np.zeros_like(y2)
+    y_full[:mp] = g["y"][:mp]
+    slots_ref = orc.combine(y_full, c["perm"], c["w"], c["T"], lay.k, lay.d)
+    assert np.array_equal(g["slots"], slots_ref)
+    assert np.array_equal(g["out"], orc.reduce(g["slots"]))

@@ -86,6 +86,57 @@ __device__ __forceinline__ bool bf16x2_finite(uint32_t p) {
   return ((p & 0x7F80u) != 0x7F80u) && ((p & 0x7F800000u) != 0x7F800000u);
 }
 
+// Eight FP32 -> eight E2M1 codes with the hardware conversion (nearest
+// even, saturating; element 0 in the low nibble).  Its equality with
+// e2m1_encode over every float is part of the codec parity test.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Codes of 8 BF16 values (4 packed words) for block scale S > 0:
+// c = Q_E2M1(RN(v / S)).  With R = RN(1/S), the products v*RN(R*(1-2^-21))
+// and v*RN(R*(1+2^-21)) bracket RN(v/S): each is within 3*2^-24 (relative)
+// of v*R*(1 -+ 2^-21), which is within 2^-24 of v/S, while RN(v/S) is within
+// 2^-24 of v/S.  The encoder is monotone, so when both brackets give the same
+// codes those are the codes of RN(v/S).  Otherwise (a quotient within about
+// 2^-21 of a rounding boundary, e.g. an exact tie) the codes are recomputed
+// from the correctly rounded division.  Quotients far below 0.25 encode to
+// zero on both sides, so subnormal products do not break the argument.
+__device__ __forceinline__ uint32_t e2m1_codes8(const uint32_t (&w)[4], float S) {
+  if (S >= 7.52316384526264e-37f) {  // 2^-120: R and the products stay finite
+    const float R = __frcp_rn(S);
+    const float Rl = __fmul_rn(R, 0.99999952316284180f);  // 1 - 2^-21
+    const float Rh = __fmul_rn(R, 1.00000047683715820f);  // 1 + 2^-21
+    float l[8], h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float v0 = bf16_lo(w[i]), v1 = bf16_hi(w[i]);
+      l[2 * i] = __fmul_rn(v0, Rl);
+      l[2 * i + 1] = __fmul_rn(v1, Rl);
+      h[2 * i] = __fmul_rn(v0, Rh);
+      h[2 * i + 1] = __fmul_rn(v1, Rh);
+    }
+    const uint32_t cl = e2m1x8(l);
+    if (cl == e2m1x8(h)) return cl;
+  }
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    q[2 * i] = __fdiv_rn(bf16_lo(w[i]), S);
+    q[2 * i + 1] = __fdiv_rn(bf16_hi(w[i]), S);
+  }
+  return e2m1x8(q);
+}
+
 // ---------------------------------------------------------------------------
 // Quantise 8 consecutive BF16 values (one uint4) that form half of a
 // 16-element block whose other half sits in lane (lane ^ 1).  Returns the 8
@@ -95,22 +146,16 @@ __device__ __forceinline__ bool bf16x2_finite(uint32_t p) {
 __device__ __forceinline__ uint32_t quant_half_block(const uint4 v, float g, float den,
                                                      uint32_t* sb_out) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float a = 0.0f;
+  uint32_t m = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  for (int i = 0; i < 4; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  float a = __uint_as_float(__vmaxu2(m, m >> 16) << 16);
   a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
   uint32_t sb = 0, packed = 0;
   if (g != 0.0f) {
     sb = e4m3_encode(__fdiv_rn(a, den));
     const float S = __fmul_rn(g, e4m3_decode(sb));
-    if (S != 0.0f) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t c0 = e2m1_encode(__fdiv_rn(bf16_lo(w[i]), S));
-        const uint32_t c1 = e2m1_encode(__fdiv_rn(bf16_hi(w[i]), S));
-        packed |= (c0 | (c1 << 4)) << (8 * i);
-      }
-    }
+    if (S != 0.0f) packed = e2m1_codes8(w, S);
   }
   *sb_out = sb;
   return packed;

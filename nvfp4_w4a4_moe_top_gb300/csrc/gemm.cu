@@ -4,29 +4,39 @@
 // AI summary methodology: outer factors applied in FP32 after the native
 // block-scaled multiply, no decoded BF16 operand).
 //
-// Design (one persistent CTA per SM, 10 warps):
-//   warp 8   TMA producer: A and B tiles (128 rows x 128 bytes = 256 FP4 of
-//            K, 128-byte swizzle) by cp.async.bulk.tensor, their block-scale
-//            tiles (4 x 512 bytes) by cp.async.bulk, into a 5-stage ring.
-//   warp 9   MMA issuer: copies block scales to tensor memory (tcgen05.cp
-//            32x128b.warpx4) and issues tcgen05.mma kind::mxf4nvf4
-//            block_scale.scale_vec::4X (M=128, N=128, K=64, UE4M3 scale per
-//            16 elements) into one of three 128-column FP32 accumulators.
-//   warps 0-7 epilogue: tcgen05.ld of the accumulator (warp w reads lanes
-//            32*(w%4).. and half (w/4) of the columns).
-// Group boundaries are the device-side offsets (multiples of 128 rows), so
-// every 128-row tile belongs to one expert; empty experts own no tile.
+// Design (one persistent CTA per SM, 16 warps):
+//   warps 12-14  TMA producers.  A work unit is one 128-row tile of the
+//            routed rows (one expert).  Its A operand (128 rows x K FP4,
+//            128-byte swizzle) is loaded once into resident shared memory, one
+//            slice per 256 elements of K; the B operand (128 weight rows x 256
+//            elements of K) and the block-scale tiles of both operands stream
+//            through three rings of stages, one ring per producer warp, the
+//            k-steps dealt round-robin over the rings.  When K does not fit,
+//            A streams through the stages too.
+//   warps 8-11  block-scale writers, one per tensor-memory lane quadrant.
+//            For each stage they move the scale tiles from shared to tensor
+//            memory with tcgen05.st: the B scales replicated in every
+//            quadrant (each quadrant of the tensor core reads all of them),
+//            the A scales only on the diagonal (row r is read from lane r,
+//            column base + r/32), and signal the stage's scales as ready.
+//   warp 15  MMA issuer: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X
+//            (M=128, N=128, K=64, UE4M3 scale per 16 elements) into one of
+//            three 128-column FP32 accumulators; nothing else goes through
+//            the tensor pipe.
+//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and
+//            half (w/4) of the accumulator's columns, releases the
+//            accumulator, then does the FP32 epilogue from registers.  The
+//            expert's per-column outer scales are staged in shared memory per
+//            unit.
 //
-//   FC1: a work unit is one 128-row tile of the routed activations; it runs
-//        over d_ff/128 chunks, each a gate tile (W1 rows c*128..) and an up
-//        tile (rows d_ff + c*128..).  The epilogue forms u = BF16(y),
-//        h = BF16(silu(gate) * up), stages h in a per-CTA scratch and keeps
-//        each row's running amax; after the last chunk it requantises the
-//        row (g_h = amax/2688, E4M3 block scales, E2M1 codes) into the FC2
-//        operand buffers.
-//   FC2: a work unit is one 128 x 128 output tile; the epilogue forms
-//        y2 = acc * (g_h * g_w2), z = BF16(w_{t,e} * y2) and writes it to
-//        slot (t, j) of the token.
+//   FC1: the items of a unit are, per 128-column chunk c of h, a gate tile
+//        (W1 rows c*128..) then an up tile (rows d_ff + c*128..).  The
+//        epilogue forms u = BF16(acc * (g_x * g_w)), h = BF16(silu(gate) * up),
+//        stages h in a per-CTA scratch (L2-resident) and keeps each row's
+//        running amax; after the last chunk it requantises the row
+//        (g_h = amax/2688, E4M3 block scales, E2M1 codes).
+//   FC2: the items of a unit are the d/128 output tiles; the epilogue forms
+//        y2 = acc * (g_h * g_w2), z = BF16(w_{t,e} * y2) and writes slot (t, j).
 //
 // Every wait is bounded (a few seconds of wall clock); on expiry the kernel
 // raises MOE_STATUS_TIMEOUT, drains its own copies and MMAs, frees tensor
@@ -39,43 +49,55 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK_BYTES = 128;
-constexpr int NST = 5;
-constexpr int A_BYTES = BM * BK_BYTES;
-constexpr int B_BYTES = BN * BK_BYTES;
-constexpr int SF_STAGE = 4 * 512;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_STAGE;  // 36 KB, a multiple of 1024
-constexpr int NSLOT = 3;
+constexpr int A_SLICE = BM * BK_BYTES;                 // 16 KB
+constexpr int B_BYTES = BN * BK_BYTES;                 // 16 KB
+constexpr int SF_STAGE = 4 * 512;                      // 2 KB per operand
+constexpr int B_STAGE = B_BYTES + 2 * SF_STAGE;        // 20 KB: B, SFB, SFA
+constexpr int MAX_A_SLOTS = 16;
+constexpr int MAX_STAGES = 4;                          // over all rings (one TMEM scale buffer each)
+constexpr int NPROD = 3;                               // producer warps (rings)
+constexpr int NSLOT = 3;                               // accumulators
 constexpr int TMEM_COLS = 512;
-constexpr int SF_TMEM_COL = NSLOT * BN;  // two 32-column buffers: [SFA 16 | SFB 16]
+constexpr int SF_TMEM_COL = NSLOT * BN;                // per stage: [A scales 16 | B scales 16]
 constexpr int NEPI_WARPS = 8;
-constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
-constexpr int NTHREADS = 320;
-constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
+constexpr int NEPI_THREADS = NEPI_WARPS * 32;
+constexpr int SFW_WARP = 8;                            // scale writers 8..11
+constexpr int PRODUCER_WARP = 12, MMA_WARP = PRODUCER_WARP + NPROD;
+constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
 
 // Instruction descriptor: E2M1 x E2M1, UE4M3 scales, both operands K-major,
 // N = 128 (bits 17-22 hold N/8), M = 128 (bits 24-28 hold M/16).
 constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 struct Tail {
-  uint64_t full[NST];
-  uint64_t empty[NST];
+  uint64_t a_full[MAX_A_SLOTS];
+  uint64_t a_empty[MAX_A_SLOTS];
+  uint64_t b_full[MAX_STAGES];
+  uint64_t b_empty[MAX_STAGES];
+  uint64_t sf_full[MAX_STAGES];
   uint64_t tfull[NSLOT];
   uint64_t tempty[NSLOT];
-  uint64_t sffree[2];
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
   float rowmax[2][BM];
-  int offsets[1025];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)NST * STAGE_BYTES + sizeof(Tail);
+constexpr size_t TAIL_BYTES = (sizeof(Tail) + 1023) / 1024 * 1024;
 
+// Poll the barrier; the abort flag and the wall clock are consulted only
+// every 256 failed polls, so a short wait costs nothing but the polls.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
       *abort_flag = 1;
@@ -88,9 +110,6 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -99,188 +118,261 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
       "l"(a), "l"(b), "r"(IDESC), "r"(acc), "r"(sfa), "r"(sfb)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
 
 // Expert owning 128-row tile mt: the last e with offsets[e] <= mt*128.
-__device__ __forceinline__ int expert_of(const int* off, int E, int mt) {
+__device__ __forceinline__ int expert_of(const int32_t* off, int E, int mt) {
   const int row0 = mt * BM;
-  int lo = 0, hi = E;  // first e' in [0, E] with off[e'] > row0, minus one
+  int lo = 0, hi = E;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (off[mid] <= row0) lo = mid + 1; else hi = mid;
+    if (__ldg(off + mid) <= row0) lo = mid + 1; else hi = mid;
   }
   return lo - 1;
 }
 
-struct Mainloop {
-  const CUtensorMap* tmap_a;
-  const CUtensorMap* tmap_b;
-  const uint8_t* a_sf;
-  const uint8_t* b_sf;
-  int kgroups;  // K / 64
-  int nk;       // k-steps of 256 elements
-};
-
-// Sequence of accumulator tiles of this CTA.  FC1: per 128-row unit, chunks
-// c = 0..nch-1, each a gate item then an up item.  FC2: one item per
-// (m-tile, n-tile) unit.
-struct Schedule {
-  bool fc1;
-  int E, num_mt, nch, ntn, N, d_ff;
-  __device__ int units() const { return fc1 ? num_mt : num_mt * ntn; }
-  __device__ int items(int) const { return fc1 ? 2 * nch : 1; }
-  __device__ int mtile(int u) const { return fc1 ? u : u / ntn; }
-  __device__ int brow(int u, int e, int q) const {
-    if (fc1) return e * N + (q & 1) * d_ff + (q >> 1) * BN;
-    return e * N + (u % ntn) * BN;
+struct Geometry {
+  int num_mt;      // 128-row units
+  int items;       // accumulator tiles per unit
+  int nk;          // k-steps of 256 elements
+  int kgroups;     // K / 64 (block-scale 4-column groups)
+  int rings;       // producer warps, each owning a ring of stages
+  int stages;      // stages per ring
+  int stage_bytes; // [A slice when streamed][B][SFB][SFA]
+  bool resident;   // A slices loaded once per unit into their own slots
+  __device__ uint32_t b_off() const { return resident ? 0u : (uint32_t)A_SLICE; }
+  // ring slot of CTA-local k-step kc and the use count of that slot
+  __device__ void slot_of(uint32_t kc, uint32_t& slot, uint32_t& use) const {
+    const uint32_t r = kc % (uint32_t)rings, pos = kc / (uint32_t)rings;
+    slot = r * (uint32_t)stages + pos % (uint32_t)stages;
+    use = pos / (uint32_t)stages;
   }
 };
 
-__device__ void producer_loop(const Mainloop& ml, const Schedule& sc, const int* off, uint8_t* stages, Tail* tl,
-                              volatile int* abort_flag, int* status) {
-  const uint32_t base = smem_u32(stages);
+// Weight row of item q of a unit of expert e.
+struct ItemRows {
+  bool fc1;
+  int N, d_ff;
+  __device__ int operator()(int e, int q) const {
+    if (fc1) return e * N + (q & 1) * d_ff + (q >> 1) * BN;
+    return e * N + q * BN;
+  }
+};
+
+// Producer r of R.  The CTA's k-steps (over units, items, K) are numbered
+// kc = 0, 1, ...; k-step kc travels through ring kc % R, position kc / R.
+// Each ring has one producer and is consumed in order, so every barrier sees
+// its phases in order.  A producer runs at most R*S k-steps ahead of the
+// consumers, fewer than the k-steps of one unit, so the resident A slots
+// (loaded at the first item of a unit by whichever producer owns that
+// k-step) never see a phase ahead of the one they wait for.
+__device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const uint8_t* a_sf,
+                              const uint8_t* b_sf, const Geometry& G, const ItemRows& rows, const int32_t* off, int E,
+                              uint32_t a_base, uint32_t ring_base, Tail* tl, volatile int* abort_flag, int* status) {
+  const uint32_t b_off = G.b_off();
   uint32_t kc = 0;
-  uint32_t issued_use[NST];
-  for (int s = 0; s < NST; ++s) issued_use[s] = 0xFFFFFFFFu;
+  uint32_t last_stage_use[MAX_STAGES], last_a_use[MAX_A_SLOTS];
+  for (int i = 0; i < MAX_STAGES; ++i) last_stage_use[i] = 0xFFFFFFFFu;
+  for (int i = 0; i < MAX_A_SLOTS; ++i) last_a_use[i] = 0xFFFFFFFFu;
   bool aborted = false;
-  for (int u = blockIdx.x; u < sc.units() && !aborted; u += gridDim.x) {
-    const int mt = sc.mtile(u);
-    const int e = expert_of(off, sc.E, mt);
-    const int nq = sc.items(u);
-    for (int q = 0; q < nq && !aborted; ++q) {
-      const int br = sc.brow(u, e, q);
-      for (int ks = 0; ks < ml.nk; ++ks, ++kc) {
-        const uint32_t s = kc % NST, use = kc / NST;
-        if (!wait_bounded(smem_u32(&tl->empty[s]), (use & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
-        const int nsf = min(4, ml.kgroups - 4 * ks);
-        const uint32_t st = base + s * STAGE_BYTES;
-        const uint32_t fb = smem_u32(&tl->full[s]);
-        mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + 2 * nsf * 512);
-        tma_load_2d(st, ml.tmap_a, ks * BK_BYTES, mt * BM, fb);
-        tma_load_2d(st + A_BYTES, ml.tmap_b, ks * BK_BYTES, br, fb);
-        bulk_load(st + A_BYTES + B_BYTES, ml.a_sf + ((int64_t)mt * ml.kgroups + 4 * ks) * 512, nsf * 512, fb);
-        bulk_load(st + A_BYTES + B_BYTES + SF_STAGE, ml.b_sf + ((int64_t)(br / BM) * ml.kgroups + 4 * ks) * 512,
-                  nsf * 512, fb);
-        issued_use[s] = use;
+  for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
+    const int e = expert_of(off, E, u);
+    const uint32_t unit_use = (uint32_t)((u - (int)blockIdx.x) / (int)gridDim.x);
+    const int64_t sfa_row = (int64_t)u * G.kgroups;
+    for (int q = 0; q < G.items && !aborted; ++q) {
+      const int br = rows(e, q);
+      const int64_t sfb_row = (int64_t)(br / BM) * G.kgroups;
+      for (int ks = 0; ks < G.nk; ++ks, ++kc) {
+        if (kc % (uint32_t)G.rings != (uint32_t)r) continue;
+        uint32_t slot, use;
+        G.slot_of(kc, slot, use);
+        if (!wait_bounded(smem_u32(&tl->b_empty[slot]), (use & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
+        const int nsf = min(4, G.kgroups - 4 * ks);
+        const uint32_t st = ring_base + slot * G.stage_bytes;
+        const uint32_t fb = smem_u32(&tl->b_full[slot]);
+        if (G.resident && q == 0) {
+          if (!wait_bounded(smem_u32(&tl->a_empty[ks]), (unit_use & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
+          const uint32_t ab = smem_u32(&tl->a_full[ks]);
+          mbar_arrive_expect_tx(ab, A_SLICE);
+          tma_load_2d(a_base + ks * A_SLICE, tmap_a, ks * BK_BYTES, u * BM, ab);
+          last_a_use[ks] = unit_use;
+        }
+        mbar_arrive_expect_tx(fb, B_BYTES + 2 * nsf * 512 + b_off);
+        if (!G.resident) tma_load_2d(st, tmap_a, ks * BK_BYTES, u * BM, fb);
+        tma_load_2d(st + b_off, tmap_b, ks * BK_BYTES, br, fb);
+        bulk_load(st + b_off + B_BYTES, b_sf + (sfb_row + 4 * ks) * 512, nsf * 512, fb);
+        bulk_load(st + b_off + B_BYTES + SF_STAGE, a_sf + (sfa_row + 4 * ks) * 512, nsf * 512, fb);
+        last_stage_use[slot] = use;
       }
     }
   }
   if (aborted) {
-    // let the copies already issued land before the CTA can exit
-    for (int s = 0; s < NST; ++s)
-      if (issued_use[s] != 0xFFFFFFFFu) {
+    // let the copies this thread issued land before the CTA can exit
+    for (int s = 0; s < MAX_STAGES; ++s)
+      if (last_stage_use[s] != 0xFFFFFFFFu) {
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(smem_u32(&tl->full[s]), issued_use[s] & 1u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
+        while (!mbar_try_wait(smem_u32(&tl->b_full[s]), last_stage_use[s] & 1u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
+        }
+      }
+    for (int ks = 0; ks < MAX_A_SLOTS; ++ks)
+      if (last_a_use[ks] != 0xFFFFFFFFu) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(smem_u32(&tl->a_full[ks]), last_a_use[ks] & 1u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
         }
       }
   }
 }
 
-__device__ void mma_loop(const Mainloop& ml, const Schedule& sc, const int* off, uint8_t* stages, Tail* tl,
-                         uint32_t tmem, volatile int* abort_flag, int* status) {
-  const uint32_t base = smem_u32(stages);
-  uint32_t kc = 0, it = 0;
+// Scale writer for lane quadrant qd (warp 8 + qd).  Per k-step, once the
+// stage has landed: lane l (row or weight row 32*qd + l) stores
+//   - the B scales of the four 64-wide K groups, replicated: columns
+//     B0 + 4i + j hold bytes [16*l + 4j, +4) of B-scale tile i, exactly as
+//     a 32x128b.warpx4 copy of the tile would place them in every quadrant;
+//   - the A scales on the diagonal only: column A0 + 4i + qd holds the four
+//     scale bytes of row 32*qd + l in A-scale tile i (bytes 16*l + 4*qd).
+// The stage's buffer is rewritten only after its next use has landed, which
+// the producer issues only after the MMAs of the previous use completed.
+__device__ void sf_writer_loop(int qd, const Geometry& G, uint32_t ring_base, Tail* tl, uint32_t tmem,
+                               volatile int* abort_flag, int* status) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t b_off = G.b_off();
+  const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16);
+  uint32_t kc = 0;
   bool aborted = false;
-  for (int u = blockIdx.x; u < sc.units() && !aborted; u += gridDim.x) {
-    const int nq = sc.items(u);
-    for (int q = 0; q < nq && !aborted; ++q, ++it) {
-      const uint32_t slot = it % NSLOT, suse = it / NSLOT;
-      if (!wait_bounded(smem_u32(&tl->tempty[slot]), (suse & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
-      tc_fence_after();
-      const uint32_t dacc = tmem + slot * BN;
-      for (int ks = 0; ks < ml.nk; ++ks, ++kc) {
-        const uint32_t s = kc % NST, use = kc / NST;
-        if (!wait_bounded(smem_u32(&tl->full[s]), use & 1u, abort_flag, status)) { aborted = true; break; }
-        const uint32_t sfb = kc & 1u;
-        if (kc >= 2 && !wait_bounded(smem_u32(&tl->sffree[sfb]), ((kc >> 1) - 1u) & 1u, abort_flag, status)) {
-          aborted = true;
-          break;
-        }
+  for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
+    for (int q = 0; q < G.items && !aborted; ++q) {
+      for (int ks = 0; ks < G.nk; ++ks, ++kc) {
+        uint32_t slot, use;
+        G.slot_of(kc, slot, use);
+        bool ok = wait_bounded(smem_u32(&tl->b_full[slot]), use & 1u, abort_flag, status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
         tc_fence_after();
-        const int nmma = min(4, ml.kgroups - 4 * ks);
-        const uint32_t st = base + s * STAGE_BYTES;
-        const uint32_t sf_a = tmem + SF_TMEM_COL + sfb * 32;
-        const uint32_t sf_b = sf_a + 16;
-        for (int i = 0; i < nmma; ++i) {
-          tc_cp_sf(sf_a + 4 * i, sdesc_sf(st + A_BYTES + B_BYTES + 512 * i));
-          tc_cp_sf(sf_b + 4 * i, sdesc_sf(st + A_BYTES + B_BYTES + SF_STAGE + 512 * i));
+        const int nsf = min(4, G.kgroups - 4 * ks);
+        const uint32_t sfb_s = ring_base + slot * G.stage_bytes + b_off + B_BYTES;
+        const uint32_t sfa_s = sfb_s + SF_STAGE;
+        uint32_t wb[16], wa[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          wa[i] = 0u;
+          if (i < nsf) {
+            v = lds128(sfb_s + 512 * i + 16 * lane);
+            wa[i] = lds32(sfa_s + 512 * i + 16 * lane + 4 * qd);
+          }
+          wb[4 * i] = v.x; wb[4 * i + 1] = v.y; wb[4 * i + 2] = v.z; wb[4 * i + 3] = v.w;
         }
-        const uint64_t adesc = sdesc_k_sw128(st);
-        const uint64_t bdesc = sdesc_k_sw128(st + A_BYTES);
-        for (int i = 0; i < nmma; ++i)
-          tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
-        tc_commit(smem_u32(&tl->empty[s]));
-        tc_commit(smem_u32(&tl->sffree[sfb]));
+        const uint32_t col = tq + SF_TMEM_COL + slot * 32;
+        tmem_st16(col + 16, wb);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_st1(col + 4 * i + qd, wa[i]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tl->sf_full[slot]));
       }
-      if (!aborted) tc_commit(smem_u32(&tl->tfull[slot]));
     }
   }
-  // all MMAs and scale copies of this CTA have completed once `done` fires
+}
+
+__device__ void mma_loop(const Geometry& G, uint32_t a_base, uint32_t ring_base, Tail* tl, uint32_t tmem,
+                         volatile int* abort_flag, int* status) {
+  const uint32_t b_off = G.b_off();
+  uint32_t kc = 0, it = 0;
+  bool aborted = false;
+  for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
+    const uint32_t unit_use = (uint32_t)((u - (int)blockIdx.x) / (int)gridDim.x);
+    for (int q = 0; q < G.items && !aborted; ++q, ++it) {
+      const uint32_t acc_slot = it % NSLOT, suse = it / NSLOT;
+      if (!wait_bounded(smem_u32(&tl->tempty[acc_slot]), (suse & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t dacc = tmem + acc_slot * BN;
+      for (int ks = 0; ks < G.nk; ++ks, ++kc) {
+        uint32_t slot, use;
+        G.slot_of(kc, slot, use);
+        if (!wait_bounded(smem_u32(&tl->b_full[slot]), use & 1u, abort_flag, status)) { aborted = true; break; }
+        if (!wait_bounded(smem_u32(&tl->sf_full[slot]), use & 1u, abort_flag, status)) { aborted = true; break; }
+        if (G.resident && q == 0 &&
+            !wait_bounded(smem_u32(&tl->a_full[ks]), unit_use & 1u, abort_flag, status)) { aborted = true; break; }
+        tc_fence_after();
+        const int nmma = min(4, G.kgroups - 4 * ks);
+        const uint32_t st = ring_base + slot * G.stage_bytes;
+        const uint32_t sf_a = tmem + SF_TMEM_COL + slot * 32;
+        const uint32_t sf_b = sf_a + 16;
+        const uint64_t adesc = sdesc_k_sw128(G.resident ? a_base + ks * A_SLICE : st);
+        const uint64_t bdesc = sdesc_k_sw128(st + b_off);
+        if (nmma == 4) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
+        } else {
+          for (int i = 0; i < nmma; ++i)
+            tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&tl->b_empty[slot]));
+        if (G.resident && q == G.items - 1) tc_commit(smem_u32(&tl->a_empty[ks]));
+      }
+      if (!aborted) tc_commit(smem_u32(&tl->tfull[acc_slot]));
+    }
+  }
+  // all MMAs of this CTA have completed once `done` fires
   tc_commit(smem_u32(&tl->done));
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(smem_u32(&tl->done), 0u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
   }
 }
 
-// Quantise 16 BF16 values held by one thread (one block): packed codes in
-// 8 bytes (even element in the low nibble) and the block-scale byte.
-__device__ __forceinline__ uint2 quant_block16(const uint32_t (&w)[8], float g, float den, uint32_t* sb_out) {
-  float a = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-  uint32_t sb = 0;
-  uint2 p = make_uint2(0u, 0u);
-  if (g != 0.0f) {
-    sb = e4m3_encode(__fdiv_rn(a, den));
-    const float S = __fmul_rn(g, e4m3_decode(sb));
-    if (S != 0.0f) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t c0 = e2m1_encode(__fdiv_rn(bf16_lo(w[i]), S));
-        const uint32_t c1 = e2m1_encode(__fdiv_rn(bf16_hi(w[i]), S));
-        const uint32_t byte = c0 | (c1 << 4);
-        if (i < 4) p.x |= byte << (8 * i); else p.y |= byte << (8 * (i - 4));
-      }
-    }
-  }
-  *sb_out = sb;
-  return p;
-}
-
-// Common prologue: barriers, tensor memory, offsets.  Returns the base of
-// the 1024-aligned stage ring.
-__device__ __forceinline__ uint8_t* setup(uint8_t* smem_raw, Tail*& tl, const int32_t* offsets, int E) {
-  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  tl = reinterpret_cast<Tail*>(stages + (size_t)NST * STAGE_BYTES);
+// Prologue: barriers and tensor memory.
+__device__ __forceinline__ Tail* setup(uint8_t* tail_ptr) {
+  Tail* tl = reinterpret_cast<Tail*>(tail_ptr);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(smem_u32(&tl->full[s]), 1);
-      mbar_init(smem_u32(&tl->empty[s]), 1);
+    for (int s = 0; s < MAX_A_SLOTS; ++s) {
+      mbar_init(smem_u32(&tl->a_full[s]), 1);
+      mbar_init(smem_u32(&tl->a_empty[s]), 1);
+    }
+    for (int s = 0; s < MAX_STAGES; ++s) {
+      mbar_init(smem_u32(&tl->b_full[s]), 1);
+      mbar_init(smem_u32(&tl->b_empty[s]), 1);
+      mbar_init(smem_u32(&tl->sf_full[s]), 4);
     }
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(smem_u32(&tl->tfull[s]), 1);
       mbar_init(smem_u32(&tl->tempty[s]), NEPI_WARPS);
     }
-    mbar_init(smem_u32(&tl->sffree[0]), 1);
-    mbar_init(smem_u32(&tl->sffree[1]), 1);
     mbar_init(smem_u32(&tl->done), 1);
     tl->abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) tl->offsets[i] = offsets[i];
   if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
                  "r"(TMEM_COLS)
@@ -290,7 +382,7 @@ __device__ __forceinline__ uint8_t* setup(uint8_t* smem_raw, Tail*& tl, const in
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  return stages;
+  return tl;
 }
 
 __device__ __forceinline__ void teardown(Tail* tl) {
@@ -303,55 +395,125 @@ __device__ __forceinline__ void teardown(Tail* tl) {
   }
 }
 
+// ---- approximate transcendentals for SiLU ----
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two FP32 -> BF16x2 (lo = first argument), round to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Codes of 16 BF16 values (8 packed words) for block scale S > 0.
+__device__ __forceinline__ uint2 e2m1_block16(const uint32_t (&w)[8], float S) {
+  const uint32_t w0[4] = {w[0], w[1], w[2], w[3]}, w1[4] = {w[4], w[5], w[6], w[7]};
+  return make_uint2(e2m1_codes8(w0, S), e2m1_codes8(w1, S));
+}
+
+// Largest BF16 magnitude of 16 values (8 packed words), as a float.
+__device__ __forceinline__ float amax16_bf16(const uint32_t (&w)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  return __uint_as_float(__vmaxu2(m, m >> 16) << 16);
+}
+
+// Stage n floats (n % 4 == 0) from global into shared memory with the
+// epilogue threads.
+__device__ __forceinline__ void stage_scales(float* dst, const float* src, int n, int tid) {
+  for (int i = tid; i < n / 4; i += NEPI_THREADS)
+    reinterpret_cast<float4*>(dst)[i] = __ldg(reinterpret_cast<const float4*>(src) + i);
+}
+
+// Shared roles of both GEMMs.  Returns true for the epilogue warps, which
+// the caller then runs.
+__device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b,
+                                                   const uint8_t* a_sf, const uint8_t* b_sf, const Geometry& G,
+                                                   const ItemRows& rows, const int32_t* off, int E, uint32_t a_base,
+                                                   uint32_t ring_base, Tail* tl, int* status) {
+  volatile int* abort_flag = &tl->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= PRODUCER_WARP && warp < MMA_WARP) {
+    if (lane == 0) {
+      prefetch_tmap(tmap_a);
+      prefetch_tmap(tmap_b);
+      producer_loop(warp - PRODUCER_WARP, tmap_a, tmap_b, a_sf, b_sf, G, rows, off, E, a_base, ring_base, tl,
+                    abort_flag, status);
+    }
+    __syncwarp();
+    return false;
+  }
+  if (warp == MMA_WARP) {
+    if (lane == 0) mma_loop(G, a_base, ring_base, tl, tl->tmem_base, abort_flag, status);
+    __syncwarp();
+    return false;
+  }
+  if (warp >= SFW_WARP && warp < SFW_WARP + 4) {
+    sf_writer_loop(warp - SFW_WARP, G, ring_base, tl, tl->tmem_base, abort_flag, status);
+    return false;
+  }
+  return true;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
 // FC1 + SwiGLU + requantisation
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_constant__ Fc1Args args) {
-  extern __shared__ uint8_t smem_raw[];
-  Tail* tl;
-  uint8_t* stages = setup(smem_raw, tl, args.offsets, args.E);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int d_ff = args.d_ff, nch = d_ff / BN;
+  Geometry G;
+  G.num_mt = __ldg(args.offsets + args.E) / BM;
+  G.items = 2 * nch;
+  G.nk = (args.d + 255) / 256;
+  G.kgroups = args.d / 64;
+  G.rings = NPROD;
+  G.stages = args.nb;
+  G.resident = args.resident != 0;
+  G.stage_bytes = G.resident ? B_STAGE : A_SLICE + B_STAGE;
+  const uint32_t a_base = smem_u32(smem);
+  const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
+  const size_t ring_bytes = (size_t)NPROD * G.stages * G.stage_bytes;
+  const uint32_t ring_base = a_base + (uint32_t)a_bytes;
+  Tail* tl = setup(smem + a_bytes + ring_bytes);
+  float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* off = tl->offsets;
-  const int d_ff = args.d_ff;
-  Schedule sc;
-  sc.fc1 = true;
-  sc.E = args.E;
-  sc.num_mt = off[args.E] / BM;
-  sc.nch = d_ff / BN;
-  sc.ntn = 1;
-  sc.N = 2 * d_ff;
-  sc.d_ff = d_ff;
-  Mainloop ml{&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, args.d / 64, (args.d + 255) / 256};
+  const ItemRows rows{true, 2 * d_ff, d_ff};
 
-  if (warp == PRODUCER_WARP) {
-    if (lane == 0) {
-      prefetch_tmap(&args.tmap_a);
-      prefetch_tmap(&args.tmap_b);
-      producer_loop(ml, sc, off, stages, tl, abort_flag, args.status);
-    }
-    __syncwarp();
-  } else if (warp == MMA_WARP) {
-    if (lane == 0) mma_loop(ml, sc, off, stages, tl, tl->tmem_base, abort_flag, args.status);
-    __syncwarp();
-  } else {
+  if (run_pipeline_roles(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
+                         ring_base, tl, args.status)) {
     // ---------------- epilogue warps ----------------
-    const int q = warp & 3, hh = warp >> 2;
-    const int rl = q * 32 + lane;  // row within the tile = TMEM lane
-    const uint32_t tmem = tl->tmem_base + ((uint32_t)(q * 32) << 16);
+    const int q4 = warp & 3, part = warp >> 2;  // part: columns 64*part.. of each chunk
+    const int rl = q4 * 32 + lane;              // row within the tile = TMEM lane
+    const uint32_t tmem = tl->tmem_base + ((uint32_t)(q4 * 32) << 16) + part * 64;
     uint4* scratch = reinterpret_cast<uint4*>(args.scratch) + (size_t)blockIdx.x * (size_t)(d_ff / 8) * BM;
     const int kgh = d_ff / 64;
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < sc.num_mt; u += gridDim.x) {
-      const int e = expert_of(off, args.E, u);
+    const float NLOG2E = -1.4426950408889634f;
+    uint32_t it = 0, uc = 0;
+    for (int u = blockIdx.x; u < G.num_mt; u += gridDim.x, ++uc) {
+      const int e = expert_of(args.offsets, args.E, u);
       const int64_t row = (int64_t)u * BM + rl;
       const float ga = args.a_g[row];
-      const float* wg = args.w_g + (int64_t)e * 2 * d_ff;
-      float rowmax = 0.0f;
-      for (int c = 0; c < sc.nch; ++c, it += 2) {
+      float* gws = gw_s + (uc & 1) * 2 * d_ff;
+      stage_scales(gws, args.w_g + (int64_t)e * 2 * d_ff, 2 * d_ff, threadIdx.x);
+      epi_barrier();
+      uint32_t amax2 = 0;  // packed BF16 magnitudes
+      for (int c = 0; c < nch; ++c, it += 2) {
         const uint32_t sg = it % NSLOT, su = (it + 1) % NSLOT;
+        const int n0 = c * BN + part * 64;  // first h column of this thread
         bool ok = !*abort_flag;
         if (ok) ok = wait_bounded(smem_u32(&tl->tfull[sg]), (it / NSLOT) & 1u, abort_flag, args.status);
         if (ok) ok = wait_bounded(smem_u32(&tl->tfull[su]), ((it + 1) / NSLOT) & 1u, abort_flag, args.status);
@@ -359,39 +521,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
         if (ok) {
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            const int col = hh * 64 + cc * 32;  // column within the 128-wide chunk
-            uint32_t G[32], U[32];
-            tmem_ld32(tmem + sg * BN + col, G);
-            tmem_ld32(tmem + su * BN + col, U);
-            const int n0 = c * BN + col;  // h column
-            uint32_t hp[16];
+          for (int hf = 0; hf < 4; ++hf) {  // four quarters of 16 columns
+            uint32_t Gv[16], Uv[16];
+            tmem_ld16(tmem + sg * BN + hf * 16, Gv);
+            tmem_ld16(tmem + su * BN + hf * 16, Uv);
+            tmem_wait_ld();
+            const int nh = n0 + hf * 16;
+            uint32_t hp[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float sgt = __fmul_rn(ga, __ldg(wg + n0 + i));
-              const float sup = __fmul_rn(ga, __ldg(wg + d_ff + n0 + i));
-              const float yg = __fmul_rn(__uint_as_float(G[i]), sgt);
-              const float yu = __fmul_rn(__uint_as_float(U[i]), sup);
-              const float ug = bf16_bits_to_f32(f32_to_bf16_bits(yg));
-              const float uu = bf16_bits_to_f32(f32_to_bf16_bits(yu));
-              const float sl = __fdividef(ug, 1.0f + __expf(-ug));
-              const uint32_t hb = f32_to_bf16_bits(__fmul_rn(sl, uu));
-              rowmax = fmaxf(rowmax, fabsf(bf16_bits_to_f32(hb)));
-              if (i & 1) hp[i >> 1] |= hb << 16; else hp[i >> 1] = hb;
-              if (args.dbg_u) {
-                args.dbg_u[row * 2 * d_ff + n0 + i] = yg;
-                args.dbg_u[row * 2 * d_ff + d_ff + n0 + i] = yu;
+            for (int i = 0; i < 16; i += 4) {
+              const float4 fg = *reinterpret_cast<const float4*>(gws + nh + i);
+              const float4 fu = *reinterpret_cast<const float4*>(gws + d_ff + nh + i);
+              const float gg[4] = {fg.x, fg.y, fg.z, fg.w}, uu[4] = {fu.x, fu.y, fu.z, fu.w};
+#pragma unroll
+              for (int jj = 0; jj < 4; jj += 2) {
+                const int m = i + jj;
+                const float yg0 = __fmul_rn(__uint_as_float(Gv[m]), __fmul_rn(ga, gg[jj]));
+                const float yg1 = __fmul_rn(__uint_as_float(Gv[m + 1]), __fmul_rn(ga, gg[jj + 1]));
+                const float yu0 = __fmul_rn(__uint_as_float(Uv[m]), __fmul_rn(ga, uu[jj]));
+                const float yu1 = __fmul_rn(__uint_as_float(Uv[m + 1]), __fmul_rn(ga, uu[jj + 1]));
+                const uint32_t ugp = bf16x2_rn(yg0, yg1), uup = bf16x2_rn(yu0, yu1);
+                const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
+                const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
+                const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
+                const uint32_t h2 = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
+                amax2 = __vmaxu2(amax2, h2 & 0x7FFF7FFFu);
+                hp[m >> 1] = h2;
+                if (args.dbg_u) {
+                  float* du = args.dbg_u + row * 2 * d_ff;
+                  du[nh + m] = yg0; du[nh + m + 1] = yg1;
+                  du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
+                }
               }
             }
             if (args.dbg_h) {
-              uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + n0);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) dh[v] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
+              uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
+              dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+              dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
             }
-            const int grp = ((c * 2 + hh) * 2 + cc) * 4;  // 16-byte column group index
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              scratch[(size_t)(grp + v) * BM + rl] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
+            scratch[(size_t)((c * 2 + part) * 8 + 2 * hf) * BM + rl] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            scratch[(size_t)((c * 2 + part) * 8 + 2 * hf + 1) * BM + rl] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
           }
         }
         tc_fence_before();
@@ -402,43 +571,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
         }
       }
       // ---- requantise the tile's rows: amax over the full d_ff row ----
-      tl->rowmax[hh][rl] = rowmax;
+      tl->rowmax[part][rl] = __uint_as_float(__vmaxu2(amax2, amax2 >> 16) << 16);
       epi_barrier();
       const float a = fmaxf(tl->rowmax[0][rl], tl->rowmax[1][rl]);
       if (!*abort_flag) {
         if (!is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
         const float g = __fdiv_rn(a, 2688.0f);
         const float den = __fmul_rn(6.0f, g);
-        for (int c = 0; c < sc.nch; ++c) {
-          uint32_t sfword = 0;
+        for (int c = 0; c < nch; ++c) {
+          uint4 cur[8];
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int grp = ((c * 2 + hh) * 2 + cc) * 4;
-            uint32_t w[16];
+          for (int v = 0; v < 8; ++v) cur[v] = scratch[(size_t)((c * 2 + part) * 8 + v) * BM + rl];
+          uint32_t sfw = 0;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 x = scratch[(size_t)(grp + v) * BM + rl];
-              w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t wb[8] = {cur[2 * b].x, cur[2 * b].y, cur[2 * b].z, cur[2 * b].w,
+                                    cur[2 * b + 1].x, cur[2 * b + 1].y, cur[2 * b + 1].z, cur[2 * b + 1].w};
+            uint32_t sb = 0;
+            uint2 p = make_uint2(0u, 0u);
+            if (g != 0.0f) {
+              sb = e4m3_encode(__fdiv_rn(amax16_bf16(wb), den));
+              const float S = __fmul_rn(g, e4m3_decode(sb));
+              if (S != 0.0f) p = e2m1_block16(wb, S);
             }
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-              uint32_t wb[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) wb[i] = w[8 * b + i];
-              uint32_t sb;
-              const uint2 p = quant_block16(wb, g, den, &sb);
-              const int n = c * BN + hh * 64 + cc * 32 + b * 16;  // first column of the block
-              *reinterpret_cast<uint2*>(args.h_codes + row * (d_ff / 2) + n / 2) = p;
-              sfword |= sb << (8 * (cc * 2 + b));
-            }
+            const int n = c * BN + part * 64 + b * 16;
+            *reinterpret_cast<uint2*>(args.h_codes + row * (d_ff / 2) + n / 2) = p;
+            sfw |= sb << (8 * b);
           }
-          const int c4 = 2 * c + hh;  // block-scale column group of columns c*128 + hh*64 .. +64
-          *reinterpret_cast<uint32_t*>(args.h_sf + ((row >> 7) * kgh + c4) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4) =
-              sfword;
+          // blocks 8c + 4*part .. +3 -> scale word 2c + part
+          const int c4 = 2 * c + part;
+          *reinterpret_cast<uint32_t*>(args.h_sf + ((row >> 7) * kgh + c4) * 512 + (row & 31) * 16 +
+                                       ((row >> 5) & 3) * 4) = sfw;
         }
-        if (hh == 0) args.h_g[row] = g;
+        if (part == 0) args.h_g[row] = g;
       }
-      epi_barrier();
     }
   }
   teardown(tl);
@@ -448,42 +614,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
 // FC2 + router-weighted scatter
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_constant__ Fc2Args args) {
-  extern __shared__ uint8_t smem_raw[];
-  Tail* tl;
-  uint8_t* stages = setup(smem_raw, tl, args.offsets, args.E);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int d = args.d, k = args.k;
+  Geometry G;
+  G.num_mt = __ldg(args.offsets + args.E) / BM;
+  G.items = d / BN;
+  G.nk = (args.d_ff + 255) / 256;
+  G.kgroups = args.d_ff / 64;
+  G.rings = NPROD;
+  G.stages = args.nb;
+  G.resident = args.resident != 0;
+  G.stage_bytes = G.resident ? B_STAGE : A_SLICE + B_STAGE;
+  const uint32_t a_base = smem_u32(smem);
+  const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
+  const size_t ring_bytes = (size_t)NPROD * G.stages * G.stage_bytes;
+  const uint32_t ring_base = a_base + (uint32_t)a_bytes;
+  Tail* tl = setup(smem + a_bytes + ring_bytes);
+  float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* off = tl->offsets;
-  const int d = args.d, k = args.k;
-  Schedule sc;
-  sc.fc1 = false;
-  sc.E = args.E;
-  sc.num_mt = off[args.E] / BM;
-  sc.nch = 1;
-  sc.ntn = d / BN;
-  sc.N = d;
-  sc.d_ff = args.d_ff;
-  Mainloop ml{&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, args.d_ff / 64, (args.d_ff + 255) / 256};
+  const ItemRows rows{false, d, args.d_ff};
 
-  if (warp == PRODUCER_WARP) {
-    if (lane == 0) {
-      prefetch_tmap(&args.tmap_a);
-      prefetch_tmap(&args.tmap_b);
-      producer_loop(ml, sc, off, stages, tl, abort_flag, args.status);
-    }
-    __syncwarp();
-  } else if (warp == MMA_WARP) {
-    if (lane == 0) mma_loop(ml, sc, off, stages, tl, tl->tmem_base, abort_flag, args.status);
-    __syncwarp();
-  } else {
-    const int q = warp & 3, hh = warp >> 2;
-    const int rl = q * 32 + lane;
-    const uint32_t tmem = tl->tmem_base + ((uint32_t)(q * 32) << 16);
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < sc.units(); u += gridDim.x, ++it) {
-      const int mt = u / sc.ntn, nt = u % sc.ntn;
-      const int e = expert_of(off, args.E, mt);
-      const int64_t row = (int64_t)mt * BM + rl;
+  if (run_pipeline_roles(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
+                         ring_base, tl, args.status)) {
+    const int q4 = warp & 3, part = warp >> 2;
+    const int rl = q4 * 32 + lane;
+    const uint32_t tmem = tl->tmem_base + ((uint32_t)(q4 * 32) << 16) + part * 64;
+    uint32_t it = 0, uc = 0;
+    for (int u = blockIdx.x; u < G.num_mt; u += gridDim.x, ++uc) {
+      const int e = expert_of(args.offsets, args.E, u);
+      const int64_t row = (int64_t)u * BM + rl;
       const int t = args.row_to_token[row];
       int j = 0;
       float w = 0.0f;
@@ -493,38 +654,50 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_c
         w = args.topk_w[(int64_t)t * k + j];
       }
       const float gh = args.a_g[row];
-      const float* wg = args.w_g + (int64_t)e * d;
-      const uint32_t slot = it % NSLOT;
-      bool ok = !*abort_flag;
-      if (ok) ok = wait_bounded(smem_u32(&tl->tfull[slot]), (it / NSLOT) & 1u, abort_flag, args.status);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (ok) {
-        tc_fence_after();
+      float* gws = gw_s + (uc & 1) * d;
+      stage_scales(gws, args.w_g + (int64_t)e * d, d, threadIdx.x);
+      epi_barrier();
+      uint16_t* dst_row = args.slots + ((int64_t)(t < 0 ? 0 : t) * k + j) * d;
+      for (int nt = 0; nt < G.items; ++nt, ++it) {
+        const uint32_t slot = it % NSLOT;
+        bool ok = !*abort_flag;
+        if (ok) ok = wait_bounded(smem_u32(&tl->tfull[slot]), (it / NSLOT) & 1u, abort_flag, args.status);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok) {
+          tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int col = hh * 64 + cc * 32;
-          uint32_t R[32];
-          tmem_ld32(tmem + slot * BN + col, R);
-          const int n0 = nt * BN + col;
-          if (t >= 0) {
-            uint32_t zp[16];
+          for (int hf = 0; hf < 4; ++hf) {
+            uint32_t R[16];
+            tmem_ld16(tmem + slot * BN + hf * 16, R);
+            tmem_wait_ld();
+            if (t < 0) continue;
+            const int n0 = nt * BN + part * 64 + hf * 16;
+            uint32_t zp[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float sc2 = __fmul_rn(gh, __ldg(wg + n0 + i));
-              const float y2 = __fmul_rn(__uint_as_float(R[i]), sc2);
-              const uint32_t zb = f32_to_bf16_bits(__fmul_rn(w, y2));
-              if (i & 1) zp[i >> 1] |= zb << 16; else zp[i >> 1] = zb;
-              if (args.dbg_y) args.dbg_y[row * d + n0 + i] = y2;
+            for (int i = 0; i < 16; i += 4) {
+              const float4 f4 = *reinterpret_cast<const float4*>(gws + n0 + i);
+              const float f[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+              for (int jj = 0; jj < 4; jj += 2) {
+                const int m = i + jj;
+                const float y0 = __fmul_rn(__uint_as_float(R[m]), __fmul_rn(gh, f[jj]));
+                const float y1 = __fmul_rn(__uint_as_float(R[m + 1]), __fmul_rn(gh, f[jj + 1]));
+                zp[m >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
+                if (args.dbg_y) {
+                  args.dbg_y[row * d + n0 + m] = y0;
+                  args.dbg_y[row * d + n0 + m + 1] = y1;
+                }
+              }
             }
-            uint4* dst = reinterpret_cast<uint4*>(args.slots + ((int64_t)t * k + j) * d + n0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(zp[4 * v], zp[4 * v + 1], zp[4 * v + 2], zp[4 * v + 3]);
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + n0);
+            dst[0] = make_uint4(zp[0], zp[1], zp[2], zp[3]);
+            dst[1] = make_uint4(zp[4], zp[5], zp[6], zp[7]);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[slot]));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[slot]));
     }
   }
   teardown(tl);
@@ -540,33 +713,53 @@ int gemm_num_ctas() {
   return sms < kMaxGemmCtas ? sms : kMaxGemmCtas;
 }
 
-static bool g_attr_set[2][64];
-
-template <typename K>
-static int prepare(K kernel, int which) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  if (dev < 64 && !g_attr_set[which][dev]) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
-      return -1;
-    g_attr_set[which][dev] = true;
+// Shared-memory plan for reduction length K and `scale_floats` per-column
+// scales per expert (staged twice): A resident when its slices fit beside one
+// stage per ring, otherwise A streams with B.  At most MAX_STAGES stages in
+// all (each has its own tensor-memory scale buffer).
+static void plan(int K, int scale_floats, int* na, int* nb, int* resident, size_t* smem) {
+  const int nk = (K + 255) / 256;
+  const size_t fixed = 1024 /* alignment */ + TAIL_BYTES + (size_t)2 * scale_floats * 4;
+  const size_t avail = SMEM_LIMIT - fixed;
+  const size_t max_per_ring = MAX_STAGES / NPROD;
+  if (nk <= MAX_A_SLOTS && (size_t)nk * A_SLICE + NPROD * (size_t)B_STAGE <= avail) {
+    *resident = 1;
+    *na = nk;
+    const size_t s = (avail - (size_t)nk * A_SLICE) / (NPROD * (size_t)B_STAGE);
+    *nb = (int)(s > max_per_ring ? max_per_ring : s);
+    *smem = fixed + (size_t)nk * A_SLICE + (size_t)NPROD * (*nb) * B_STAGE;
+  } else {
+    *resident = 0;
+    *na = 0;
+    const size_t s = avail / (NPROD * (size_t)(A_SLICE + B_STAGE));
+    *nb = (int)(s > max_per_ring ? max_per_ring : s);
+    *smem = fixed + (size_t)NPROD * (*nb) * (A_SLICE + B_STAGE);
   }
+}
+
+static int set_smem(const void* kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess ? 0 : -1;
+}
+
+int launch_fc1(Fc1Args& a, cudaStream_t stream) {
+  size_t smem;
+  plan(a.d, 2 * a.d_ff, &a.na, &a.nb, &a.resident, &smem);
+  if (smem > (size_t)SMEM_LIMIT || a.nb < 1) return -1;
+  if (set_smem((const void*)fc1_swiglu_kernel, smem) != 0) return -1;
+  const int grid = gemm_num_ctas();
+  if (grid <= 0) return -1;
+  fc1_swiglu_kernel<<<grid, NTHREADS, smem, stream>>>(a);
   return 0;
 }
 
-int launch_fc1(const Fc1Args& a, cudaStream_t stream) {
-  if (prepare(fc1_swiglu_kernel, 0) != 0) return -1;
+int launch_fc2(Fc2Args& a, cudaStream_t stream) {
+  size_t smem;
+  plan(a.d_ff, a.d, &a.na, &a.nb, &a.resident, &smem);
+  if (smem > (size_t)SMEM_LIMIT || a.nb < 1) return -1;
+  if (set_smem((const void*)fc2_scatter_kernel, smem) != 0) return -1;
   const int grid = gemm_num_ctas();
   if (grid <= 0) return -1;
-  fc1_swiglu_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a);
-  return 0;
-}
-
-int launch_fc2(const Fc2Args& a, cudaStream_t stream) {
-  if (prepare(fc2_scatter_kernel, 1) != 0) return -1;
-  const int grid = gemm_num_ctas();
-  if (grid <= 0) return -1;
-  fc2_scatter_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(a);
+  fc2_scatter_kernel<<<grid, NTHREADS, smem, stream>>>(a);
   return 0;
 }
 

@@ -55,6 +55,7 @@ struct Fc1Args {
   uint16_t* dbg_h;
   uint16_t* scratch;
   int* status;
+  int na, nb, resident;  // shared-memory plan, set by launch_fc1
 };
 struct Fc2Args {
   CUtensorMap tmap_a, tmap_b;
@@ -70,11 +71,12 @@ struct Fc2Args {
   uint16_t* slots;
   float* dbg_y;
   int* status;
+  int na, nb, resident;  // shared-memory plan, set by launch_fc2
 };
 
 int gemm_num_ctas();  // persistent grid size on the current device
-int launch_fc1(const Fc1Args& a, cudaStream_t stream);
-int launch_fc2(const Fc2Args& a, cudaStream_t stream);
+int launch_fc1(Fc1Args& a, cudaStream_t stream);
+int launch_fc2(Fc2Args& a, cudaStream_t stream);
 constexpr int kMaxGemmCtas = 256;
 
 }  // namespace moe

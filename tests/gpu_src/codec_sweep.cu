@@ -32,9 +32,35 @@ __global__ void e2m1_sweep(unsigned int* first, unsigned long long* viol, unsign
   if (sbad) atomicAdd(sign_viol, sbad);
 }
 
+// The hardware conversion used by the quantisers against the reference
+// encoder, over every finite float of either sign.
+__global__ void e2m1_cvt_sweep(unsigned long long* viol) {
+  const unsigned int stride = gridDim.x * blockDim.x;
+  unsigned long long bad = 0;
+  for (unsigned int p = blockIdx.x * blockDim.x + threadIdx.x; p < 0x7F800000u; p += stride) {
+    for (unsigned int sgn = 0; sgn < 2; ++sgn) {
+      const float v = __uint_as_float(p | (sgn << 31));
+      const float eight[8] = {v, v, v, v, v, v, v, v};
+      const unsigned int c = moe::e2m1_encode(v);
+      if (moe::e2m1x8(eight) != c * 0x11111111u) ++bad;
+    }
+  }
+  if (bad) atomicAdd(viol, bad);
+}
+
 __global__ void e4m3_decode_all(float* out) {
   const int c = threadIdx.x;
   if (c < 0x7F) out[c] = moe::e4m3_decode(c);
+}
+
+extern "C" int run_cvt_sweep(unsigned long long* viol) {
+  unsigned long long* d_v;
+  if (cudaMalloc(&d_v, 8)) return -1;
+  cudaMemset(d_v, 0, 8);
+  e2m1_cvt_sweep<<<152 * 8, 256>>>(d_v);
+  const int rc = cudaMemcpy(viol, d_v, 8, cudaMemcpyDeviceToHost) ? -2 : 0;
+  cudaFree(d_v);
+  return rc;
 }
 
 extern "C" int run_codec_sweeps(unsigned int* e4m3_first, unsigned long long* e4m3_viol, unsigned int* e2m1_first,

@@ -24,3 +24,14 @@ def test_codecs_exhaustive(orc):
         assert f2[c] == orc.lib().orc_e2m1_first_input_of_code(c), c
     for c in range(0x7F):
         assert vals[c] == orc.e4m3_value(c)
+
+
+def test_hardware_e2m1_conversion_exhaustive(orc):
+    """The quantisers encode with the hardware E2M1 conversion; it equals the
+    reference encoder (itself equal to the oracle above) on every finite
+    float of either sign."""
+    from gpu_util import build_test_so
+    L = ctypes.CDLL(build_test_so("codec_sweep"))
+    v = ctypes.c_ulonglong()
+    assert L.run_cvt_sweep(ctypes.byref(v)) == 0
+    assert v.value == 0

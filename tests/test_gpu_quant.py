@@ -45,6 +45,31 @@ def test_quantize_rows_bitexact(orc, rows, K, scale):
     _cmp(orc, got, orc.quantize_rows(xb), rows, K)
 
 
+@pytest.mark.parametrize("g_exp", [-14, -3, 2])
+def test_quantize_rows_exact_ties(orc, g_exp):
+    """Rows built from exact block scales and E2M1 grid values and midpoints:
+    every quotient is exact, half of them exact rounding ties, which the
+    quantiser must resolve like the specification (nearest even)."""
+    from gpu_util import dev, host
+    from helpers import lossless_rows
+    import torch
+    rng = np.random.default_rng(50 + g_exp)
+    rows, K = 96, 256
+    x = lossless_rows(rng, rows, K, g_exp)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    # replace a third of the non-maximal elements by midpoints (ties)
+    blk = np.abs(x).reshape(rows, K // 16, 16).max(2, keepdims=True) / 6.0
+    sel = rng.random(x.shape) < 0.33
+    m = rng.choice(mids, x.shape) * rng.choice([-1, 1], x.shape)
+    tied = (m.reshape(rows, K // 16, 16) * blk).reshape(rows, K)
+    x = np.where(sel & (np.abs(x) < np.repeat(blk.reshape(rows, -1), 16, 1) * 6), tied, x).astype(np.float32)
+    xb = bf16(x)
+    q = M.empty_quantized(rows, K)
+    M.nvfp4_quantize_rows(dev(xb), K, None, None, rows, q["codes"], q["sf"], q["g"])
+    torch.cuda.synchronize()
+    _cmp(orc, (host(q["codes"]), host(q["sf"]), host(q["g"])), orc.quantize_rows(xb), rows, K)
+
+
 def test_quantize_rows_map_amax_and_pad(orc):
     from gpu_util import dev, host
     import torch

@@ -162,6 +162,36 @@ int moe_permute_amax(const float* logits, const int32_t* ext_ids,
                      int32_t* token_slot_row, float* amax_tok, float* amax_row,
                      void* ws, size_t ws_bytes, int* status, void* stream);
 
+/* moe_permute_amax without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin of another runtime that owns all device
+ * memory and passes in only its buffers and a stream, or a serving loop that
+ * must not call cudaMalloc (which can synchronise the device) on its hot
+ * path.  The paper has no counterpart of this entry point: it is a library
+ * convenience.
+ *
+ * Arguments and results are those of moe_permute_amax.  The chunk-histogram
+ * scratch lives in a fixed MOE_PERMUTE_NOALLOC_SCRATCH_BYTES array inside
+ * the library, held on every GPU that loads the library until the process
+ * exits; nothing is allocated or freed.  Shapes whose scratch,
+ * moe_permute_workspace_bytes(T, E), exceeds that size return
+ * MOE_ERR_WORKSPACE before any CUDA call (with 1 MiB: T up to 524288 tokens
+ * at E = 128, 65536 at E = 1024).
+ *
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress, once per device); make that
+ * first call before any stream capture.  All calls share the one array, so
+ * calls whose GPU work overlaps (other streams or host threads at the same
+ * time) race and give wrong results: serialise them.  The array needs no
+ * clearing between calls. */
+#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1 << 20)
+int moe_permute_amax_noalloc(const float* logits, const int32_t* ext_ids,
+                             const float* ext_w, const uint16_t* x, int T,
+                             int E, int k, int d, int32_t* topk_ids,
+                             float* topk_w, int32_t* counts, int32_t* offsets,
+                             int32_t* row_to_token, int32_t* token_slot_row,
+                             float* amax_tok, float* amax_row, int* status,
+                             void* stream);
+
 /* Quantise rows into the GEMM's buffers (Technical Report section 5.1
  * equation; AI summary methodology: codes, block scales and outer scales are
  * written straight into the contiguous buffers the GEMM consumes).

@@ -49,6 +49,7 @@ _SIGS = {
     "moe_expert_forward_workspace_layout": (I32, [I32, I32, I32, I32, I32, P]),
     "moe_nvfp4_quantize_weights": (I32, [P, I32, I32, I32, P, P, P, P, P]),
     "moe_permute_amax": (I32, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
+    "moe_permute_amax_noalloc": (I32, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P]),
     "nvfp4_quantize_rows": (I32, [P, I32, I32, P, P, I32, P, P, P, P, P]),
     "nvfp4_grouped_gemm_fc1_swiglu": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
     "nvfp4_grouped_gemm_fc2_unpermute": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, I32, I32, P, P, P, P, P]),
@@ -145,6 +146,17 @@ def moe_permute_amax(logits, ext_ids, ext_w, x, T, E, k, d, topk_ids, topk_w, co
         _p(logits), _p(ext_ids), _p(ext_w), _p(x), T, E, k, d, _p(topk_ids), _p(topk_w), _p(counts),
         _p(offsets), _p(row_to_token), _p(token_slot_row), _p(amax_tok), _p(amax_row), _p(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _p(status), _s(stream)))
+
+
+def moe_permute_amax_noalloc(logits, ext_ids, ext_w, x, T, E, k, d, topk_ids, topk_w, counts, offsets,
+                             row_to_token, token_slot_row, amax_tok, amax_row, status=None, stream=None):
+    """moe_permute_amax with the library's own fixed scratch array instead of
+    a workspace: for callers that cannot allocate device memory.  Calls that
+    overlap on the GPU race on that array; see include/moe_nvfp4.h."""
+    _check("moe_permute_amax_noalloc", lib().moe_permute_amax_noalloc(
+        _p(logits), _p(ext_ids), _p(ext_w), _p(x), T, E, k, d, _p(topk_ids), _p(topk_w), _p(counts),
+        _p(offsets), _p(row_to_token), _p(token_slot_row), _p(amax_tok), _p(amax_row), _p(status),
+        _s(stream)))
 
 
 def nvfp4_quantize_rows(src, K, row_map, amax, dst_rows, codes, sf, g, status=None, stream=None):

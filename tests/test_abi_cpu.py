@@ -16,7 +16,7 @@ def L():
 
 def test_exports_every_header_function(L):
     names = M.header_functions()
-    assert len(names) == 14, names
+    assert len(names) == 15, names
     for n in names:
         assert hasattr(L, n), n
     for n in ["moe_nvfp4_quantize_weights", "moe_permute_amax", "nvfp4_quantize_rows",
@@ -86,6 +86,12 @@ def test_entry_points_reject_bad_arguments(L):
     bad = list(args)
     bad[0] = None
     assert L.moe_permute_amax(*bad, FAKE, 1 << 30, None, None) == M.MOE_ERR_POINTER
+    # the no-allocation variant rejects shapes whose histograms exceed its
+    # fixed scratch array before any CUDA call
+    na = [FAKE, None, None, FAKE, 600000, 128, 2, 256] + [FAKE] * 8 + [None, None]
+    assert L.moe_permute_amax_noalloc(*na) == M.MOE_ERR_WORKSPACE
+    na[5] = 2000
+    assert L.moe_permute_amax_noalloc(*na) == M.MOE_ERR_SHAPE
     fc1 = [FAKE] * 4 + [8, 1024, 256, 128] + [FAKE] * 8 + [FAKE]
     assert L.nvfp4_grouped_gemm_fc1_swiglu(*fc1, 16, None, None) == M.MOE_ERR_WORKSPACE
     fc1b = list(fc1)

@@ -10,8 +10,9 @@
 //            128-byte swizzle) is loaded once into resident shared memory, one
 //            slice per 256 elements of K; the B operand (128 weight rows x 256
 //            elements of K) and the block-scale tiles of both operands stream
-//            through three rings of stages, one ring per producer warp, the
-//            k-steps dealt round-robin over the rings.  When K does not fit,
+//            through four rings of one or two stages, the k-steps dealt
+//            round-robin over the rings; producer warp p feeds the rings r
+//            with r % 3 == p, each ring from one warp in order.  When K does not fit,
 //            A streams through the stages too.
 //   warps 8-11  block-scale writers, one per tensor-memory lane quadrant.
 //            For each stage they move the scale tiles from shared to tensor
@@ -21,8 +22,9 @@
 //            column base + r/32), and signal the stage's scales as ready.
 //   warp 15  MMA issuer: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X
 //            (M=128, N=128, K=64, UE4M3 scale per 16 elements) into one of
-//            three 128-column FP32 accumulators; nothing else goes through
-//            the tensor pipe.
+//            the 128-column FP32 accumulators (three for FC1, two for FC2);
+//            nothing else goes through the tensor pipe.  Tensor memory after
+//            the accumulators holds one 32-column scale buffer per stage.
 //   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and
 //            half (w/4) of the accumulator's columns, releases the
 //            accumulator, then does the FP32 epilogue from registers.  The
@@ -54,15 +56,19 @@ constexpr int B_BYTES = BN * BK_BYTES;                 // 16 KB
 constexpr int SF_STAGE = 4 * 512;                      // 2 KB per operand
 constexpr int B_STAGE = B_BYTES + 2 * SF_STAGE;        // 20 KB: B, SFB, SFA
 constexpr int MAX_A_SLOTS = 16;
-constexpr int MAX_STAGES = 4;                          // over all rings (one TMEM scale buffer each)
-constexpr int NPROD = 3;                               // producer warps (rings)
-constexpr int NSLOT = 3;                               // accumulators
+constexpr int MAX_STAGES = 8;                          // over all rings (one TMEM scale buffer each)
+constexpr int NPROD_WARPS = 3;                         // producer warps: warp p feeds rings r with r % 3 == p
+constexpr int NSLOT_MAX = 3;                           // accumulators
+constexpr int FC1_NSLOT = 3;                           // FC1 pairs gate and up tiles: three
+constexpr int FC2_NSLOT = 2;                           // FC2: double buffering
+constexpr int FC2_STAGE_ROW = 128;                     // FC2 output staging: 64 BF16 columns per row
+constexpr int FC2_STAGING_BYTES = 8 * 32 * FC2_STAGE_ROW;  // 32 rows per epilogue warp
 constexpr int TMEM_COLS = 512;
-constexpr int SF_TMEM_COL = NSLOT * BN;                // per stage: [A scales 16 | B scales 16]
+constexpr int SF_COLS = 32;                            // per stage: [A scales 16 | B scales 16]
 constexpr int NEPI_WARPS = 8;
 constexpr int NEPI_THREADS = NEPI_WARPS * 32;
 constexpr int SFW_WARP = 8;                            // scale writers 8..11
-constexpr int PRODUCER_WARP = 12, MMA_WARP = PRODUCER_WARP + NPROD;
+constexpr int PRODUCER_WARP = 12, MMA_WARP = PRODUCER_WARP + NPROD_WARPS;
 constexpr int NTHREADS = (MMA_WARP + 1) * 32;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
@@ -77,8 +83,8 @@ struct Tail {
   uint64_t b_full[MAX_STAGES];
   uint64_t b_empty[MAX_STAGES];
   uint64_t sf_full[MAX_STAGES];
-  uint64_t tfull[NSLOT];
-  uint64_t tempty[NSLOT];
+  uint64_t tfull[NSLOT_MAX];
+  uint64_t tempty[NSLOT_MAX];
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
@@ -105,6 +111,18 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
       return false;
     }
   }
+}
+
+// Warp-wide wait: lane 0 polls, the other lanes wait at the warp barrier
+// and then take their own (immediately satisfied) look at the completed
+// phase, so a waiting warp costs the barrier unit one poller, not 32.  All
+// 32 lanes call it; the result is the same in every lane.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status);
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  if (ok) (void)mbar_try_wait(bar, parity);
+  return ok;
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -144,6 +162,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
   return v;
 }
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -166,16 +187,30 @@ struct Geometry {
   int items;       // accumulator tiles per unit
   int nk;          // k-steps of 256 elements
   int kgroups;     // K / 64 (block-scale 4-column groups)
-  int rings;       // producer warps, each owning a ring of stages
-  int stages;      // stages per ring
+  int rings;       // rings of stages, 3 or 4; ring r is fed by producer warp r % 3
+  int log2_stages; // stages per ring = 1 << log2_stages
   int stage_bytes; // [A slice when streamed][B][SFB][SFA]
+  int nslot;       // accumulators (128 TMEM columns each)
   bool resident;   // A slices loaded once per unit into their own slots
   __device__ uint32_t b_off() const { return resident ? 0u : (uint32_t)A_SLICE; }
+  // first TMEM column of the scale buffers (one per stage, after the accumulators)
+  __device__ uint32_t sf_col() const { return (uint32_t)(nslot * BN); }
+  // ring of CTA-local k-step kc and its position in the ring
+  __device__ void ring_of(uint32_t kc, uint32_t& r, uint32_t& pos) const {
+    if (rings == 4) {
+      r = kc & 3u;
+      pos = kc >> 2;
+    } else {
+      pos = kc / 3u;
+      r = kc - 3u * pos;
+    }
+  }
   // ring slot of CTA-local k-step kc and the use count of that slot
   __device__ void slot_of(uint32_t kc, uint32_t& slot, uint32_t& use) const {
-    const uint32_t r = kc % (uint32_t)rings, pos = kc / (uint32_t)rings;
-    slot = r * (uint32_t)stages + pos % (uint32_t)stages;
-    use = pos / (uint32_t)stages;
+    uint32_t r, pos;
+    ring_of(kc, r, pos);
+    slot = (r << log2_stages) + (pos & ((1u << log2_stages) - 1u));
+    use = pos >> log2_stages;
   }
 };
 
@@ -193,9 +228,9 @@ struct ItemRows {
 // kc = 0, 1, ...; k-step kc travels through ring kc % R, position kc / R.
 // Each ring has one producer and is consumed in order, so every barrier sees
 // its phases in order.  A producer runs at most R*S k-steps ahead of the
-// consumers, fewer than the k-steps of one unit, so the resident A slots
-// (loaded at the first item of a unit by whichever producer owns that
-// k-step) never see a phase ahead of the one they wait for.
+// MMAs; the plan keeps that below the reach that would let a resident A
+// slot's a_empty wait (at the first item of a unit, by whichever producer
+// owns that k-step) alias an older phase.
 __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const uint8_t* a_sf,
                               const uint8_t* b_sf, const Geometry& G, const ItemRows& rows, const int32_t* off, int E,
                               uint32_t a_base, uint32_t ring_base, Tail* tl, volatile int* abort_flag, int* status) {
@@ -213,7 +248,9 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
       const int br = rows(e, q);
       const int64_t sfb_row = (int64_t)(br / BM) * G.kgroups;
       for (int ks = 0; ks < G.nk; ++ks, ++kc) {
-        if (kc % (uint32_t)G.rings != (uint32_t)r) continue;
+        uint32_t ring, pos;
+        G.ring_of(kc, ring, pos);
+        if (ring % (uint32_t)NPROD_WARPS != (uint32_t)r) continue;
         uint32_t slot, use;
         G.slot_of(kc, slot, use);
         if (!wait_bounded(smem_u32(&tl->b_empty[slot]), (use & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
@@ -262,6 +299,9 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
 //     scale bytes of row 32*qd + l in A-scale tile i (bytes 16*l + 4*qd).
 // The stage's buffer is rewritten only after its next use has landed, which
 // the producer issues only after the MMAs of the previous use completed.
+// The writers also wait for the resident A slice of the k-step (first item of
+// a unit), so the MMA thread waits on sf_full alone: its completion implies
+// that the stage's operands and the A slice have landed.
 __device__ void sf_writer_loop(int qd, const Geometry& G, uint32_t ring_base, Tail* tl, uint32_t tmem,
                                volatile int* abort_flag, int* status) {
   const int lane = threadIdx.x & 31;
@@ -270,12 +310,14 @@ __device__ void sf_writer_loop(int qd, const Geometry& G, uint32_t ring_base, Ta
   uint32_t kc = 0;
   bool aborted = false;
   for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
+    const uint32_t unit_use = (uint32_t)((u - (int)blockIdx.x) / (int)gridDim.x);
     for (int q = 0; q < G.items && !aborted; ++q) {
       for (int ks = 0; ks < G.nk; ++ks, ++kc) {
         uint32_t slot, use;
         G.slot_of(kc, slot, use);
-        bool ok = wait_bounded(smem_u32(&tl->b_full[slot]), use & 1u, abort_flag, status);
-        if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
+        bool ok = warp_wait(smem_u32(&tl->b_full[slot]), use & 1u, abort_flag, status);
+        if (ok && G.resident && q == 0) ok = warp_wait(smem_u32(&tl->a_full[ks]), unit_use & 1u, abort_flag, status);
+        if (!ok) { aborted = true; break; }
         tc_fence_after();
         const int nsf = min(4, G.kgroups - 4 * ks);
         const uint32_t sfb_s = ring_base + slot * G.stage_bytes + b_off + B_BYTES;
@@ -291,7 +333,7 @@ __device__ void sf_writer_loop(int qd, const Geometry& G, uint32_t ring_base, Ta
           }
           wb[4 * i] = v.x; wb[4 * i + 1] = v.y; wb[4 * i + 2] = v.z; wb[4 * i + 3] = v.w;
         }
-        const uint32_t col = tq + SF_TMEM_COL + slot * 32;
+        const uint32_t col = tq + G.sf_col() + slot * SF_COLS;
         tmem_st16(col + 16, wb);
 #pragma unroll
         for (int i = 0; i < 4; ++i) tmem_st1(col + 4 * i + qd, wa[i]);
@@ -310,23 +352,19 @@ __device__ void mma_loop(const Geometry& G, uint32_t a_base, uint32_t ring_base,
   uint32_t kc = 0, it = 0;
   bool aborted = false;
   for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
-    const uint32_t unit_use = (uint32_t)((u - (int)blockIdx.x) / (int)gridDim.x);
     for (int q = 0; q < G.items && !aborted; ++q, ++it) {
-      const uint32_t acc_slot = it % NSLOT, suse = it / NSLOT;
+      const uint32_t acc_slot = it % (uint32_t)G.nslot, suse = it / (uint32_t)G.nslot;
       if (!wait_bounded(smem_u32(&tl->tempty[acc_slot]), (suse & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t dacc = tmem + acc_slot * BN;
       for (int ks = 0; ks < G.nk; ++ks, ++kc) {
         uint32_t slot, use;
         G.slot_of(kc, slot, use);
-        if (!wait_bounded(smem_u32(&tl->b_full[slot]), use & 1u, abort_flag, status)) { aborted = true; break; }
         if (!wait_bounded(smem_u32(&tl->sf_full[slot]), use & 1u, abort_flag, status)) { aborted = true; break; }
-        if (G.resident && q == 0 &&
-            !wait_bounded(smem_u32(&tl->a_full[ks]), unit_use & 1u, abort_flag, status)) { aborted = true; break; }
         tc_fence_after();
         const int nmma = min(4, G.kgroups - 4 * ks);
         const uint32_t st = ring_base + slot * G.stage_bytes;
-        const uint32_t sf_a = tmem + SF_TMEM_COL + slot * 32;
+        const uint32_t sf_a = tmem + G.sf_col() + slot * SF_COLS;
         const uint32_t sf_b = sf_a + 16;
         const uint64_t adesc = sdesc_k_sw128(G.resident ? a_base + ks * A_SLICE : st);
         const uint64_t bdesc = sdesc_k_sw128(st + b_off);
@@ -365,7 +403,7 @@ __device__ __forceinline__ Tail* setup(uint8_t* tail_ptr) {
       mbar_init(smem_u32(&tl->b_empty[s]), 1);
       mbar_init(smem_u32(&tl->sf_full[s]), 4);
     }
-    for (int s = 0; s < NSLOT; ++s) {
+    for (int s = 0; s < NSLOT_MAX; ++s) {
       mbar_init(smem_u32(&tl->tfull[s]), 1);
       mbar_init(smem_u32(&tl->tempty[s]), NEPI_WARPS);
     }
@@ -479,13 +517,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
   G.items = 2 * nch;
   G.nk = (args.d + 255) / 256;
   G.kgroups = args.d / 64;
-  G.rings = NPROD;
-  G.stages = args.nb;
+  G.rings = args.rings;
+  G.log2_stages = args.nb == 2 ? 1 : 0;
+  G.nslot = FC1_NSLOT;
   G.resident = args.resident != 0;
   G.stage_bytes = G.resident ? B_STAGE : A_SLICE + B_STAGE;
   const uint32_t a_base = smem_u32(smem);
   const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
-  const size_t ring_bytes = (size_t)NPROD * G.stages * G.stage_bytes;
+  const size_t ring_bytes = (size_t)G.rings * (1 << G.log2_stages) * G.stage_bytes;
   const uint32_t ring_base = a_base + (uint32_t)a_bytes;
   Tail* tl = setup(smem + a_bytes + ring_bytes);
   float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
@@ -512,48 +551,68 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
       epi_barrier();
       uint32_t amax2 = 0;  // packed BF16 magnitudes
       for (int c = 0; c < nch; ++c, it += 2) {
-        const uint32_t sg = it % NSLOT, su = (it + 1) % NSLOT;
+        const uint32_t sg = it % FC1_NSLOT, su = (it + 1) % FC1_NSLOT;
         const int n0 = c * BN + part * 64;  // first h column of this thread
-        bool ok = !*abort_flag;
-        if (ok) ok = wait_bounded(smem_u32(&tl->tfull[sg]), (it / NSLOT) & 1u, abort_flag, args.status);
-        if (ok) ok = wait_bounded(smem_u32(&tl->tfull[su]), ((it + 1) / NSLOT) & 1u, abort_flag, args.status);
-        ok = __all_sync(0xFFFFFFFFu, ok);
+        bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
+        if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (it / FC1_NSLOT) & 1u, abort_flag, args.status);
+        if (ok) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
+        // Drain both accumulators into registers as the BF16 FC1 outputs u
+        // (this thread's 64 gate and 64 up columns), release them to the MMA
+        // warp, then form h from registers.
+        uint32_t UG[32], UU[32];
         if (ok) {
           tc_fence_after();
-#pragma unroll 1
+#pragma unroll
           for (int hf = 0; hf < 4; ++hf) {  // four quarters of 16 columns
-            uint32_t Gv[16], Uv[16];
-            tmem_ld16(tmem + sg * BN + hf * 16, Gv);
-            tmem_ld16(tmem + su * BN + hf * 16, Uv);
-            tmem_wait_ld();
-            const int nh = n0 + hf * 16;
-            uint32_t hp[8];
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              const float4 fg = *reinterpret_cast<const float4*>(gws + nh + i);
-              const float4 fu = *reinterpret_cast<const float4*>(gws + d_ff + nh + i);
-              const float gg[4] = {fg.x, fg.y, fg.z, fg.w}, uu[4] = {fu.x, fu.y, fu.z, fu.w};
+            for (int gu = 0; gu < 2; ++gu) {  // gate, then up: 16 registers in flight
+              uint32_t V[16];
+              tmem_ld16(tmem + (gu ? su : sg) * BN + hf * 16, V);
+              tmem_wait_ld();
+              const int nh = n0 + hf * 16;
+              const float* gsc = gws + gu * d_ff + nh;
 #pragma unroll
-              for (int jj = 0; jj < 4; jj += 2) {
-                const int m = i + jj;
-                const float yg0 = __fmul_rn(__uint_as_float(Gv[m]), __fmul_rn(ga, gg[jj]));
-                const float yg1 = __fmul_rn(__uint_as_float(Gv[m + 1]), __fmul_rn(ga, gg[jj + 1]));
-                const float yu0 = __fmul_rn(__uint_as_float(Uv[m]), __fmul_rn(ga, uu[jj]));
-                const float yu1 = __fmul_rn(__uint_as_float(Uv[m + 1]), __fmul_rn(ga, uu[jj + 1]));
-                const uint32_t ugp = bf16x2_rn(yg0, yg1), uup = bf16x2_rn(yu0, yu1);
-                const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
-                const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
-                const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
-                const uint32_t h2 = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
-                amax2 = __vmaxu2(amax2, h2 & 0x7FFF7FFFu);
-                hp[m >> 1] = h2;
-                if (args.dbg_u) {
-                  float* du = args.dbg_u + row * 2 * d_ff;
-                  du[nh + m] = yg0; du[nh + m + 1] = yg1;
-                  du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
+              for (int i = 0; i < 16; i += 4) {
+                const float4 f4 = *reinterpret_cast<const float4*>(gsc + i);
+                const float f[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                for (int jj = 0; jj < 4; jj += 2) {
+                  const int m = i + jj;
+                  const float y0 = __fmul_rn(__uint_as_float(V[m]), __fmul_rn(ga, f[jj]));
+                  const float y1 = __fmul_rn(__uint_as_float(V[m + 1]), __fmul_rn(ga, f[jj + 1]));
+                  if (gu) UU[hf * 8 + (m >> 1)] = bf16x2_rn(y0, y1);
+                  else UG[hf * 8 + (m >> 1)] = bf16x2_rn(y0, y1);
+                  if (args.dbg_u) {
+                    float* du = args.dbg_u + row * 2 * d_ff + gu * d_ff + nh;
+                    du[m] = y0;
+                    du[m + 1] = y1;
+                  }
                 }
               }
             }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&tl->tempty[sg]));
+          mbar_arrive(smem_u32(&tl->tempty[su]));
+        }
+        if (ok) {
+#pragma unroll
+          for (int hf = 0; hf < 4; ++hf) {
+            uint32_t hp[8];
+#pragma unroll
+            for (int m2 = 0; m2 < 8; ++m2) {
+              const uint32_t ugp = UG[hf * 8 + m2], uup = UU[hf * 8 + m2];
+              const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
+              const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
+              const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
+              const uint32_t h2 = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
+              amax2 = __vmaxu2(amax2, h2 & 0x7FFF7FFFu);
+              hp[m2] = h2;
+            }
+            const int nh = n0 + hf * 16;
             if (args.dbg_h) {
               uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
               dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
@@ -562,12 +621,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
             scratch[(size_t)((c * 2 + part) * 8 + 2 * hf) * BM + rl] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
             scratch[(size_t)((c * 2 + part) * 8 + 2 * hf + 1) * BM + rl] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&tl->tempty[sg]));
-          mbar_arrive(smem_u32(&tl->tempty[su]));
         }
       }
       // ---- requantise the tile's rows: amax over the full d_ff row ----
@@ -622,19 +675,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_c
   G.items = d / BN;
   G.nk = (args.d_ff + 255) / 256;
   G.kgroups = args.d_ff / 64;
-  G.rings = NPROD;
-  G.stages = args.nb;
+  G.rings = args.rings;
+  G.log2_stages = args.nb == 2 ? 1 : 0;
+  G.nslot = FC2_NSLOT;
   G.resident = args.resident != 0;
   G.stage_bytes = G.resident ? B_STAGE : A_SLICE + B_STAGE;
   const uint32_t a_base = smem_u32(smem);
   const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
-  const size_t ring_bytes = (size_t)NPROD * G.stages * G.stage_bytes;
+  const size_t ring_bytes = (size_t)G.rings * (1 << G.log2_stages) * G.stage_bytes;
   const uint32_t ring_base = a_base + (uint32_t)a_bytes;
   Tail* tl = setup(smem + a_bytes + ring_bytes);
   float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ItemRows rows{false, d, args.d_ff};
+  // per epilogue warp: 32 rows x 64 BF16 columns, 16-byte chunks XOR-swizzled by row
+  const uint32_t stg = smem_u32(smem + a_bytes + ring_bytes + TAIL_BYTES + (size_t)2 * d * 4) +
+                       (uint32_t)(warp < NEPI_WARPS ? warp : 0) * 32 * FC2_STAGE_ROW;
 
   if (run_pipeline_roles(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
                          ring_base, tl, args.status)) {
@@ -659,18 +716,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_c
       epi_barrier();
       uint16_t* dst_row = args.slots + ((int64_t)(t < 0 ? 0 : t) * k + j) * d;
       for (int nt = 0; nt < G.items; ++nt, ++it) {
-        const uint32_t slot = it % NSLOT;
-        bool ok = !*abort_flag;
-        if (ok) ok = wait_bounded(smem_u32(&tl->tfull[slot]), (it / NSLOT) & 1u, abort_flag, args.status);
-        ok = __all_sync(0xFFFFFFFFu, ok);
+        const uint32_t slot = it % FC2_NSLOT;
+        bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
+        if (ok) ok = warp_wait(smem_u32(&tl->tfull[slot]), (it / FC2_NSLOT) & 1u, abort_flag, args.status);
+        // Drain the accumulator (this thread's 64 columns) into registers,
+        // release it to the MMA warp, then scale, weight and store.
+        uint32_t R[4][16];
         if (ok) {
           tc_fence_after();
-#pragma unroll 1
+#pragma unroll
+          for (int hf = 0; hf < 4; ++hf) tmem_ld16(tmem + slot * BN + hf * 16, R[hf]);
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[slot]));
+        if (ok) {
+          // scale and weight into the staging tile, then write each row's 64
+          // columns as one 128-byte segment (8 lanes per row, 4 rows per
+          // instruction); pad rows (t < 0) are not stored
+#pragma unroll
           for (int hf = 0; hf < 4; ++hf) {
-            uint32_t R[16];
-            tmem_ld16(tmem + slot * BN + hf * 16, R);
-            tmem_wait_ld();
-            if (t < 0) continue;
             const int n0 = nt * BN + part * 64 + hf * 16;
             uint32_t zp[8];
 #pragma unroll
@@ -680,23 +746,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_c
 #pragma unroll
               for (int jj = 0; jj < 4; jj += 2) {
                 const int m = i + jj;
-                const float y0 = __fmul_rn(__uint_as_float(R[m]), __fmul_rn(gh, f[jj]));
-                const float y1 = __fmul_rn(__uint_as_float(R[m + 1]), __fmul_rn(gh, f[jj + 1]));
+                const float y0 = __fmul_rn(__uint_as_float(R[hf][m]), __fmul_rn(gh, f[jj]));
+                const float y1 = __fmul_rn(__uint_as_float(R[hf][m + 1]), __fmul_rn(gh, f[jj + 1]));
                 zp[m >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
-                if (args.dbg_y) {
+                if (args.dbg_y && t >= 0) {
                   args.dbg_y[row * d + n0 + m] = y0;
                   args.dbg_y[row * d + n0 + m + 1] = y1;
                 }
               }
             }
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + n0);
-            dst[0] = make_uint4(zp[0], zp[1], zp[2], zp[3]);
-            dst[1] = make_uint4(zp[4], zp[5], zp[6], zp[7]);
+            sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf) ^ (lane & 7)), zp[0], zp[1], zp[2], zp[3]);
+            sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf + 1) ^ (lane & 7)), zp[4], zp[5], zp[6], zp[7]);
           }
+          __syncwarp();
+          const unsigned long long my_dst =
+              t >= 0 ? reinterpret_cast<unsigned long long>(dst_row + nt * BN + part * 64) : 0ull;
+          const int sub = lane >> 3, ch = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + sub;
+            const unsigned long long dp = __shfl_sync(0xFFFFFFFFu, my_dst, rr);
+            const uint4 v = lds128(stg + rr * FC2_STAGE_ROW + 16 * (ch ^ (rr & 7)));
+            if (dp) reinterpret_cast<uint4*>(dp)[ch] = v;
+          }
+          __syncwarp();
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[slot]));
       }
     }
   }
@@ -713,28 +787,44 @@ int gemm_num_ctas() {
   return sms < kMaxGemmCtas ? sms : kMaxGemmCtas;
 }
 
-// Shared-memory plan for reduction length K and `scale_floats` per-column
-// scales per expert (staged twice): A resident when its slices fit beside one
-// stage per ring, otherwise A streams with B.  At most MAX_STAGES stages in
-// all (each has its own tensor-memory scale buffer).
-static void plan(int K, int scale_floats, int* na, int* nb, int* resident, size_t* smem) {
+// Pipeline plan for reduction length K, `items` accumulator tiles per unit,
+// `scale_floats` per-column scales per expert (staged twice) and `extra`
+// bytes of epilogue staging.  The tensor memory after the accumulators holds
+// one scale buffer per stage; rings are 3 or 4, stages per ring 1 or 2, and
+// the plan takes the most stages that fit.  A is resident (loaded once per
+// unit) when its slices fit beside the rings and a unit spans enough
+// k-steps: a producer runs up to rings*S k-steps ahead of the MMAs, and
+// (items + 1) * nk >= rings*S keeps it from reaching the A slots of unit m
+// before the slots of unit m-2 are released, so the parity of every a_empty
+// wait is unambiguous.  Otherwise A streams through the stages with B.
+static bool plan(int K, int items, int scale_floats, int nslot, size_t extra, int* rings, int* na, int* nb,
+                 int* resident, size_t* smem) {
   const int nk = (K + 255) / 256;
-  const size_t fixed = 1024 /* alignment */ + TAIL_BYTES + (size_t)2 * scale_floats * 4;
+  const size_t fixed = 1024 /* alignment */ + TAIL_BYTES + (size_t)2 * scale_floats * 4 + extra;
+  if (fixed >= (size_t)SMEM_LIMIT) return false;
   const size_t avail = SMEM_LIMIT - fixed;
-  const size_t max_per_ring = MAX_STAGES / NPROD;
-  if (nk <= MAX_A_SLOTS && (size_t)nk * A_SLICE + NPROD * (size_t)B_STAGE <= avail) {
-    *resident = 1;
-    *na = nk;
-    const size_t s = (avail - (size_t)nk * A_SLICE) / (NPROD * (size_t)B_STAGE);
-    *nb = (int)(s > max_per_ring ? max_per_ring : s);
-    *smem = fixed + (size_t)nk * A_SLICE + (size_t)NPROD * (*nb) * B_STAGE;
-  } else {
-    *resident = 0;
-    *na = 0;
-    const size_t s = avail / (NPROD * (size_t)(A_SLICE + B_STAGE));
-    *nb = (int)(s > max_per_ring ? max_per_ring : s);
-    *smem = fixed + (size_t)NPROD * (*nb) * (A_SLICE + B_STAGE);
+  static const int cand[4][2] = {{4, 2}, {3, 2}, {4, 1}, {3, 1}};  // (rings, stages per ring), most stages first
+  for (int pass = 0; pass < 2; ++pass) {  // pass 0: A resident, pass 1: A streamed
+    for (const auto& c : cand) {
+      const int R = c[0], S = c[1];
+      if (nslot * BN + R * S * SF_COLS > TMEM_COLS) continue;
+      size_t need;
+      if (pass == 0) {
+        if (nk > MAX_A_SLOTS || (int64_t)(items + 1) * nk < (int64_t)R * S) continue;
+        need = (size_t)nk * A_SLICE + (size_t)R * S * B_STAGE;
+      } else {
+        need = (size_t)R * S * (A_SLICE + B_STAGE);
+      }
+      if (need > avail) continue;
+      *rings = R;
+      *nb = S;
+      *resident = pass == 0 ? 1 : 0;
+      *na = pass == 0 ? nk : 0;
+      *smem = fixed + need;
+      return true;
+    }
   }
+  return false;
 }
 
 static int set_smem(const void* kernel, size_t smem) {
@@ -743,8 +833,7 @@ static int set_smem(const void* kernel, size_t smem) {
 
 int launch_fc1(Fc1Args& a, cudaStream_t stream) {
   size_t smem;
-  plan(a.d, 2 * a.d_ff, &a.na, &a.nb, &a.resident, &smem);
-  if (smem > (size_t)SMEM_LIMIT || a.nb < 1) return -1;
+  if (!plan(a.d, 2 * (a.d_ff / BN), 2 * a.d_ff, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem)) return -1;
   if (set_smem((const void*)fc1_swiglu_kernel, smem) != 0) return -1;
   const int grid = gemm_num_ctas();
   if (grid <= 0) return -1;
@@ -754,8 +843,8 @@ int launch_fc1(Fc1Args& a, cudaStream_t stream) {
 
 int launch_fc2(Fc2Args& a, cudaStream_t stream) {
   size_t smem;
-  plan(a.d_ff, a.d, &a.na, &a.nb, &a.resident, &smem);
-  if (smem > (size_t)SMEM_LIMIT || a.nb < 1) return -1;
+  if (!plan(a.d_ff, a.d / BN, a.d, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident, &smem))
+    return -1;
   if (set_smem((const void*)fc2_scatter_kernel, smem) != 0) return -1;
   const int grid = gemm_num_ctas();
   if (grid <= 0) return -1;

@@ -55,7 +55,7 @@ struct Fc1Args {
   uint16_t* dbg_h;
   uint16_t* scratch;
   int* status;
-  int na, nb, resident;  // shared-memory plan, set by launch_fc1
+  int rings, na, nb, resident;  // pipeline plan, set by launch_fc1
 };
 struct Fc2Args {
   CUtensorMap tmap_a, tmap_b;
@@ -71,7 +71,7 @@ struct Fc2Args {
   uint16_t* slots;
   float* dbg_y;
   int* status;
-  int na, nb, resident;  // shared-memory plan, set by launch_fc2
+  int rings, na, nb, resident;  // pipeline plan, set by launch_fc2
 };
 
 int gemm_num_ctas();  // persistent grid size on the current device

@@ -59,12 +59,16 @@ def run_fc1(lay, c):
                 u=host(dbg_u), h=host(dbg_h, np.uint16))
 
 
-CASES = [("tiny", None), ("small", None), ("custom_d128", None), ("custom_skew", None)]
+CASES = [("tiny", None), ("small", None), ("custom_d128", None), ("custom_skew", None), ("custom_many_units", None)]
 
 
 def layer_of(name):
     if name == "custom_d128":
         return synth.custom(T=300, d=128, E=3, k=2, d_ff=256, seed=4)
+    if name == "custom_many_units":
+        # K = 128 in both GEMMs: one k-step per item, hundreds of units per
+        # launch, so the producers run many units ahead of the MMAs
+        return synth.custom(T=6000, d=128, E=4, k=2, d_ff=128, seed=6)
     if name == "custom_skew":
         return synth.custom(T=700, d=384, E=16, k=3, d_ff=384, seed=5, logits="bias", bias_std=3.0,
                             n_forced_empty=5)

@@ -20,9 +20,9 @@ __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
   return va > vb || (va == vb && ea < eb);
 }
 
-// One CTA per chunk of 256 tokens, one warp per token at a time.
+// One CTA per chunk of 256 tokens, sixteen warps, one warp per token at a time.
 template <int NPL>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits,
+__global__ void __launch_bounds__(512) route_kernel(const float* __restrict__ logits,
                                                    const int32_t* __restrict__ ext_ids,
                                                    const float* __restrict__ ext_w, int T, int E, int k,
                                                    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
@@ -131,7 +131,7 @@ int launch_route(const float* logits, const int32_t* ext_ids, const float* ext_w
   const size_t smem = (size_t)E * (kChunk / 32) * sizeof(uint32_t);
   const int npl = (E + 31) / 32;
 #define MOE_ROUTE(N)                                                                                 \
-  route_kernel<N><<<C, 256, smem, stream>>>(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, \
+  route_kernel<N><<<C, 512, smem, stream>>>(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, \
                                            token_slot_row, hist, status)
   if (npl <= 1) MOE_ROUTE(1);
   else if (npl <= 2) MOE_ROUTE(2);
@@ -282,8 +282,11 @@ int launch_pad_rows(const int32_t* offsets, const int32_t* counts, int E, int64_
 
 // One warp per token: rows of its k slots, amax of x (read once into
 // registers), quantisation, and the same codes / block scales / outer scale
-// written into each of the k destination rows.
-template <int MAXCH>
+// written into each of the k destination rows.  Lane L holds, for each group
+// of 1024 columns, the 32 consecutive columns from 32*L (two whole 16-element
+// blocks), so a block never spans lanes, its codes go out as one 16-byte
+// store per row, and lanes L, L ^ 1 together form one 32-bit scale word.
+template <int NG>
 __global__ void __launch_bounds__(256) permute_quant_kernel(
     const int32_t* __restrict__ topk_ids, int32_t* __restrict__ tsr, const int32_t* __restrict__ hist,
     const int32_t* __restrict__ offsets, int T, int E, int k, const uint16_t* __restrict__ x, int d,
@@ -300,57 +303,74 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     row_to_token[row] = t;
   }
   const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
-  const int n8 = d / 8;
-  uint4 v[MAXCH];
+  const int n8 = d / 8;  // 8-column vectors of the row
+  uint4 v[NG][4];
   float a = 0.0f;
   bool fin = true;
 #pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    const int e8 = i * 32 + lane;
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (e8 < n8) {
-      v[i] = __ldg(xr + e8);
-      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+  for (int g = 0; g < NG; ++g) {
+    const int e8 = g * 128 + 4 * lane;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        fin = fin && bf16x2_finite(w[q]);
-        a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+    for (int q = 0; q < 4; ++q) {
+      v[g][q] = make_uint4(0u, 0u, 0u, 0u);
+      if (e8 < n8) {
+        v[g][q] = __ldg(xr + e8 + q);
+        const uint32_t w[4] = {v[g][q].x, v[g][q].y, v[g][q].z, v[g][q].w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          fin = fin && bf16x2_finite(w[m]);
+          a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[m])), fabsf(bf16_hi(w[m]))));
+        }
       }
     }
   }
   if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, MOE_STATUS_NONFINITE_X);
   a = warp_max(a);
   if (lane == 0 && amax_tok) amax_tok[t] = a;
-  const float g = __fdiv_rn(a, 2688.0f);
-  const float den = __fmul_rn(6.0f, g);
+  const float gs = __fdiv_rn(a, 2688.0f);
+  const float den = __fmul_rn(6.0f, gs);
   const int kg = d / 64;
-  uint32_t packed[MAXCH], sfw[MAXCH];
+  uint4 cw[NG];
+  uint32_t sfw[NG];
 #pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    packed[i] = 0u;
-    sfw[i] = 0u;
-    if (i * 32 < n8) {
-      uint32_t sb;
-      packed[i] = quant_half_block(v[i], g, den, &sb);
-      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
-      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
-      sfw[i] = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  for (int g = 0; g < NG; ++g) {
+    uint32_t c[4] = {0u, 0u, 0u, 0u}, sb2 = 0u;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {  // the lane's two blocks of 16
+      const uint4 p0 = v[g][2 * b], p1 = v[g][2 * b + 1];
+      const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w}, w1[4] = {p1.x, p1.y, p1.z, p1.w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = __vmaxu2(__vmaxu2(m, w0[i] & 0x7FFF7FFFu), w1[i] & 0x7FFF7FFFu);
+      const float ab = __uint_as_float(__vmaxu2(m, m >> 16) << 16);
+      uint32_t sb = 0;
+      if (gs != 0.0f) {
+        sb = e4m3_encode(__fdiv_rn(ab, den));
+        const float S = __fmul_rn(gs, e4m3_decode(sb));
+        if (S != 0.0f) {
+          c[2 * b] = e2m1_codes8(w0, S);
+          c[2 * b + 1] = e2m1_codes8(w1, S);
+        }
+      }
+      sb2 |= sb << (8 * b);
     }
+    cw[g] = make_uint4(c[0], c[1], c[2], c[3]);
+    sfw[g] = sb2 | (__shfl_xor_sync(0xFFFFFFFFu, sb2, 1) << 16);
   }
   for (int j = 0; j < k; ++j) {
     const int64_t r = __shfl_sync(0xFFFFFFFFu, row, j);
-    uint32_t* crow = reinterpret_cast<uint32_t*>(codes + r * (d / 2));
+    uint4* crow = reinterpret_cast<uint4*>(codes + r * (d / 2));
 #pragma unroll
-    for (int i = 0; i < MAXCH; ++i) {
-      const int e8 = i * 32 + lane;
+    for (int g = 0; g < NG; ++g) {
+      const int e8 = g * 128 + 4 * lane;
       if (e8 < n8) {
-        crow[e8] = packed[i];
-        if ((lane & 7) == 0)
-          *reinterpret_cast<uint32_t*>(sf + ((r >> 7) * kg + (e8 >> 3)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) = sfw[i];
+        crow[e8 >> 2] = cw[g];
+        if ((lane & 1) == 0)
+          *reinterpret_cast<uint32_t*>(sf + ((r >> 7) * kg + (e8 >> 3)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) =
+              sfw[g];
       }
     }
-    if (lane == 0) gout[r] = g;
+    if (lane == 0) gout[r] = gs;
   }
 }
 
@@ -358,17 +378,15 @@ int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const
                          int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
                          uint8_t* codes, uint8_t* sf, float* g, int* status, cudaStream_t stream) {
   if (T == 0) return 0;
-  const int nch = (d / 8 + 31) / 32;
+  const int ng = (d + 1023) / 1024;
   const dim3 grid((T + 7) / 8);
-  if (nch <= 4)
-    permute_quant_kernel<4><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d,
-                                                     row_to_token, amax_tok, codes, sf, g, status);
-  else if (nch <= 8)
-    permute_quant_kernel<8><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d,
-                                                     row_to_token, amax_tok, codes, sf, g, status);
-  else
-    permute_quant_kernel<16><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d,
-                                                      row_to_token, amax_tok, codes, sf, g, status);
+#define MOE_PQ(N)                                                                                       \
+  permute_quant_kernel<N><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d, \
+                                                    row_to_token, amax_tok, codes, sf, g, status)
+  if (ng <= 1) MOE_PQ(1);
+  else if (ng <= 2) MOE_PQ(2);
+  else MOE_PQ(4);
+#undef MOE_PQ
   return 0;
 }
 

@@ -103,7 +103,9 @@ size_t nvfp4_sf_bytes(int64_t rows, int K);
 /* Workspace of moe_permute_amax (chunk histograms). */
 size_t moe_permute_workspace_bytes(int T, int E);
 
-/* Workspace of nvfp4_grouped_gemm_fc1_swiglu (per-CTA h staging). */
+/* Workspace of nvfp4_grouped_gemm_fc1_swiglu: h staging, two 128 x d_ff
+ * BF16 buffers per CTA (a unit is staged while the previous one is
+ * requantised). */
 size_t nvfp4_fc1_workspace_bytes(int d_ff);
 
 /* Workspace of moe_expert_forward (all intermediates of one forward). */

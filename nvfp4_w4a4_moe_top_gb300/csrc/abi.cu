@@ -97,7 +97,7 @@ FwdLayout fwd_layout(int T, int E, int k, int d, int d_ff) {
       (size_t)T * k * 4, (size_t)T * k * 4, (size_t)T * k * 4, (size_t)E * 4, (size_t)(E + 1) * 4, (size_t)mc * 4,
       (size_t)T * 4,     (size_t)mc * (d / 2), sf_bytes_of(mc, d), (size_t)mc * 4, (size_t)mc * (d_ff / 2),
       sf_bytes_of(mc, d_ff), (size_t)mc * 4, (size_t)T * k * d * 2, (size_t)C * E * 4,
-      (size_t)moe::kMaxGemmCtas * 128 * d_ff * 2};
+      (size_t)moe::kMaxGemmCtas * 2 * 128 * d_ff * 2};
   FwdLayout L;
   size_t o = 0;
   for (int i = 0; i < 16; ++i) {
@@ -143,7 +143,7 @@ size_t moe_permute_workspace_bytes(int T, int E) {
 
 size_t nvfp4_fc1_workspace_bytes(int d_ff) {
   if (d_ff < 128 || d_ff % 128 != 0) return 0;
-  return (size_t)moe::kMaxGemmCtas * 128 * d_ff * 2;
+  return (size_t)moe::kMaxGemmCtas * 2 * 128 * d_ff * 2;
 }
 
 size_t moe_expert_forward_workspace_bytes(int T, int E, int k, int d, int d_ff) {

@@ -473,6 +473,40 @@ __device__ __forceinline__ void stage_scales(float* dst, const float* src, int n
     reinterpret_cast<float4*>(dst)[i] = __ldg(reinterpret_cast<const float4*>(src) + i);
 }
 
+// FC1 requantisation of one thread's 64 columns (half `part` of chunk c) of
+// row `row`, read back from the scratch vectors this thread staged: per block
+// of 16 the E4M3 scale s_b = E4M3(a_b / (6 g)) and the E2M1 codes of
+// h / (g s_b); the chunk's four scale bytes form scale word 2c + part.
+__device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int part, int rl, int64_t row, float g,
+                                              float den, uint8_t* h_codes, uint8_t* h_sf, int d_ff) {
+  uint4 cur[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v) cur[v] = scr[(size_t)((c * 2 + part) * 8 + v) * BM + rl];
+  uint32_t sfw = 0;
+  uint32_t cw[8];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t wb[8] = {cur[2 * b].x, cur[2 * b].y, cur[2 * b].z, cur[2 * b].w,
+                            cur[2 * b + 1].x, cur[2 * b + 1].y, cur[2 * b + 1].z, cur[2 * b + 1].w};
+    uint32_t sb = 0;
+    uint2 p = make_uint2(0u, 0u);
+    if (g != 0.0f) {
+      sb = e4m3_encode(__fdiv_rn(amax16_bf16(wb), den));
+      const float S = __fmul_rn(g, e4m3_decode(sb));
+      if (S != 0.0f) p = e2m1_block16(wb, S);
+    }
+    cw[2 * b] = p.x;
+    cw[2 * b + 1] = p.y;
+    sfw |= sb << (8 * b);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(h_codes + row * (d_ff / 2) + (c * BN + part * 64) / 2);
+  dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  const int kgh = d_ff / 64;
+  *reinterpret_cast<uint32_t*>(h_sf + ((row >> 7) * kgh + 2 * c + part) * 512 + (row & 31) * 16 +
+                               ((row >> 5) & 3) * 4) = sfw;
+}
+
 // Shared roles of both GEMMs.  Returns true for the epilogue warps, which
 // the caller then runs.
 __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b,
@@ -538,14 +572,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
     const int q4 = warp & 3, part = warp >> 2;  // part: columns 64*part.. of each chunk
     const int rl = q4 * 32 + lane;              // row within the tile = TMEM lane
     const uint32_t tmem = tl->tmem_base + ((uint32_t)(q4 * 32) << 16) + part * 64;
-    uint4* scratch = reinterpret_cast<uint4*>(args.scratch) + (size_t)blockIdx.x * (size_t)(d_ff / 8) * BM;
-    const int kgh = d_ff / 64;
+    // Two scratch buffers per CTA: unit i stages h in buffer i % 2 while the
+    // thread requantises its own row half of unit i - 1 from the other,
+    // one chunk after each chunk of unit i (the thread reads back only what
+    // it wrote, so program order is the only ordering needed).
+    uint4* scratch_cta = reinterpret_cast<uint4*>(args.scratch) + (size_t)blockIdx.x * 2 * (size_t)(d_ff / 8) * BM;
     const float NLOG2E = -1.4426950408889634f;
+    bool have_prev = false;
+    int64_t row_prev = 0;
+    float g_prev = 0.0f, den_prev = 0.0f;
+    const uint4* scr_prev = scratch_cta;
     uint32_t it = 0, uc = 0;
     for (int u = blockIdx.x; u < G.num_mt; u += gridDim.x, ++uc) {
       const int e = expert_of(args.offsets, args.E, u);
       const int64_t row = (int64_t)u * BM + rl;
       const float ga = args.a_g[row];
+      uint4* scratch = scratch_cta + (size_t)(uc & 1) * (size_t)(d_ff / 8) * BM;
       float* gws = gw_s + (uc & 1) * 2 * d_ff;
       stage_scales(gws, args.w_g + (int64_t)e * 2 * d_ff, 2 * d_ff, threadIdx.x);
       epi_barrier();
@@ -622,42 +664,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
             scratch[(size_t)((c * 2 + part) * 8 + 2 * hf + 1) * BM + rl] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
           }
         }
+        if (have_prev && !*abort_flag)
+          requant_chunk(scr_prev, c, part, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf, d_ff);
       }
-      // ---- requantise the tile's rows: amax over the full d_ff row ----
+      // ---- outer scale of the unit's rows: amax over the full d_ff row ----
       tl->rowmax[part][rl] = __uint_as_float(__vmaxu2(amax2, amax2 >> 16) << 16);
       epi_barrier();
       const float a = fmaxf(tl->rowmax[0][rl], tl->rowmax[1][rl]);
-      if (!*abort_flag) {
-        if (!is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
-        const float g = __fdiv_rn(a, 2688.0f);
-        const float den = __fmul_rn(6.0f, g);
-        for (int c = 0; c < nch; ++c) {
-          uint4 cur[8];
-#pragma unroll
-          for (int v = 0; v < 8; ++v) cur[v] = scratch[(size_t)((c * 2 + part) * 8 + v) * BM + rl];
-          uint32_t sfw = 0;
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const uint32_t wb[8] = {cur[2 * b].x, cur[2 * b].y, cur[2 * b].z, cur[2 * b].w,
-                                    cur[2 * b + 1].x, cur[2 * b + 1].y, cur[2 * b + 1].z, cur[2 * b + 1].w};
-            uint32_t sb = 0;
-            uint2 p = make_uint2(0u, 0u);
-            if (g != 0.0f) {
-              sb = e4m3_encode(__fdiv_rn(amax16_bf16(wb), den));
-              const float S = __fmul_rn(g, e4m3_decode(sb));
-              if (S != 0.0f) p = e2m1_block16(wb, S);
-            }
-            const int n = c * BN + part * 64 + b * 16;
-            *reinterpret_cast<uint2*>(args.h_codes + row * (d_ff / 2) + n / 2) = p;
-            sfw |= sb << (8 * b);
-          }
-          // blocks 8c + 4*part .. +3 -> scale word 2c + part
-          const int c4 = 2 * c + part;
-          *reinterpret_cast<uint32_t*>(args.h_sf + ((row >> 7) * kgh + c4) * 512 + (row & 31) * 16 +
-                                       ((row >> 5) & 3) * 4) = sfw;
-        }
-        if (part == 0) args.h_g[row] = g;
-      }
+      if (have_prev && part == 0) args.h_g[row_prev] = g_prev;
+      if (!*abort_flag && !is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
+      have_prev = true;
+      row_prev = row;
+      g_prev = __fdiv_rn(a, 2688.0f);
+      den_prev = __fmul_rn(6.0f, g_prev);
+      scr_prev = scratch;
+    }
+    // the last unit
+    if (have_prev) {
+      if (!*abort_flag)
+        for (int c = 0; c < nch; ++c)
+          requant_chunk(scr_prev, c, part, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf, d_ff);
+      if (part == 0) args.h_g[row_prev] = g_prev;
     }
   }
   teardown(tl);

@@ -32,7 +32,7 @@ def test_helpers_match_oracle(L, orc):
         assert M.sf_bytes(rows, K) == orc.sf_bytes(rows, K)
     assert M.sf_bytes(10, 48) == 0
     assert M.status_string(-3) == "workspace too small"
-    assert M.fc1_workspace_bytes(768) == 256 * 128 * 768 * 2
+    assert M.fc1_workspace_bytes(768) == 256 * 2 * 128 * 768 * 2
 
 
 def test_workspace_layout_is_disjoint_and_aligned(L):

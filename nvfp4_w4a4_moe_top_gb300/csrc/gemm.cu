@@ -144,6 +144,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[15])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,"
+      "%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
@@ -598,40 +608,54 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
         bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (it / FC1_NSLOT) & 1u, abort_flag, args.status);
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
-        // Drain both accumulators into registers as the BF16 FC1 outputs u
-        // (this thread's 64 gate and 64 up columns), release them to the MMA
-        // warp, then form h from registers.
-        uint32_t UG[32], UU[32];
+        // Two halves of 32 columns: load gate and up (one tensor-memory round
+        // trip), u = BF16(acc * (g_x * g_w)), h = BF16(silu(u_gate) * u_up),
+        // stage h; the accumulators are released after the second half.
         if (ok) {
           tc_fence_after();
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t Gv[32], Uv[32];
+            tmem_ld32(tmem + sg * BN + hh * 32, Gv);
+            tmem_ld32(tmem + su * BN + hh * 32, Uv);
+            tmem_wait_ld();
+            const int nh = n0 + hh * 32;
+            uint32_t hp[16];
 #pragma unroll
-          for (int hf = 0; hf < 4; ++hf) {  // four quarters of 16 columns
+            for (int i = 0; i < 32; i += 4) {
+              const float4 fg = *reinterpret_cast<const float4*>(gws + nh + i);
+              const float4 fu = *reinterpret_cast<const float4*>(gws + d_ff + nh + i);
+              const float gg[4] = {fg.x, fg.y, fg.z, fg.w}, uu[4] = {fu.x, fu.y, fu.z, fu.w};
 #pragma unroll
-            for (int gu = 0; gu < 2; ++gu) {  // gate, then up: 16 registers in flight
-              uint32_t V[16];
-              tmem_ld16(tmem + (gu ? su : sg) * BN + hf * 16, V);
-              tmem_wait_ld();
-              const int nh = n0 + hf * 16;
-              const float* gsc = gws + gu * d_ff + nh;
-#pragma unroll
-              for (int i = 0; i < 16; i += 4) {
-                const float4 f4 = *reinterpret_cast<const float4*>(gsc + i);
-                const float f[4] = {f4.x, f4.y, f4.z, f4.w};
-#pragma unroll
-                for (int jj = 0; jj < 4; jj += 2) {
-                  const int m = i + jj;
-                  const float y0 = __fmul_rn(__uint_as_float(V[m]), __fmul_rn(ga, f[jj]));
-                  const float y1 = __fmul_rn(__uint_as_float(V[m + 1]), __fmul_rn(ga, f[jj + 1]));
-                  if (gu) UU[hf * 8 + (m >> 1)] = bf16x2_rn(y0, y1);
-                  else UG[hf * 8 + (m >> 1)] = bf16x2_rn(y0, y1);
-                  if (args.dbg_u) {
-                    float* du = args.dbg_u + row * 2 * d_ff + gu * d_ff + nh;
-                    du[m] = y0;
-                    du[m + 1] = y1;
-                  }
+              for (int jj = 0; jj < 4; jj += 2) {
+                const int m = i + jj;
+                const float yg0 = __fmul_rn(__uint_as_float(Gv[m]), __fmul_rn(ga, gg[jj]));
+                const float yg1 = __fmul_rn(__uint_as_float(Gv[m + 1]), __fmul_rn(ga, gg[jj + 1]));
+                const float yu0 = __fmul_rn(__uint_as_float(Uv[m]), __fmul_rn(ga, uu[jj]));
+                const float yu1 = __fmul_rn(__uint_as_float(Uv[m + 1]), __fmul_rn(ga, uu[jj + 1]));
+                const uint32_t ugp = bf16x2_rn(yg0, yg1), uup = bf16x2_rn(yu0, yu1);
+                const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
+                const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
+                const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
+                const uint32_t h2 = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
+                amax2 = __vmaxu2(amax2, h2 & 0x7FFF7FFFu);
+                hp[m >> 1] = h2;
+                if (args.dbg_u) {
+                  float* du = args.dbg_u + row * 2 * d_ff;
+                  du[nh + m] = yg0; du[nh + m + 1] = yg1;
+                  du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
                 }
               }
             }
+            if (args.dbg_h) {
+              uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) dh[q] = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              scratch[(size_t)((c * 2 + part) * 8 + 4 * hh + q) * BM + rl] =
+                  make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
           }
         }
         tc_fence_before();
@@ -639,30 +663,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
         if (lane == 0) {
           mbar_arrive(smem_u32(&tl->tempty[sg]));
           mbar_arrive(smem_u32(&tl->tempty[su]));
-        }
-        if (ok) {
-#pragma unroll
-          for (int hf = 0; hf < 4; ++hf) {
-            uint32_t hp[8];
-#pragma unroll
-            for (int m2 = 0; m2 < 8; ++m2) {
-              const uint32_t ugp = UG[hf * 8 + m2], uup = UU[hf * 8 + m2];
-              const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
-              const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
-              const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
-              const uint32_t h2 = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
-              amax2 = __vmaxu2(amax2, h2 & 0x7FFF7FFFu);
-              hp[m2] = h2;
-            }
-            const int nh = n0 + hf * 16;
-            if (args.dbg_h) {
-              uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
-              dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-              dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
-            }
-            scratch[(size_t)((c * 2 + part) * 8 + 2 * hf) * BM + rl] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-            scratch[(size_t)((c * 2 + part) * 8 + 2 * hf + 1) * BM + rl] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
-          }
         }
         if (have_prev && !*abort_flag)
           requant_chunk(scr_prev, c, part, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf, d_ff);

@@ -61,15 +61,28 @@ constexpr int NPROD_WARPS = 3;                         // producer warps: warp p
 constexpr int NSLOT_MAX = 3;                           // accumulators
 constexpr int FC1_NSLOT = 3;                           // FC1 pairs gate and up tiles: three
 constexpr int FC2_NSLOT = 2;                           // FC2: double buffering
-constexpr int FC2_STAGE_ROW = 128;                     // FC2 output staging: 64 BF16 columns per row
-constexpr int FC2_STAGING_BYTES = 8 * 32 * FC2_STAGE_ROW;  // 32 rows per epilogue warp
+// Epilogue warps per kernel: warp w serves TMEM lane quadrant w % 4 and
+// column part w / 4 of each accumulator.  FC1's SwiGLU/requantisation is
+// latency-bound and gains from four warps per scheduler (16 warps, 32
+// columns each, 80 registers per thread); FC2's light epilogue keeps 8 warps
+// of 64 columns at 128 registers.
+constexpr int FC1_NE = 16, FC2_NE = 8;
+constexpr int FC1_PARTS = FC1_NE / 4, FC1_PART_COLS = BN / FC1_PARTS;  // 4 parts of 32 columns
+constexpr int FC2_PARTS = FC2_NE / 4, FC2_PART_COLS = BN / FC2_PARTS;  // 2 parts of 64 columns
+constexpr int FC2_STAGE_ROW = FC2_PART_COLS * 2;       // FC2 output staging: one part's BF16 columns per row
+constexpr int FC2_STAGING_BYTES = FC2_NE * 32 * FC2_STAGE_ROW;  // 32 rows per epilogue warp
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COLS = 32;                            // per stage: [A scales 16 | B scales 16]
-constexpr int NEPI_WARPS = 8;
-constexpr int NEPI_THREADS = NEPI_WARPS * 32;
-constexpr int SFW_WARP = 8;                            // scale writers 8..11
-constexpr int PRODUCER_WARP = 12, MMA_WARP = PRODUCER_WARP + NPROD_WARPS;
-constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+// Warp roles for NE epilogue warps: epilogue 0..NE-1, scale writers
+// NE..NE+3, producers NE+4..NE+6, MMA issuer NE+7.
+template <int NE>
+struct Roles {
+  static constexpr int EPI_THREADS = NE * 32;
+  static constexpr int SFW = NE;
+  static constexpr int PROD = NE + 4;
+  static constexpr int MMA = PROD + NPROD_WARPS;
+  static constexpr int THREADS = (MMA + 1) * 32;
+};
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
 
@@ -88,7 +101,7 @@ struct Tail {
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
-  float rowmax[2][BM];
+  float rowmax[4][BM];  // per column part (FC1)
 };
 
 constexpr size_t TAIL_BYTES = (sizeof(Tail) + 1023) / 1024 * 1024;
@@ -144,16 +157,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[15])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,"
-      "%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
@@ -166,7 +169,10 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+template <int NE>
+__device__ __forceinline__ void epi_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(Roles<NE>::EPI_THREADS) : "memory");
+}
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -400,6 +406,7 @@ __device__ void mma_loop(const Geometry& G, uint32_t a_base, uint32_t ring_base,
 }
 
 // Prologue: barriers and tensor memory.
+template <int NE>
 __device__ __forceinline__ Tail* setup(uint8_t* tail_ptr) {
   Tail* tl = reinterpret_cast<Tail*>(tail_ptr);
   const int warp = threadIdx.x >> 5;
@@ -415,13 +422,13 @@ __device__ __forceinline__ Tail* setup(uint8_t* tail_ptr) {
     }
     for (int s = 0; s < NSLOT_MAX; ++s) {
       mbar_init(smem_u32(&tl->tfull[s]), 1);
-      mbar_init(smem_u32(&tl->tempty[s]), NEPI_WARPS);
+      mbar_init(smem_u32(&tl->tempty[s]), NE);
     }
     mbar_init(smem_u32(&tl->done), 1);
     tl->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == MMA_WARP) {
+  if (warp == Roles<NE>::MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
                  "r"(TMEM_COLS)
                  : "memory");
@@ -433,11 +440,12 @@ __device__ __forceinline__ Tail* setup(uint8_t* tail_ptr) {
   return tl;
 }
 
+template <int NE>
 __device__ __forceinline__ void teardown(Tail* tl) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if ((threadIdx.x >> 5) == MMA_WARP) {
+  if ((threadIdx.x >> 5) == Roles<NE>::MMA) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
                  : "memory");
   }
@@ -478,24 +486,26 @@ __device__ __forceinline__ float amax16_bf16(const uint32_t (&w)[8]) {
 
 // Stage n floats (n % 4 == 0) from global into shared memory with the
 // epilogue threads.
+template <int NE>
 __device__ __forceinline__ void stage_scales(float* dst, const float* src, int n, int tid) {
-  for (int i = tid; i < n / 4; i += NEPI_THREADS)
+  for (int i = tid; i < n / 4; i += Roles<NE>::EPI_THREADS)
     reinterpret_cast<float4*>(dst)[i] = __ldg(reinterpret_cast<const float4*>(src) + i);
 }
 
-// FC1 requantisation of one thread's 64 columns (half `part` of chunk c) of
-// row `row`, read back from the scratch vectors this thread staged: per block
-// of 16 the E4M3 scale s_b = E4M3(a_b / (6 g)) and the E2M1 codes of
-// h / (g s_b); the chunk's four scale bytes form scale word 2c + part.
+// FC1 requantisation of one thread's 32 columns (part `part` of chunk c,
+// two blocks of 16) of row `row`, read back from the scratch vectors this
+// thread staged: per block the E4M3 scale s_b = E4M3(a_b / (6 g)) and the
+// E2M1 codes of h / (g s_b).  The two scale bytes are bytes 2*(part % 2)
+// and +1 of scale word 2c + part/2.
 __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int part, int rl, int64_t row, float g,
                                               float den, uint8_t* h_codes, uint8_t* h_sf, int d_ff) {
-  uint4 cur[8];
+  uint4 cur[4];
 #pragma unroll
-  for (int v = 0; v < 8; ++v) cur[v] = scr[(size_t)((c * 2 + part) * 8 + v) * BM + rl];
-  uint32_t sfw = 0;
-  uint32_t cw[8];
+  for (int v = 0; v < 4; ++v) cur[v] = scr[(size_t)((c * FC1_PARTS + part) * 4 + v) * BM + rl];
+  uint32_t sb2 = 0;
+  uint32_t cw[4];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
+  for (int b = 0; b < 2; ++b) {
     const uint32_t wb[8] = {cur[2 * b].x, cur[2 * b].y, cur[2 * b].z, cur[2 * b].w,
                             cur[2 * b + 1].x, cur[2 * b + 1].y, cur[2 * b + 1].z, cur[2 * b + 1].w};
     uint32_t sb = 0;
@@ -507,41 +517,42 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int part,
     }
     cw[2 * b] = p.x;
     cw[2 * b + 1] = p.y;
-    sfw |= sb << (8 * b);
+    sb2 |= sb << (8 * b);
   }
-  uint4* dst = reinterpret_cast<uint4*>(h_codes + row * (d_ff / 2) + (c * BN + part * 64) / 2);
-  dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-  dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  *reinterpret_cast<uint4*>(h_codes + row * (d_ff / 2) + (c * BN + part * FC1_PART_COLS) / 2) =
+      make_uint4(cw[0], cw[1], cw[2], cw[3]);
   const int kgh = d_ff / 64;
-  *reinterpret_cast<uint32_t*>(h_sf + ((row >> 7) * kgh + 2 * c + part) * 512 + (row & 31) * 16 +
-                               ((row >> 5) & 3) * 4) = sfw;
+  *reinterpret_cast<uint16_t*>(h_sf + ((row >> 7) * kgh + 2 * c + (part >> 1)) * 512 + (row & 31) * 16 +
+                               ((row >> 5) & 3) * 4 + 2 * (part & 1)) = (uint16_t)sb2;
 }
 
 // Shared roles of both GEMMs.  Returns true for the epilogue warps, which
 // the caller then runs.
+template <int NE>
 __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b,
                                                    const uint8_t* a_sf, const uint8_t* b_sf, const Geometry& G,
                                                    const ItemRows& rows, const int32_t* off, int E, uint32_t a_base,
                                                    uint32_t ring_base, Tail* tl, int* status) {
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp >= PRODUCER_WARP && warp < MMA_WARP) {
+  using RL = Roles<NE>;
+  if (warp >= RL::PROD && warp < RL::MMA) {
     if (lane == 0) {
       prefetch_tmap(tmap_a);
       prefetch_tmap(tmap_b);
-      producer_loop(warp - PRODUCER_WARP, tmap_a, tmap_b, a_sf, b_sf, G, rows, off, E, a_base, ring_base, tl,
+      producer_loop(warp - RL::PROD, tmap_a, tmap_b, a_sf, b_sf, G, rows, off, E, a_base, ring_base, tl,
                     abort_flag, status);
     }
     __syncwarp();
     return false;
   }
-  if (warp == MMA_WARP) {
+  if (warp == RL::MMA) {
     if (lane == 0) mma_loop(G, a_base, ring_base, tl, tl->tmem_base, abort_flag, status);
     __syncwarp();
     return false;
   }
-  if (warp >= SFW_WARP && warp < SFW_WARP + 4) {
-    sf_writer_loop(warp - SFW_WARP, G, ring_base, tl, tl->tmem_base, abort_flag, status);
+  if (warp >= RL::SFW && warp < RL::SFW + 4) {
+    sf_writer_loop(warp - RL::SFW, G, ring_base, tl, tl->tmem_base, abort_flag, status);
     return false;
   }
   return true;
@@ -552,7 +563,7 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
 // ---------------------------------------------------------------------------
 // FC1 + SwiGLU + requantisation
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_constant__ Fc1Args args) {
+__global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(const __grid_constant__ Fc1Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int d_ff = args.d_ff, nch = d_ff / BN;
@@ -570,18 +581,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
   const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
   const size_t ring_bytes = (size_t)G.rings * (1 << G.log2_stages) * G.stage_bytes;
   const uint32_t ring_base = a_base + (uint32_t)a_bytes;
-  Tail* tl = setup(smem + a_bytes + ring_bytes);
+  Tail* tl = setup<FC1_NE>(smem + a_bytes + ring_bytes);
   float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ItemRows rows{true, 2 * d_ff, d_ff};
 
-  if (run_pipeline_roles(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
+  if (run_pipeline_roles<FC1_NE>(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
                          ring_base, tl, args.status)) {
     // ---------------- epilogue warps ----------------
-    const int q4 = warp & 3, part = warp >> 2;  // part: columns 64*part.. of each chunk
+    const int q4 = warp & 3, part = warp >> 2;  // part: columns FC1_PART_COLS*part.. of each chunk
     const int rl = q4 * 32 + lane;              // row within the tile = TMEM lane
-    const uint32_t tmem = tl->tmem_base + ((uint32_t)(q4 * 32) << 16) + part * 64;
+    const uint32_t tmem = tl->tmem_base + ((uint32_t)(q4 * 32) << 16) + part * FC1_PART_COLS;
     // Two scratch buffers per CTA: unit i stages h in buffer i % 2 while the
     // thread requantises its own row half of unit i - 1 from the other,
     // one chunk after each chunk of unit i (the thread reads back only what
@@ -599,30 +610,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
       const float ga = args.a_g[row];
       uint4* scratch = scratch_cta + (size_t)(uc & 1) * (size_t)(d_ff / 8) * BM;
       float* gws = gw_s + (uc & 1) * 2 * d_ff;
-      stage_scales(gws, args.w_g + (int64_t)e * 2 * d_ff, 2 * d_ff, threadIdx.x);
-      epi_barrier();
+      stage_scales<FC1_NE>(gws, args.w_g + (int64_t)e * 2 * d_ff, 2 * d_ff, threadIdx.x);
+      epi_barrier<FC1_NE>();
       uint32_t amax2 = 0;  // packed BF16 magnitudes
       for (int c = 0; c < nch; ++c, it += 2) {
         const uint32_t sg = it % FC1_NSLOT, su = (it + 1) % FC1_NSLOT;
-        const int n0 = c * BN + part * 64;  // first h column of this thread
+        const int n0 = c * BN + part * FC1_PART_COLS;  // first h column of this thread
         bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (it / FC1_NSLOT) & 1u, abort_flag, args.status);
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
-        // Two halves of 32 columns: load gate and up (one tensor-memory round
+        // Two halves of 16 columns: load gate and up (one tensor-memory round
         // trip), u = BF16(acc * (g_x * g_w)), h = BF16(silu(u_gate) * u_up),
         // stage h; the accumulators are released after the second half.
         if (ok) {
           tc_fence_after();
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t Gv[32], Uv[32];
-            tmem_ld32(tmem + sg * BN + hh * 32, Gv);
-            tmem_ld32(tmem + su * BN + hh * 32, Uv);
+            uint32_t Gv[16], Uv[16];
+            tmem_ld16(tmem + sg * BN + hh * 16, Gv);
+            tmem_ld16(tmem + su * BN + hh * 16, Uv);
             tmem_wait_ld();
-            const int nh = n0 + hh * 32;
-            uint32_t hp[16];
+            const int nh = n0 + hh * 16;
+            uint32_t hp[8];
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
+            for (int i = 0; i < 16; i += 4) {
               const float4 fg = *reinterpret_cast<const float4*>(gws + nh + i);
               const float4 fu = *reinterpret_cast<const float4*>(gws + d_ff + nh + i);
               const float gg[4] = {fg.x, fg.y, fg.z, fg.w}, uu[4] = {fu.x, fu.y, fu.z, fu.w};
@@ -649,13 +660,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
             }
             if (args.dbg_h) {
               uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) dh[q] = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+              dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+              dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              scratch[(size_t)((c * 2 + part) * 8 + 4 * hh + q) * BM + rl] =
-                  make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+            scratch[(size_t)((c * FC1_PARTS + part) * 4 + 2 * hh) * BM + rl] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            scratch[(size_t)((c * FC1_PARTS + part) * 4 + 2 * hh + 1) * BM + rl] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
           }
         }
         tc_fence_before();
@@ -669,8 +678,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
       }
       // ---- outer scale of the unit's rows: amax over the full d_ff row ----
       tl->rowmax[part][rl] = __uint_as_float(__vmaxu2(amax2, amax2 >> 16) << 16);
-      epi_barrier();
-      const float a = fmaxf(tl->rowmax[0][rl], tl->rowmax[1][rl]);
+      epi_barrier<FC1_NE>();
+      float a = tl->rowmax[0][rl];
+#pragma unroll
+      for (int p2 = 1; p2 < FC1_PARTS; ++p2) a = fmaxf(a, tl->rowmax[p2][rl]);
       if (have_prev && part == 0) args.h_g[row_prev] = g_prev;
       if (!*abort_flag && !is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
       have_prev = true;
@@ -687,13 +698,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc1_swiglu_kernel(const __grid_co
       if (part == 0) args.h_g[row_prev] = g_prev;
     }
   }
-  teardown(tl);
+  teardown<FC1_NE>(tl);
 }
 
 // ---------------------------------------------------------------------------
 // FC2 + router-weighted scatter
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_constant__ Fc2Args args) {
+__global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(const __grid_constant__ Fc2Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int d = args.d, k = args.k;
@@ -711,16 +722,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_c
   const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
   const size_t ring_bytes = (size_t)G.rings * (1 << G.log2_stages) * G.stage_bytes;
   const uint32_t ring_base = a_base + (uint32_t)a_bytes;
-  Tail* tl = setup(smem + a_bytes + ring_bytes);
+  Tail* tl = setup<FC2_NE>(smem + a_bytes + ring_bytes);
   float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ItemRows rows{false, d, args.d_ff};
   // per epilogue warp: 32 rows x 64 BF16 columns, 16-byte chunks XOR-swizzled by row
   const uint32_t stg = smem_u32(smem + a_bytes + ring_bytes + TAIL_BYTES + (size_t)2 * d * 4) +
-                       (uint32_t)(warp < NEPI_WARPS ? warp : 0) * 32 * FC2_STAGE_ROW;
+                       (uint32_t)(warp < FC2_NE ? warp : 0) * 32 * FC2_STAGE_ROW;
 
-  if (run_pipeline_roles(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
+  if (run_pipeline_roles<FC2_NE>(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
                          ring_base, tl, args.status)) {
     const int q4 = warp & 3, part = warp >> 2;
     const int rl = q4 * 32 + lane;
@@ -739,8 +750,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_c
       }
       const float gh = args.a_g[row];
       float* gws = gw_s + (uc & 1) * d;
-      stage_scales(gws, args.w_g + (int64_t)e * d, d, threadIdx.x);
-      epi_barrier();
+      stage_scales<FC2_NE>(gws, args.w_g + (int64_t)e * d, d, threadIdx.x);
+      epi_barrier<FC2_NE>();
       uint16_t* dst_row = args.slots + ((int64_t)(t < 0 ? 0 : t) * k + j) * d;
       for (int nt = 0; nt < G.items; ++nt, ++it) {
         const uint32_t slot = it % FC2_NSLOT;
@@ -801,7 +812,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) fc2_scatter_kernel(const __grid_c
       }
     }
   }
-  teardown(tl);
+  teardown<FC2_NE>(tl);
 }
 
 // ---------------------------------------------------------------------------
@@ -864,7 +875,7 @@ int launch_fc1(Fc1Args& a, cudaStream_t stream) {
   if (set_smem((const void*)fc1_swiglu_kernel, smem) != 0) return -1;
   const int grid = gemm_num_ctas();
   if (grid <= 0) return -1;
-  fc1_swiglu_kernel<<<grid, NTHREADS, smem, stream>>>(a);
+  fc1_swiglu_kernel<<<grid, Roles<FC1_NE>::THREADS, smem, stream>>>(a);
   return 0;
 }
 
@@ -875,7 +886,7 @@ int launch_fc2(Fc2Args& a, cudaStream_t stream) {
   if (set_smem((const void*)fc2_scatter_kernel, smem) != 0) return -1;
   const int grid = gemm_num_ctas();
   if (grid <= 0) return -1;
-  fc2_scatter_kernel<<<grid, NTHREADS, smem, stream>>>(a);
+  fc2_scatter_kernel<<<grid, Roles<FC2_NE>::THREADS, smem, stream>>>(a);
   return 0;
 }
 

@@ -563,6 +563,10 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
 // ---------------------------------------------------------------------------
 // FC1 + SwiGLU + requantisation
 // ---------------------------------------------------------------------------
+// DBG: also write the debug outputs (pre-cast FP32 u, h before
+// requantisation) when their pointers are set; the production launch uses
+// the instantiation without them.
+template <bool DBG>
 __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(const __grid_constant__ Fc1Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -651,14 +655,14 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
                 const uint32_t h2 = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
                 amax2 = __vmaxu2(amax2, h2 & 0x7FFF7FFFu);
                 hp[m >> 1] = h2;
-                if (args.dbg_u) {
+                if (DBG && args.dbg_u) {
                   float* du = args.dbg_u + row * 2 * d_ff;
                   du[nh + m] = yg0; du[nh + m + 1] = yg1;
                   du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
                 }
               }
             }
-            if (args.dbg_h) {
+            if (DBG && args.dbg_h) {
               uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
               dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
               dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
@@ -704,6 +708,9 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
 // ---------------------------------------------------------------------------
 // FC2 + router-weighted scatter
 // ---------------------------------------------------------------------------
+// DBG: also write the debug output (pre-weighting FP32 y2) when its pointer
+// is set.
+template <bool DBG>
 __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(const __grid_constant__ Fc2Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -744,8 +751,16 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
       int j = 0;
       float w = 0.0f;
       if (t >= 0) {
-        for (int jj = 0; jj < k; ++jj)
-          if (args.token_slot_row[(int64_t)t * k + jj] == (int)row) j = jj;
+        // slot of this row among the token's k (loads issued eight at a time)
+        const int32_t* ts = args.token_slot_row + (int64_t)t * k;
+        for (int j0 = 0; j0 < k; j0 += 8) {
+          int v8[8];
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) v8[q8] = j0 + q8 < k ? ts[j0 + q8] : -1;
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8)
+            if (v8[q8] == (int)row) j = j0 + q8;
+        }
         w = args.topk_w[(int64_t)t * k + j];
       }
       const float gh = args.a_g[row];
@@ -787,7 +802,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
                 const float y0 = __fmul_rn(__uint_as_float(R[hf][m]), __fmul_rn(gh, f[jj]));
                 const float y1 = __fmul_rn(__uint_as_float(R[hf][m + 1]), __fmul_rn(gh, f[jj + 1]));
                 zp[m >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
-                if (args.dbg_y && t >= 0) {
+                if (DBG && args.dbg_y && t >= 0) {
                   args.dbg_y[row * d + n0 + m] = y0;
                   args.dbg_y[row * d + n0 + m + 1] = y1;
                 }
@@ -872,10 +887,12 @@ static int set_smem(const void* kernel, size_t smem) {
 int launch_fc1(Fc1Args& a, cudaStream_t stream) {
   size_t smem;
   if (!plan(a.d, 2 * (a.d_ff / BN), 2 * a.d_ff, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem)) return -1;
-  if (set_smem((const void*)fc1_swiglu_kernel, smem) != 0) return -1;
+  const bool dbg = a.dbg_u != nullptr || a.dbg_h != nullptr;
+  void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true> : fc1_swiglu_kernel<false>;
+  if (set_smem((const void*)kern, smem) != 0) return -1;
   const int grid = gemm_num_ctas();
   if (grid <= 0) return -1;
-  fc1_swiglu_kernel<<<grid, Roles<FC1_NE>::THREADS, smem, stream>>>(a);
+  kern<<<grid, Roles<FC1_NE>::THREADS, smem, stream>>>(a);
   return 0;
 }
 
@@ -883,10 +900,11 @@ int launch_fc2(Fc2Args& a, cudaStream_t stream) {
   size_t smem;
   if (!plan(a.d_ff, a.d / BN, a.d, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident, &smem))
     return -1;
-  if (set_smem((const void*)fc2_scatter_kernel, smem) != 0) return -1;
+  void (*kern)(const Fc2Args) = a.dbg_y != nullptr ? fc2_scatter_kernel<true> : fc2_scatter_kernel<false>;
+  if (set_smem((const void*)kern, smem) != 0) return -1;
   const int grid = gemm_num_ctas();
   if (grid <= 0) return -1;
-  fc2_scatter_kernel<<<grid, Roles<FC2_NE>::THREADS, smem, stream>>>(a);
+  kern<<<grid, Roles<FC2_NE>::THREADS, smem, stream>>>(a);
   return 0;
 }
 

@@ -20,9 +20,9 @@ __device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
   return va > vb || (va == vb && ea < eb);
 }
 
-// One CTA per chunk of 256 tokens, sixteen warps, one warp per token at a time.
+// One CTA per chunk of 256 tokens, 32 warps, one warp per token at a time.
 template <int NPL>
-__global__ void __launch_bounds__(512) route_kernel(const float* __restrict__ logits,
+__global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits,
                                                    const int32_t* __restrict__ ext_ids,
                                                    const float* __restrict__ ext_w, int T, int E, int k,
                                                    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
@@ -131,7 +131,7 @@ int launch_route(const float* logits, const int32_t* ext_ids, const float* ext_w
   const size_t smem = (size_t)E * (kChunk / 32) * sizeof(uint32_t);
   const int npl = (E + 31) / 32;
 #define MOE_ROUTE(N)                                                                                 \
-  route_kernel<N><<<C, 512, smem, stream>>>(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, \
+  route_kernel<N><<<C, 1024, smem, stream>>>(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, \
                                            token_slot_row, hist, status)
   if (npl <= 1) MOE_ROUTE(1);
   else if (npl <= 2) MOE_ROUTE(2);

@@ -79,6 +79,9 @@ def lib():
                 "orc_e4m3_first_input_of_code": (I64, [ctypes.c_uint8]),
                 "orc_e2m1_first_input_of_code": (I64, [ctypes.c_uint8]),
                 "orc_num_threads": (I32, []),
+                "orc_rht16_rows": (None, [P, I64, I32, P, P]),
+                "orc_quantize_tensor": (None, [P, I64, I32, P, P, P]),
+                "orc_quantize_weights_per_expert": (None, [P, I32, I32, I32, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -353,3 +356,45 @@ class TokenOracle:
 
 def num_threads():
     return int(lib().orc_num_threads())
+
+
+# --------------------------------------------------------------------------
+# contrast recipes (not the hot path's recipe)
+# --------------------------------------------------------------------------
+def rht16_rows(x_f32, signs16):
+    """Blockwise 16-point random Hadamard transform of FP32 rows."""
+    x = _c(x_f32, np.float32)
+    rows, K = x.shape
+    y = np.zeros_like(x)
+    lib().orc_rht16_rows(_p(x), rows, K, _p(_c(signs16, np.int8)), _p(y))
+    return y
+
+
+def quantize_tensor(x_f32):
+    """Per-tensor NVFP4: (codes, sf_swz, g [rows]) with one shared g."""
+    x = _c(x_f32, np.float32)
+    rows, K = x.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros(max(sf_bytes(rows, K), 1), np.uint8)
+    g = np.zeros(rows, np.float32)
+    lib().orc_quantize_tensor(_p(x), rows, K, _p(codes), _p(sf), _p(g))
+    return codes, sf, g
+
+
+def quantize_per_tensor_rht(x_bf16, signs16):
+    """The RHT-enabled per-tensor contrast reference: BF16 rows -> FP32 ->
+    blockwise RHT -> per-tensor NVFP4."""
+    x = bf16_bits_to_f32(_c(x_bf16, np.uint16))
+    return quantize_tensor(rht16_rows(x, signs16))
+
+
+def quantize_weights_per_expert(W_bf16):
+    """Weights [E][N][K] (BF16 bits) with one outer scale per expert tensor:
+    (codes [E][N][K/2], sf_swz, g [E][N] with g[e][:] = g_e)."""
+    W = _c(W_bf16, np.uint16)
+    E, N, K = W.shape
+    codes = np.zeros((E, N, K // 2), np.uint8)
+    sf = np.zeros(max(sf_bytes(E * N, K), 1), np.uint8)
+    g = np.zeros((E, N), np.float32)
+    lib().orc_quantize_weights_per_expert(_p(W), E, N, K, _p(codes), _p(sf), _p(g))
+    return codes, sf, g

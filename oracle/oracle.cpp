@@ -463,3 +463,59 @@ int orc_num_threads(void) {
 }
 
 }  // extern "C"
+
+/* ---- contrast recipes ---- */
+
+/* Blockwise 16-point random Hadamard transform ([SUM-M] contrast). */
+void orc_rht16_rows(const float* x, int64_t rows, int K, const int8_t* signs16, float* y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < K / 16; ++b) {
+            const float* xb = x + r * K + 16 * b;
+            float* yb = y + r * K + 16 * b;
+            for (int i = 0; i < 16; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < 16; ++j) {
+                    const int hij = (__builtin_popcount((unsigned)(i & j)) & 1) ? -1 : 1;
+                    acc += (double)(hij * signs16[j]) * (double)xb[j];
+                }
+                yb[i] = (float)(acc * 0.25);
+            }
+        }
+    }
+}
+
+/* One outer scale for the whole tensor ([RB-P] scale-granularity choice). */
+void orc_quantize_tensor(const float* x, int64_t rows, int K, uint8_t* codes, uint8_t* sf_swz, float* g_out) {
+    float a = 0.0f;
+    for (int64_t i = 0; i < rows * (int64_t)K; ++i) a = std::max(a, std::fabs(x[i]));
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        std::vector<uint8_t> sf((size_t)K / 16, 0);
+        float gr = 0.0f;
+        orc_quantize_row(x + r * K, K, a, codes + r * (K / 2), sf.data(), &gr);
+        g_out[r] = gr;
+        for (int c = 0; c < K / 16; ++c) sf_swz[orc_sf_offset(r, c, K)] = sf[c];
+    }
+}
+
+/* Per-expert weight outer scale ("miniTE CUTLASS", [TR 4.3] table). */
+void orc_quantize_weights_per_expert(const uint16_t* W, int E, int N, int K, uint8_t* codes, uint8_t* sf_swz,
+                                     float* g) {
+    for (int e = 0; e < E; ++e) {
+        float a = 0.0f;
+        const uint16_t* we = W + (int64_t)e * N * K;
+        for (int64_t i = 0; i < (int64_t)N * K; ++i) a = std::max(a, std::fabs(orc_bf16_to_f32(we[i])));
+#pragma omp parallel for schedule(static)
+        for (int n = 0; n < N; ++n) {
+            const int64_t r = (int64_t)e * N + n;
+            std::vector<float> v((size_t)K);
+            std::vector<uint8_t> sf((size_t)K / 16, 0);
+            for (int j = 0; j < K; ++j) v[j] = orc_bf16_to_f32(we[(int64_t)n * K + j]);
+            float gr = 0.0f;
+            orc_quantize_row(v.data(), K, a, codes + r * (K / 2), sf.data(), &gr);
+            g[r] = gr;
+            for (int c = 0; c < K / 16; ++c) sf_swz[orc_sf_offset(r, c, K)] = sf[c];
+        }
+    }
+}

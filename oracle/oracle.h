@@ -97,6 +97,29 @@ int64_t orc_e4m3_first_input_of_code(uint8_t code);
 int64_t orc_e2m1_first_input_of_code(uint8_t code);
 int     orc_num_threads(void);
 
+/* ---- contrast recipes (not the hot path's recipe) ---- */
+
+/* Random Hadamard transform along K in blocks of 16, a contrast reference
+ * for the recipe the pages switch off ([SUM-M]: Hadamard transforms off, so
+ * a token's codes do not depend on the other tokens of its batch):
+ *   y[16b + i] = RN_f32( (1/4) * sum_j H[i][j] * s[j] * x[16b + j] ),
+ * H the 16x16 Sylvester Hadamard matrix (H[i][j] = (-1)^popcount(i & j)),
+ * s a +-1 sign vector of length 16; evaluated in FP64, rounded once. */
+void orc_rht16_rows(const float* x, int64_t rows, int K, const int8_t* signs16, float* y);
+
+/* Per-tensor NVFP4 quantisation of FP32 rows: one outer scale
+ * g = amax(all rows) / 2688 shared by every row ([RB-P]: the outer scale's
+ * granularity, per-tensor / per-row / per-token, is a recipe choice), block
+ * scales and codes as orc_quantize_row.  g_out[r] = g for every row. */
+void orc_quantize_tensor(const float* x, int64_t rows, int K, uint8_t* codes, uint8_t* sf_swz, float* g_out);
+
+/* Weights with one outer scale per expert tensor ("miniTE CUTLASS" column of
+ * [TR 4.3]'s table): for expert e, g_e = max |W_e| / 2688 over its N x K
+ * entries; every row of the expert is quantised with that amax.
+ * g[e][n] = g_e for all n. */
+void orc_quantize_weights_per_expert(const uint16_t* W, int E, int N, int K, uint8_t* codes, uint8_t* sf_swz,
+                                     float* g);
+
 #ifdef __cplusplus
 }
 #endif

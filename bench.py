@@ -200,7 +200,7 @@ def native(args):
     W1 = torch.stack([to_dev(lay.w1_expert(e)) for e in range(E)])
     W2 = torch.stack([to_dev(lay.w2_expert(e)) for e in range(E)])
     w1q, w2q = M.quantize_weights(W1), M.quantize_weights(W2)
-    del W1, W2
+    w1e, w2e = M.quantize_weights_per_expert(W1), M.quantize_weights_per_expert(W2)
     x_np, lg_np = make_inputs(lay, shard_seed(args.seed, rank))
     x, lg = to_dev(x_np), to_dev(lg_np)
     out = torch.empty((T, d), dtype=torch.int16, device=dev)
@@ -264,6 +264,32 @@ def native(args):
         v["row_to_token"], v["token_slot_row"], v["topk_w"], T, k, slots2, out, None, status, stream))
 
     peaks, peak_kind = load_peaks()
+
+    # ---- weight quantisation (once per optimizer step, outside the forward):
+    # the per-row recipe and the per-expert recipe, W1 and W2 each call ----
+    def quant_rows():
+        M.moe_nvfp4_quantize_weights(W1, w1q["codes"], w1q["sf"], w1q["g"], status, stream)
+        M.moe_nvfp4_quantize_weights(W2, w2q["codes"], w2q["sf"], w2q["g"], status, stream)
+
+    def quant_expert():
+        M.moe_nvfp4_quantize_weights_per_expert(W1, w1e["codes"], w1e["sf"], w1e["g"], w1e["amax_e"], status,
+                                                 stream)
+        M.moe_nvfp4_quantize_weights_per_expert(W2, w2e["codes"], w2e["sf"], w2e["g"], w2e["amax_e"], status,
+                                                 stream)
+
+    t_wq_row, t_wq_exp = timed(quant_rows), timed(quant_expert)
+    wq_bytes = sum(W.numel() * 2 + W.numel() // 2 + W.numel() // 16 + W.shape[0] * W.shape[1] * 4 for W in (W1, W2))
+    t_fwd_exp = timed(lambda: M.moe_expert_forward(x, lg, T, E, k, d, F, w1e["codes"], w1e["sf"], w1e["g"],
+                                                   w2e["codes"], w2e["sf"], w2e["g"], out, ws, status, stream))
+    del W1, W2
+    wq = lambda t: {"ms": round(t * 1e3, 4), "achieved": round(wq_bytes / t / 1e9, 1), "unit": "GB/s",
+                    "frac": round(wq_bytes / t / 1e9 / peaks["hbm_gbs"], 4)}
+    next_rows = {"weight_quant_per_row": dict(wq(t_wq_row), launches=2),
+                 "weight_quant_per_expert": dict(wq(t_wq_exp), launches=4,
+                                                 note="two passes over W: expert amax, then encode"),
+                 "forward_per_expert_weights": {"value": round(T / t_fwd_exp, 1), "unit": UNIT,
+                                                "ms_per_step": round(t_fwd_exp * 1e3, 4)},
+                 "algorithmic_bytes_weight_quant": int(wq_bytes)}
     alg = algorithmic(lay)
     fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
     fc1_tflops = alg["fc1_flops"] / t_fc1 / 1e12
@@ -313,7 +339,7 @@ def native(args):
             "config": {"workload": args.workload, "T": T, "d": d, "E": E, "k": k, "d_ff": F,
                        "parallelism": "token data parallel x%d" % world, "l2": "inputs larger than L2 (no flush)"},
             "gpu_launches": 7 * args.steps, "roofline": roofline, "roofline_hbm": roofline_hbm,
-            "clocks": clocks, "e2e": e2e}
+            "clocks": clocks, "e2e": e2e, "next_rows": next_rows}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(lay, args)
     if rank == 0:

@@ -138,6 +138,27 @@ int moe_nvfp4_quantize_weights(const uint16_t* W, int E, int N, int K,
                                uint8_t* codes, uint8_t* sf, float* g,
                                int* status, void* stream);
 
+/* NVFP4 quantisation of expert weights with ONE outer scale per expert
+ * weight tensor (Technical Report section 4.3 table, "miniTE CUTLASS"
+ * column, recipe nvfp4_cursor2_cutlass_v2; the per-row variant above is the
+ * "miniTE per-token" column).  g_e = max|W_e| / (6 * 448); block scales and
+ * codes follow the section 5.1 equation with that g_e for every row of
+ * expert e.  g_e is written replicated into g[e][0..N-1], so the grouped
+ * GEMMs consume the result unchanged (their epilogue multiplies by
+ * g_x * g_w of the row).
+ *   W, codes, sf, g, shapes   as moe_nvfp4_quantize_weights
+ *   amax_e f32 [E]  (out) max |W_e| of each expert; also the accumulator of
+ *                   the reduction, so it must not alias W, codes, sf or g
+ * Two launches and one memset on `stream`: zero amax_e, per-expert maximum
+ * (integer atomicMax on the bits of non-negative floats), then the row
+ * quantiser.  NaN/Inf weights set MOE_STATUS_NONFINITE_WEIGHT; NaNs do not
+ * enter the maximum.  Errors as moe_nvfp4_quantize_weights, plus
+ * MOE_ERR_CUDA if the memset cannot be enqueued. */
+int moe_nvfp4_quantize_weights_per_expert(const uint16_t* W, int E, int N,
+                                          int K, uint8_t* codes, uint8_t* sf,
+                                          float* g, float* amax_e, int* status,
+                                          void* stream);
+
 /* Route, permute, pad, expert offsets, and per-token amax gathered in the
  * same pass (rainbus summary, method step 6: sort fused with the amax scan,
  * padding carries the statistics; AI summary methodology: no separate amax

@@ -48,6 +48,7 @@ _SIGS = {
     "moe_expert_forward_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
     "moe_expert_forward_workspace_layout": (I32, [I32, I32, I32, I32, I32, P]),
     "moe_nvfp4_quantize_weights": (I32, [P, I32, I32, I32, P, P, P, P, P]),
+    "moe_nvfp4_quantize_weights_per_expert": (I32, [P, I32, I32, I32, P, P, P, P, P, P]),
     "moe_permute_amax": (I32, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_permute_amax_noalloc": (I32, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P]),
     "nvfp4_quantize_rows": (I32, [P, I32, I32, P, P, I32, P, P, P, P, P]),
@@ -140,6 +141,12 @@ def moe_nvfp4_quantize_weights(W, codes, sf, g, status=None, stream=None):
            lib().moe_nvfp4_quantize_weights(_p(W), E, N, K, _p(codes), _p(sf), _p(g), _p(status), _s(stream)))
 
 
+def moe_nvfp4_quantize_weights_per_expert(W, codes, sf, g, amax_e, status=None, stream=None):
+    E, N, K = W.shape
+    _check("moe_nvfp4_quantize_weights_per_expert", lib().moe_nvfp4_quantize_weights_per_expert(
+        _p(W), E, N, K, _p(codes), _p(sf), _p(g), _p(amax_e), _p(status), _s(stream)))
+
+
 def moe_permute_amax(logits, ext_ids, ext_w, x, T, E, k, d, topk_ids, topk_w, counts, offsets,
                      row_to_token, token_slot_row, amax_tok, amax_row, ws, status=None, stream=None):
     _check("moe_permute_amax", lib().moe_permute_amax(
@@ -207,6 +214,19 @@ def quantize_weights(W):
     E, N, K = W.shape
     q = empty_quantized(E * N, K, W.device)
     moe_nvfp4_quantize_weights(W, q["codes"], q["sf"], q["g"])
+    q["codes"] = q["codes"].view(E, N, K // 2)
+    q["g"] = q["g"].view(E, N)
+    return q
+
+
+def quantize_weights_per_expert(W):
+    """quantize_weights with one outer scale per expert tensor; the dict also
+    holds amax_e [E] = max |W_e|."""
+    import torch
+    E, N, K = W.shape
+    q = empty_quantized(E * N, K, W.device)
+    q["amax_e"] = torch.empty(E, dtype=torch.float32, device=W.device)
+    moe_nvfp4_quantize_weights_per_expert(W, q["codes"], q["sf"], q["g"], q["amax_e"])
     q["codes"] = q["codes"].view(E, N, K // 2)
     q["g"] = q["g"].view(E, N)
     return q

@@ -166,8 +166,21 @@ int moe_nvfp4_quantize_weights(const uint16_t* W, int E, int N, int K, uint8_t* 
     return MOE_ERR_SHAPE;
   int rc = check_device();
   if (rc != MOE_OK) return rc;
-  moe::launch_quantize_rows(W, (int64_t)E * N, K, nullptr, nullptr, (int64_t)E * N, codes, sf, g, status,
+  moe::launch_quantize_rows(W, (int64_t)E * N, K, nullptr, nullptr, 1, (int64_t)E * N, codes, sf, g, status,
                             MOE_STATUS_NONFINITE_WEIGHT, (cudaStream_t)stream);
+  return finish();
+}
+
+int moe_nvfp4_quantize_weights_per_expert(const uint16_t* W, int E, int N, int K, uint8_t* codes, uint8_t* sf,
+                                          float* g, float* amax_e, int* status, void* stream) {
+  if (!ok_ptr(W) || !ok_ptr(codes) || !ok_ptr(sf) || !ok_ptr(g) || !ok_ptr(amax_e) || !ok_opt(status))
+    return MOE_ERR_POINTER;
+  if (E < 1 || N < 128 || N % 128 != 0 || K < 64 || K > 4096 || K % 64 != 0 || (int64_t)E * N >= (int64_t(1) << 31))
+    return MOE_ERR_SHAPE;
+  int rc = check_device();
+  if (rc != MOE_OK) return rc;
+  if (moe::launch_quantize_weights_per_expert(W, E, N, K, codes, sf, g, amax_e, status, (cudaStream_t)stream) != 0)
+    return MOE_ERR_CUDA;
   return finish();
 }
 
@@ -180,7 +193,7 @@ int nvfp4_quantize_rows(const uint16_t* src, int src_rows, int K, const int32_t*
   if (!row_map && dst_rows > src_rows) return MOE_ERR_SHAPE;
   int rc = check_device();
   if (rc != MOE_OK) return rc;
-  moe::launch_quantize_rows(src, src_rows, K, row_map, amax, dst_rows, codes, sf, g, status, MOE_STATUS_NONFINITE_X,
+  moe::launch_quantize_rows(src, src_rows, K, row_map, amax, 1, dst_rows, codes, sf, g, status, MOE_STATUS_NONFINITE_X,
                             (cudaStream_t)stream);
   return finish();
 }

@@ -8,9 +8,15 @@ namespace moe {
 
 constexpr int kRouteChunk = 256;  // tokens per routing chunk (one CTA)
 
+// amax (optional) holds one entry per amax_rows consecutive source rows.
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,
-                         const float* amax, int64_t dst_rows, uint8_t* codes, uint8_t* sf, float* g,
-                         int* status, int nonfinite_bit, cudaStream_t stream);
+                         const float* amax, int64_t amax_rows, int64_t dst_rows, uint8_t* codes, uint8_t* sf,
+                         float* g, int* status, int nonfinite_bit, cudaStream_t stream);
+
+// Per-expert max |W| into amax_e[E], then the row quantiser with that amax
+// for all N rows of each expert.  Returns -1 if the memset fails to enqueue.
+int launch_quantize_weights_per_expert(const uint16_t* W, int E, int N, int K, uint8_t* codes, uint8_t* sf, float* g,
+                                       float* amax_e, int* status, cudaStream_t stream);
 
 // Routing: top-k, weights, in-chunk ranks (into token_slot_row) and chunk
 // histograms hist[C][E].

@@ -18,7 +18,7 @@ __device__ __forceinline__ int64_t sf_word_offset(int64_t row, int c4, int kgrou
 template <int MAXCH>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(
     const uint16_t* __restrict__ src, int64_t src_rows, int K, const int32_t* __restrict__ row_map,
-    const float* __restrict__ amax, int64_t dst_rows, uint8_t* __restrict__ codes,
+    const float* __restrict__ amax, int64_t amax_rows, int64_t dst_rows, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ sf, float* __restrict__ gout, int* status, int nonfinite_bit) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
     }
   }
   if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, nonfinite_bit);
-  a = amax ? amax[s] : warp_max(a);
+  a = amax ? amax[s / amax_rows] : warp_max(a);
   const float g = __fdiv_rn(a, 2688.0f);
   const float den = __fmul_rn(6.0f, g);
 #pragma unroll
@@ -79,18 +79,77 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
 }
 
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,
-                         const float* amax, int64_t dst_rows, uint8_t* codes, uint8_t* sf, float* g,
-                         int* status, int nonfinite_bit, cudaStream_t stream) {
+                         const float* amax, int64_t amax_rows, int64_t dst_rows, uint8_t* codes, uint8_t* sf,
+                         float* g, int* status, int nonfinite_bit, cudaStream_t stream) {
   if (dst_rows <= 0) return 0;
   const int nch = (K / 8 + 31) / 32;
   const dim3 grid((unsigned)((dst_rows + 7) / 8));
   if (nch <= 4)
-    quantize_rows_kernel<4><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, dst_rows, codes, sf, g, status, nonfinite_bit);
+    quantize_rows_kernel<4><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes, sf,
+                                                      g, status, nonfinite_bit);
   else if (nch <= 8)
-    quantize_rows_kernel<8><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, dst_rows, codes, sf, g, status, nonfinite_bit);
+    quantize_rows_kernel<8><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes, sf,
+                                                      g, status, nonfinite_bit);
   else
-    quantize_rows_kernel<16><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, dst_rows, codes, sf, g, status, nonfinite_bit);
+    quantize_rows_kernel<16><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes,
+                                                       sf, g, status, nonfinite_bit);
   return 0;
+}
+
+// max |W_e| of each expert tensor (one outer scale per expert weight tensor:
+// miniTE Technical Report section 4.3 table, "miniTE CUTLASS" column).
+// blockIdx.y is the expert; the blocks of one expert stride over its N*K
+// values with 128-bit loads, reduce in shared memory and fold their maximum
+// into amax_e[e] with one integer atomicMax on the float's bits (valid
+// because every candidate is >= +0, and amax_e starts at +0).  NaNs do not
+// win a maximum; the quantiser flags them.
+__global__ void __launch_bounds__(256) expert_amax_kernel(const uint16_t* __restrict__ W, int64_t per_expert,
+                                                          float* __restrict__ amax_e) {
+  const uint4* src = reinterpret_cast<const uint4*>(W + (int64_t)blockIdx.y * per_expert);
+  const int64_t n8 = per_expert / 8;
+  const int64_t stride = (int64_t)gridDim.x * 256;
+  float a = 0.0f;
+  int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+    }
+  }
+  for (; i < n8; i += stride) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+  }
+  a = warp_max(a);
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    a = threadIdx.x < 8 ? red[threadIdx.x] : 0.0f;
+    a = warp_max(a);
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_e + blockIdx.y), __float_as_uint(a));
+  }
+}
+
+int launch_quantize_weights_per_expert(const uint16_t* W, int E, int N, int K, uint8_t* codes, uint8_t* sf, float* g,
+                                       float* amax_e, int* status, cudaStream_t stream) {
+  if (cudaMemsetAsync(amax_e, 0, (size_t)E * sizeof(float), stream) != cudaSuccess) return -1;
+  const int64_t per_expert = (int64_t)N * K;
+  // about eight resident 256-thread blocks per SM over all experts, and no
+  // block without work
+  const int64_t want = (8 * 152 + E - 1) / E;
+  const int64_t most = (per_expert / 8 + 255) / 256;
+  const unsigned gx = (unsigned)(want < most ? want : most);
+  expert_amax_kernel<<<dim3(gx, (unsigned)E), 256, 0, stream>>>(W, per_expert, amax_e);
+  return launch_quantize_rows(W, (int64_t)E * N, K, nullptr, amax_e, N, (int64_t)E * N, codes, sf, g, status,
+                              MOE_STATUS_NONFINITE_WEIGHT, stream);
 }
 
 }  // namespace moe

@@ -16,10 +16,10 @@ def L():
 
 def test_exports_every_header_function(L):
     names = M.header_functions()
-    assert len(names) == 15, names
+    assert len(names) == 16, names
     for n in names:
         assert hasattr(L, n), n
-    for n in ["moe_nvfp4_quantize_weights", "moe_permute_amax", "nvfp4_quantize_rows",
+    for n in ["moe_nvfp4_quantize_weights", "moe_nvfp4_quantize_weights_per_expert", "moe_permute_amax", "nvfp4_quantize_rows",
               "nvfp4_grouped_gemm_fc1_swiglu", "nvfp4_grouped_gemm_fc2_unpermute", "moe_expert_forward"]:
         assert n in names
 
@@ -75,6 +75,11 @@ def test_entry_points_reject_bad_arguments(L):
     assert L.moe_nvfp4_quantize_weights(FAKE, 2, 100, 64, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert L.moe_nvfp4_quantize_weights(FAKE, 2, 128, 48, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert L.moe_nvfp4_quantize_weights(None, 2, 128, 64, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_POINTER
+    qe = L.moe_nvfp4_quantize_weights_per_expert
+    assert qe(FAKE, 2, 100, 64, FAKE, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
+    assert qe(FAKE, 0, 128, 64, FAKE, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
+    assert qe(FAKE, 2, 128, 64, FAKE, FAKE, FAKE, None, None, None) == M.MOE_ERR_POINTER
+    assert qe(FAKE, 2, 128, 64, FAKE, FAKE, FAKE, MIS, None, None) == M.MOE_ERR_POINTER
     assert L.nvfp4_quantize_rows(FAKE, 4, 100, None, None, 4, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert L.nvfp4_quantize_rows(FAKE, 4, 64, None, None, 5, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert L.nvfp4_quantize_rows(FAKE, 4, 64, MIS, None, 4, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_POINTER

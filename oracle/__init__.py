@@ -82,6 +82,9 @@ def lib():
                 "orc_rht16_rows": (None, [P, I64, I32, P, P]),
                 "orc_quantize_tensor": (None, [P, I64, I32, P, P, P]),
                 "orc_quantize_weights_per_expert": (None, [P, I32, I32, I32, P, P, P]),
+                "orc_bwd_router": (None, [P, P, P, P, P, I64, I32, I32, I32, P, P]),
+                "orc_bwd_dy2": (None, [P, P, P, I64, I32, I32, I64, P]),
+                "orc_bwd_expert": (None, [P, P, P, P, I64, I32, I32, P, P, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -398,3 +401,84 @@ def quantize_weights_per_expert(W_bf16):
     g = np.zeros((E, N), np.float32)
     lib().orc_quantize_weights_per_expert(_p(W), E, N, K, _p(codes), _p(sf), _p(g))
     return codes, sf, g
+
+
+# --------------------------------------------------------------------------
+# backward: straight-through estimator, BF16 GEMM operands (orc_bwd_* in
+# oracle.h state the formulas and the passages they follow)
+# --------------------------------------------------------------------------
+def bwd_router(dY_bf16, y2, w, ids, token_slot_row, E):
+    dY = _c(dY_bf16, np.uint16)
+    T, d = dY.shape
+    k = ids.shape[1]
+    dw = np.zeros((T, k), np.float32)
+    dl = np.zeros((T, E), np.float32)
+    lib().orc_bwd_router(_p(dY), _p(_c(y2, np.float32)), _p(_c(w, np.float32)), _p(_c(ids, np.int32)),
+                         _p(_c(token_slot_row, np.int32)), T, k, d, E, _p(dw), _p(dl))
+    return dw, dl
+
+
+def bwd_dy2(dY_bf16, w, token_slot_row, M):
+    dY = _c(dY_bf16, np.uint16)
+    T, d = dY.shape
+    k = w.shape[1]
+    out = np.zeros((M, d), np.uint16)
+    lib().orc_bwd_dy2(_p(dY), _p(_c(w, np.float32)), _p(_c(token_slot_row, np.int32)), T, k, d, M, _p(out))
+    return out
+
+
+def bwd_expert(dy2_rows, u_rows, h_rows, x_rows, W1e, W2e):
+    """One expert over the given rows: (du BF16 [n][2F], dxr FP64 [n][d],
+    dW1 FP32 [2F][d], dW2 FP32 [d][F])."""
+    dy2 = _c(dy2_rows, np.uint16)
+    n, d = dy2.shape
+    F = W2e.shape[1]
+    du = np.zeros((n, 2 * F), np.uint16)
+    dxr = np.zeros((n, d), np.float64)
+    dW1 = np.zeros((2 * F, d), np.float32)
+    dW2 = np.zeros((d, F), np.float32)
+    lib().orc_bwd_expert(_p(dy2), _p(_c(u_rows, np.uint16)), _p(_c(h_rows, np.uint16)), _p(_c(x_rows, np.uint16)),
+                         n, d, F, _p(_c(W1e, np.uint16)), _p(_c(W2e, np.uint16)), _p(du), _p(dxr), _p(dW1), _p(dW2))
+    return du, dxr, dW1, dW2
+
+
+def gather_x_rows(x_bf16, row_to_token):
+    """BF16 input row of each permuted row's token, zero on pad rows (a
+    gather, no arithmetic)."""
+    x = _c(x_bf16, np.uint16)
+    r2t = np.asarray(row_to_token)
+    out = np.zeros((r2t.shape[0], x.shape[1]), np.uint16)
+    real = r2t >= 0
+    out[real] = x[r2t[real]]
+    return out
+
+
+def moe_backward(dY_bf16, x_bf16, W1_bf16, W2_bf16, fwd):
+    """Straight-through backward of moe_forward's result `fwd` (its ids, w,
+    permutation, u, h and y2 are the saved values).  Returns dx FP32 [T][d]
+    (sum over the token's slots in FP64, rounded once), dW1 FP32 [E][2F][d],
+    dW2 FP32 [E][d][F], dw FP32 [T][k], dlogits FP32 [T][E], and the BF16
+    GEMM operands dy2 [M][d] and du [M][2F] (M = padded rows)."""
+    W1, W2 = _c(W1_bf16, np.uint16), _c(W2_bf16, np.uint16)
+    E, F2, d = W1.shape
+    F = F2 // 2
+    perm = fwd["perm"]
+    M = perm["m_pad"]
+    offs = perm["offsets"]
+    T = x_bf16.shape[0]
+    dw, dl = bwd_router(dY_bf16, fwd["y2"], fwd["w"], fwd["ids"], perm["token_slot_row"], E)
+    dy2 = bwd_dy2(dY_bf16, fwd["w"], perm["token_slot_row"], M)
+    xr = gather_x_rows(x_bf16, perm["row_to_token"][:M])
+    du = np.zeros((M, F2), np.uint16)
+    dxr = np.zeros((M, d), np.float64)
+    dW1 = np.zeros((E, F2, d), np.float32)
+    dW2 = np.zeros((E, d, F), np.float32)
+    u, h = np.asarray(fwd["u"]), np.asarray(fwd["h"])
+    for e in range(E):
+        a, b = int(offs[e]), int(offs[e + 1])
+        if a == b:
+            continue
+        du[a:b], dxr[a:b], dW1[e], dW2[e] = bwd_expert(dy2[a:b], u[a:b], h[a:b], xr[a:b], W1[e], W2[e])
+    tsr = perm["token_slot_row"]
+    dx = dxr[tsr].sum(axis=1).astype(np.float32) if T > 0 else np.zeros((0, d), np.float32)
+    return dict(dx=dx, dW1=dW1, dW2=dW2, dw=dw, dlogits=dl, dy2=dy2, du=du, dxr=dxr)

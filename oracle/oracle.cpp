@@ -519,3 +519,87 @@ void orc_quantize_weights_per_expert(const uint16_t* W, int E, int N, int K, uin
         }
     }
 }
+
+/* ---- backward ---- */
+
+void orc_bwd_router(const uint16_t* dY, const float* y2, const float* w, const int32_t* ids,
+                    const int32_t* token_slot_row, int64_t T, int k, int d, int E, float* dw, float* dlogits) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        std::vector<double> g((size_t)k);
+        for (int j = 0; j < k; ++j) {
+            const int64_t r = token_slot_row[t * k + j];
+            double s = 0.0;
+            for (int n = 0; n < d; ++n) s += (double)orc_bf16_to_f32(dY[t * d + n]) * (double)y2[r * d + n];
+            g[j] = s;
+            dw[t * k + j] = (float)s;
+        }
+        double mean = 0.0;
+        for (int j = 0; j < k; ++j) mean += (double)w[t * k + j] * g[j];
+        for (int e = 0; e < E; ++e) dlogits[t * E + e] = 0.0f;
+        for (int j = 0; j < k; ++j) dlogits[t * E + ids[t * k + j]] = (float)((double)w[t * k + j] * (g[j] - mean));
+    }
+}
+
+void orc_bwd_dy2(const uint16_t* dY, const float* w, const int32_t* token_slot_row, int64_t T, int k, int d,
+                 int64_t M, uint16_t* dy2) {
+    for (int64_t i = 0; i < M * d; ++i) dy2[i] = 0;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int64_t r = token_slot_row[t * k + j];
+            const float wj = w[t * k + j];
+            for (int n = 0; n < d; ++n) {
+                const float p = wj * orc_bf16_to_f32(dY[t * d + n]);  // one FP32 rounding
+                dy2[r * d + n] = orc_f32_to_bf16(p);
+            }
+        }
+}
+
+void orc_bwd_expert(const uint16_t* dy2, const uint16_t* u, const uint16_t* h, const uint16_t* xr, int64_t n,
+                    int d, int F, const uint16_t* W1, const uint16_t* W2, uint16_t* du, double* dxr, float* dW1,
+                    float* dW2) {
+    const int F2 = 2 * F;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        std::vector<double> dh((size_t)F, 0.0);
+        for (int m = 0; m < d; ++m) {
+            const double a = orc_bf16_to_f32(dy2[r * d + m]);
+            if (a == 0.0) continue;
+            for (int f = 0; f < F; ++f) dh[f] += a * (double)orc_bf16_to_f32(W2[(int64_t)m * F + f]);
+        }
+        for (int f = 0; f < F; ++f) {
+            const double g = orc_bf16_to_f32(u[r * F2 + f]);
+            const double v = orc_bf16_to_f32(u[r * F2 + F + f]);
+            const double s = 1.0 / (1.0 + std::exp(-g));
+            du[r * F2 + f] = orc_f64_to_bf16(dh[f] * v * s * (1.0 + g * (1.0 - s)));
+            du[r * F2 + F + f] = orc_f64_to_bf16(dh[f] * g * s);
+        }
+        for (int i = 0; i < d; ++i) dxr[r * d + i] = 0.0;
+        for (int j = 0; j < F2; ++j) {
+            const double a = orc_bf16_to_f32(du[r * F2 + j]);
+            if (a == 0.0) continue;
+            for (int i = 0; i < d; ++i) dxr[r * d + i] += a * (double)orc_bf16_to_f32(W1[(int64_t)j * d + i]);
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < d; ++m) {
+        std::vector<double> acc((size_t)F, 0.0);
+        for (int64_t r = 0; r < n; ++r) {
+            const double a = orc_bf16_to_f32(dy2[r * d + m]);
+            if (a == 0.0) continue;
+            for (int f = 0; f < F; ++f) acc[f] += a * (double)orc_bf16_to_f32(h[r * F + f]);
+        }
+        for (int f = 0; f < F; ++f) dW2[(int64_t)m * F + f] = (float)acc[f];
+    }
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < F2; ++j) {
+        std::vector<double> acc((size_t)d, 0.0);
+        for (int64_t r = 0; r < n; ++r) {
+            const double a = orc_bf16_to_f32(du[r * F2 + j]);
+            if (a == 0.0) continue;
+            for (int i = 0; i < d; ++i) acc[i] += a * (double)orc_bf16_to_f32(xr[r * d + i]);
+        }
+        for (int i = 0; i < d; ++i) dW1[(int64_t)j * d + i] = (float)acc[i];
+    }
+}

@@ -120,6 +120,45 @@ void orc_quantize_tensor(const float* x, int64_t rows, int K, uint8_t* codes, ui
 void orc_quantize_weights_per_expert(const uint16_t* W, int E, int N, int K, uint8_t* codes, uint8_t* sf_swz,
                                      float* g);
 
+/* ---- backward (straight-through, BF16 GEMM operands) ----
+ *
+ * [SUM-M] and the main paper's contributions list: the backward is a
+ * straight-through estimator on the saved original BF16 activations and
+ * weights, with no backward quantisation; [RB-S] step 5: BF16 GEMMs on the
+ * saved BF16 operands.  [TR 4.3] (text below the table): the layer bypass
+ * saves the original BF16 operands and skips backward quantisation.
+ * Readings: the quantisers pass gradients unchanged; the saved values are
+ * the forward's own u = BF16(FC1 output), h = BF16(SwiGLU output) and the
+ * FP32 expert output y2; the BF16 GEMM operands are dy2 = BF16(w * dY)
+ * (router coefficient in FP32, then the cast, as in the forward) and
+ * du = BF16(SwiGLU backward); everything else is evaluated in FP64 here. */
+
+/* Router gradients from the saved expert outputs:
+ *   dw[t][j]  = sum_n dY[t][n] * y2[row(t,j)][n]
+ *   dlogits[t][ids[t][j]] = w_j * (dw_j - sum_i w_i dw_i), 0 elsewhere
+ * (the weights are a softmax over the selected logits; top-k selection is
+ * piecewise constant).  FP64, rounded once to FP32. */
+void orc_bwd_router(const uint16_t* dY, const float* y2, const float* w, const int32_t* ids,
+                    const int32_t* token_slot_row, int64_t T, int k, int d, int E, float* dw, float* dlogits);
+
+/* dy2[row(t,j)][n] = BF16(RN_f32(w[t][j] * dY[t][n])); pad rows (every row
+ * not named by token_slot_row) are zero.  dy2 is [M][d]. */
+void orc_bwd_dy2(const uint16_t* dY, const float* w, const int32_t* token_slot_row, int64_t T, int k, int d,
+                 int64_t M, uint16_t* dy2);
+
+/* One expert over n of its rows (dy2, u, h, xr hold those rows; xr[i] is the
+ * BF16 input row of the row's token, zero on pad rows):
+ *   dh[r][f]  = sum_n dy2[r][n] W2[n][f]                        (FP64)
+ *   s = 1/(1+exp(-g)), g = u[r][f], v = u[r][F+f]
+ *   du[r][f]   = BF16(dh * v * s * (1 + g (1 - s)))             (gate half)
+ *   du[r][F+f] = BF16(dh * g * s)                                (up half)
+ *   dxr[r][i] = sum_j du[r][j] W1[j][i]                         (FP64 out)
+ *   dW2[n][f] = sum_r dy2[r][n] h[r][f],  dW1[j][i] = sum_r du[r][j] xr[r][i]
+ * (FP64, rounded once to FP32).  W1 is [2F][d], W2 is [d][F]. */
+void orc_bwd_expert(const uint16_t* dy2, const uint16_t* u, const uint16_t* h, const uint16_t* xr, int64_t n,
+                    int d, int F, const uint16_t* W1, const uint16_t* W2, uint16_t* du, double* dxr, float* dW1,
+                    float* dW2);
+
 #ifdef __cplusplus
 }
 #endif

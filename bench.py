@@ -281,7 +281,42 @@ def native(args):
     wq_bytes = sum(W.numel() * 2 + W.numel() // 2 + W.numel() // 16 + W.shape[0] * W.shape[1] * 4 for W in (W1, W2))
     t_fwd_exp = timed(lambda: M.moe_expert_forward(x, lg, T, E, k, d, F, w1e["codes"], w1e["sf"], w1e["g"],
                                                    w2e["codes"], w2e["sf"], w2e["g"], out, ws, status, stream))
-    del W1, W2
+    # ---- forward + straight-through BF16 backward of the layer (training
+    # step; weights quantised beforehand, as for the forward) ----
+    mc = M.m_cap(T, E, k)
+    su = torch.empty((mc, 2 * F), dtype=torch.int16, device=dev)
+    sh = torch.empty((mc, F), dtype=torch.int16, device=dev)
+    sy = torch.empty((mc, d), dtype=torch.float32, device=dev)
+    dY = to_dev(synth.layer(args.workload, seed=shard_seed(args.seed, rank)).grad_out())
+    gx = torch.empty((T, d), dtype=torch.float32, device=dev)
+    gW1 = torch.empty((E, 2 * F, d), dtype=torch.float32, device=dev)
+    gW2 = torch.empty((E, d, F), dtype=torch.float32, device=dev)
+    gl = torch.empty((T, E), dtype=torch.float32, device=dev)
+    gw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    bws = torch.empty(M.backward_workspace_bytes(T, E, k, d, F), dtype=torch.uint8, device=dev)
+    fv = M.forward_views(ws, T, E, k, d, F)
+
+    def fwd_train():
+        M.moe_expert_forward_train(x, lg, T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"], w2q["sf"],
+                                   w2q["g"], out, ws, su, sh, sy, status, stream)
+
+    def bwd():
+        M.moe_expert_backward(dY, x, T, E, k, d, F, W1, W2, fv["topk_ids"], fv["topk_w"], fv["offsets"],
+                              fv["row_to_token"], fv["token_slot_row"], su, sh, sy, gx, gW1, gW2, gl, gw, bws, status,
+                              stream)
+
+    t_ftrain = timed(fwd_train)
+    t_bwd = timed(bwd)
+    t_fb = timed(lambda: (fwd_train(), bwd()))
+    alg0 = algorithmic(lay)
+    bwd_flops = 2.0 * (alg0["fc1_flops"] + alg0["fc2_flops"])  # dgrad + wgrad of both GEMMs
+    del W1, W2, su, sh, sy, bws, gW1, gW2
+    fb = {"value": round(T / t_fb, 1), "unit": UNIT, "ms_per_step": round(t_fb * 1e3, 4),
+          "forward_train_ms": round(t_ftrain * 1e3, 4), "backward_ms": round(t_bwd * 1e3, 4),
+          "backward_gemm_tflop": round(bwd_flops / 1e12, 3),
+          "backward_bf16_tflops": round(bwd_flops / t_bwd / 1e12, 1),
+          "backward_frac_of_bf16_peak": round(bwd_flops / t_bwd / 1e12 / peaks["bf16_tflops"], 4),
+          "launches": 13, "workload": "forward with saved values + BF16 backward, dY ~ N(0, 1e-3)"}
     wq = lambda t: {"ms": round(t * 1e3, 4), "achieved": round(wq_bytes / t / 1e9, 1), "unit": "GB/s",
                     "frac": round(wq_bytes / t / 1e9 / peaks["hbm_gbs"], 4)}
     next_rows = {"weight_quant_per_row": dict(wq(t_wq_row), launches=2),
@@ -289,7 +324,7 @@ def native(args):
                                                  note="two passes over W: expert amax, then encode"),
                  "forward_per_expert_weights": {"value": round(T / t_fwd_exp, 1), "unit": UNIT,
                                                 "ms_per_step": round(t_fwd_exp * 1e3, 4)},
-                 "algorithmic_bytes_weight_quant": int(wq_bytes)}
+                 "algorithmic_bytes_weight_quant": int(wq_bytes), "forward_backward": fb}
     alg = algorithmic(lay)
     fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
     fc1_tflops = alg["fc1_flops"] / t_fc1 / 1e12

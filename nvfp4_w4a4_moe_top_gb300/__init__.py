@@ -55,6 +55,10 @@ _SIGS = {
     "nvfp4_grouped_gemm_fc1_swiglu": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
     "nvfp4_grouped_gemm_fc2_unpermute": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, I32, I32, P, P, P, P, P]),
     "moe_expert_forward": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
+    "moe_expert_forward_train": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P]),
+    "moe_expert_backward_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
+    "moe_expert_backward": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ,
+                                  P, P]),
 }
 
 _lib = None
@@ -196,6 +200,26 @@ def moe_expert_forward(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_co
         _p(x), _p(logits), T, E, k, d, d_ff, _p(w1_codes), _p(w1_sf), _p(w1_g), _p(w2_codes), _p(w2_sf),
         _p(w2_g), _p(out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
         _s(stream)))
+
+
+def moe_expert_forward_train(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws,
+                             save_u, save_h, save_y2, status=None, stream=None):
+    _check("moe_expert_forward_train", lib().moe_expert_forward_train(
+        _p(x), _p(logits), T, E, k, d, d_ff, _p(w1_codes), _p(w1_sf), _p(w1_g), _p(w2_codes), _p(w2_sf),
+        _p(w2_g), _p(out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(save_u), _p(save_h),
+        _p(save_y2), _p(status), _s(stream)))
+
+
+def moe_expert_backward(dY, x, T, E, k, d, d_ff, W1, W2, topk_ids, topk_w, offsets, row_to_token, token_slot_row,
+                        u, h, y2, dx, dW1, dW2, dlogits, dw, ws, status=None, stream=None):
+    _check("moe_expert_backward", lib().moe_expert_backward(
+        _p(dY), _p(x), T, E, k, d, d_ff, _p(W1), _p(W2), _p(topk_ids), _p(topk_w), _p(offsets), _p(row_to_token),
+        _p(token_slot_row), _p(u), _p(h), _p(y2), _p(dx), _p(dW1), _p(dW2), _p(dlogits), _p(dw), _p(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _p(status), _s(stream)))
+
+
+def backward_workspace_bytes(T, E, k, d, d_ff):
+    return int(lib().moe_expert_backward_workspace_bytes(T, E, k, d, d_ff))
 
 
 # --------------------------------------------------------------------------

@@ -80,6 +80,19 @@ int encode_operand(CUtensorMap* map, const void* base, int64_t rows, int row_byt
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// 2-D BF16 tensor of `rows` x `cols` (row-major), read in boxes of
+// box_rows rows x 64 columns (128 bytes) with the 128-byte swizzle.
+int encode_bf16(CUtensorMap* map, const void* base, int64_t rows, int cols, int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int finish() {
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -107,6 +120,31 @@ FwdLayout fwd_layout(int T, int E, int k, int d, int d_ff) {
   L.total = o;
   return L;
 }
+
+struct BwdLayout {
+  size_t off[4];  // dy2 bf16 [mc][d], xp bf16 [mc][d], du bf16 [mc][2 d_ff], dxr f32 [mc][d]
+  size_t total;
+};
+
+BwdLayout bwd_layout(int T, int E, int k, int d, int d_ff) {
+  const int64_t mc = m_cap_of(T, E, k);
+  const size_t sizes[4] = {(size_t)mc * d * 2, (size_t)mc * d * 2, (size_t)mc * 2 * d_ff * 2, (size_t)mc * d * 4};
+  BwdLayout L;
+  size_t o = 0;
+  for (int i = 0; i < 4; ++i) {
+    L.off[i] = o;
+    o += up1024(sizes[i]);
+  }
+  L.total = o;
+  return L;
+}
+
+// The forward of moe_expert_forward; with save_u / save_h / save_y2 set it
+// also keeps the values the backward needs.
+int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
+                 const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g, const uint8_t* w2_codes,
+                 const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, uint16_t* save_u,
+                 uint16_t* save_h, float* save_y2, int* status, void* stream);
 
 }  // namespace
 
@@ -295,6 +333,100 @@ int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E, int
                        const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g, const uint8_t* w2_codes,
                        const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, int* status,
                        void* stream) {
+  return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
+                      nullptr, nullptr, nullptr, status, stream);
+}
+
+int moe_expert_forward_train(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
+                             const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g,
+                             const uint8_t* w2_codes, const uint8_t* w2_sf, const float* w2_g, uint16_t* out,
+                             void* ws, size_t ws_bytes, uint16_t* save_u, uint16_t* save_h, float* save_y2,
+                             int* status, void* stream) {
+  if (T > 0 && (!ok_ptr(save_u) || !ok_ptr(save_h) || !ok_ptr(save_y2))) return MOE_ERR_POINTER;
+  return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
+                      save_u, save_h, save_y2, status, stream);
+}
+
+size_t moe_expert_backward_workspace_bytes(int T, int E, int k, int d, int d_ff) {
+  if (!ok_model_shape(T, E, k, d, d_ff)) return 0;
+  return bwd_layout(T, E, k, d, d_ff).total;
+}
+
+int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int k, int d, int d_ff,
+                        const uint16_t* W1, const uint16_t* W2, const int32_t* topk_ids, const float* topk_w,
+                        const int32_t* offsets, const int32_t* row_to_token, const int32_t* token_slot_row,
+                        const uint16_t* u, const uint16_t* h, const float* y2, float* dx, float* dW1, float* dW2,
+                        float* dlogits, float* dw, void* ws, size_t ws_bytes, int* status, void* stream) {
+  if (!ok_model_shape(T, E, k, d, d_ff)) return MOE_ERR_SHAPE;
+  if (!ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(dW1) || !ok_ptr(dW2) || !ok_opt(dlogits) || !ok_opt(status))
+    return MOE_ERR_POINTER;
+  if (T > 0 && (!ok_ptr(dY) || !ok_ptr(x) || !ok_ptr(topk_ids) || !ok_ptr(topk_w) || !ok_ptr(offsets) ||
+                !ok_ptr(row_to_token) || !ok_ptr(token_slot_row) || !ok_ptr(u) || !ok_ptr(h) || !ok_ptr(y2) ||
+                !ok_ptr(dx) || !ok_ptr(dw) || !ok_ptr(ws)))
+    return MOE_ERR_POINTER;
+  const BwdLayout L = bwd_layout(T, E, k, d, d_ff);
+  if (T > 0 && ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  int rc = check_device();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (T == 0) {  // no rows: zero weight gradients
+    if (cudaMemsetAsync(dW1, 0, (size_t)E * 2 * d_ff * d * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, (size_t)E * d * d_ff * 4, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return finish();
+  }
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* dy2 = reinterpret_cast<uint16_t*>(w + L.off[0]);
+  uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.off[1]);
+  uint16_t* du = reinterpret_cast<uint16_t*>(w + L.off[2]);
+  float* dxr = reinterpret_cast<float*>(w + L.off[3]);
+  const int64_t mc = m_cap_of(T, E, k);
+  const int F = d_ff;
+
+  moe::launch_bwd_rows(dY, x, y2, topk_w, row_to_token, token_slot_row, offsets, E, T, k, d, mc, dy2, xp, dw, s);
+  if (dlogits) moe::launch_bwd_logits(dw, topk_w, topk_ids, T, E, k, dlogits, s);
+
+  moe::BwdGemmArgs g;
+  // dh = dy2 . W2_e, SwiGLU backward -> du
+  std::memset(&g, 0, sizeof(g));
+  if (encode_bf16(&g.tmap_a, dy2, mc, d, 128) != MOE_OK || encode_bf16(&g.tmap_b, W2, (int64_t)E * d, F, 64) != MOE_OK)
+    return MOE_ERR_CUDA;
+  g.mode = moe::BWD_DGRAD_SWIGLU; g.a_mn = 0; g.E = E; g.offsets = offsets; g.N = F; g.K = d; g.F = F;
+  g.u = u; g.du = du; g.status = status;
+  if (moe::launch_bwd_gemm(g, (int)(mc / 128), s) != 0) return MOE_ERR_CUDA;
+  // dW2_e = dy2_e^T . h_e
+  std::memset(&g, 0, sizeof(g));
+  if (encode_bf16(&g.tmap_a, dy2, mc, d, 64) != MOE_OK || encode_bf16(&g.tmap_b, h, mc, F, 64) != MOE_OK)
+    return MOE_ERR_CUDA;
+  g.mode = moe::BWD_WGRAD; g.a_mn = 1; g.E = E; g.offsets = offsets; g.N = F; g.Mo = d; g.out = dW2; g.status = status;
+  if (moe::launch_bwd_gemm(g, 0, s) != 0) return MOE_ERR_CUDA;
+  // dxr = du . W1_e
+  std::memset(&g, 0, sizeof(g));
+  if (encode_bf16(&g.tmap_a, du, mc, 2 * F, 128) != MOE_OK ||
+      encode_bf16(&g.tmap_b, W1, (int64_t)E * 2 * F, d, 64) != MOE_OK)
+    return MOE_ERR_CUDA;
+  g.mode = moe::BWD_DGRAD; g.a_mn = 0; g.E = E; g.offsets = offsets; g.N = d; g.K = 2 * F; g.out = dxr;
+  g.status = status;
+  if (moe::launch_bwd_gemm(g, (int)(mc / 128), s) != 0) return MOE_ERR_CUDA;
+  // dW1_e = du_e^T . xp_e
+  std::memset(&g, 0, sizeof(g));
+  if (encode_bf16(&g.tmap_a, du, mc, 2 * F, 64) != MOE_OK || encode_bf16(&g.tmap_b, xp, mc, d, 64) != MOE_OK)
+    return MOE_ERR_CUDA;
+  g.mode = moe::BWD_WGRAD; g.a_mn = 1; g.E = E; g.offsets = offsets; g.N = d; g.Mo = 2 * F; g.out = dW1;
+  g.status = status;
+  if (moe::launch_bwd_gemm(g, 0, s) != 0) return MOE_ERR_CUDA;
+  moe::launch_bwd_dx(dxr, token_slot_row, T, k, d, dx, s);
+  return finish();
+}
+
+}  // extern "C"
+
+namespace {
+
+int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
+                 const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g, const uint8_t* w2_codes,
+                 const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, uint16_t* save_u,
+                 uint16_t* save_h, float* save_y2, int* status, void* stream) {
   if (!ok_model_shape(T, E, k, d, d_ff)) return MOE_ERR_SHAPE;
   if (!ok_ptr(w1_codes) || !ok_ptr(w1_sf) || !ok_ptr(w1_g) || !ok_ptr(w2_codes) || !ok_ptr(w2_sf) || !ok_ptr(w2_g) ||
       !ok_opt(status))
@@ -338,6 +470,7 @@ int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E, int
   a1.a_sf = x_sf; a1.a_g = x_g; a1.w_sf = w1_sf; a1.w_g = w1_g; a1.offsets = offsets;
   a1.E = E; a1.d = d; a1.d_ff = d_ff;
   a1.h_codes = h_codes; a1.h_sf = h_sf; a1.h_g = h_g; a1.scratch = scratch; a1.status = status;
+  a1.save_u = save_u; a1.dbg_h = save_h;
   if (moe::launch_fc1(a1, s) != 0) return MOE_ERR_CUDA;
 
   moe::Fc2Args a2;
@@ -347,9 +480,10 @@ int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E, int
   a2.a_sf = h_sf; a2.a_g = h_g; a2.w_sf = w2_sf; a2.w_g = w2_g; a2.offsets = offsets;
   a2.E = E; a2.d_ff = d_ff; a2.d = d; a2.k = k;
   a2.row_to_token = r2t; a2.token_slot_row = tsr; a2.topk_w = topk_w; a2.slots = slots; a2.status = status;
+  a2.dbg_y = save_y2;
   if (moe::launch_fc2(a2, s) != 0) return MOE_ERR_CUDA;
   moe::launch_unpermute_reduce(slots, T, k, d, out, s);
   return finish();
 }
 
-}  // extern "C"
+}  // namespace

@@ -1,0 +1,524 @@
+// Straight-through BF16 backward of the MoE expert layer (main paper,
+// contributions list, and the AI summary's "Methodology in Plain English":
+// a straight-through estimator on the saved original BF16 activations and
+// weights, no backward quantisation; rainbus summary, method step 5: BF16
+// GEMMs on the saved BF16 operands; Technical Report section 4.3, text below
+// the table: the layer bypass saves the original BF16 operands).
+//
+// Launch sequence of moe_expert_backward:
+//   bwd_rows_kernel     per permuted row r of token t, slot j:
+//                         dy2[r] = BF16(RN_f32(w_tj * dY[t]))  (GEMM operand)
+//                         xp[r]  = x[t]                        (GEMM operand)
+//                         dw[t][j] = <dY[t], y2[r]>            (FP32)
+//                       pad rows of dy2 and xp are zeroed.
+//   bwd_logits_kernel   dlogits[t][e_j] = w_j (dw_j - sum_i w_i dw_i).
+//   bwd_gemm (DGRAD_SWIGLU)  dh = dy2 . W2_e (FP32 in tensor memory), then
+//                       SwiGLU backward in the epilogue against the saved u:
+//                         du[gate] = BF16(dh * up * s (1 + g (1 - s)))
+//                         du[up]   = BF16(dh * g * s),  s = sigmoid(g).
+//   bwd_gemm (WGRAD)    dW2_e = dy2_e^T . h_e       (FP32 out)
+//   bwd_gemm (DGRAD)    dxr = du . W1_e             (FP32 per row)
+//   bwd_gemm (WGRAD)    dW1_e = du_e^T . xp_e       (FP32 out)
+//   bwd_dx_kernel       dx[t] = sum_j dxr[row(t,j)], ascending j, FP32.
+//
+// bwd_gemm is one persistent kernel (one CTA per SM, 10 warps) running
+// tcgen05.mma kind::f16 (BF16 x BF16 -> FP32, M = 128, N = 128 or 256,
+// K = 16 per instruction) from 128-byte-swizzled TMA tiles:
+//   warp 8   TMA producer: per 64-deep k-step one A tile (128 rows) and one B
+//            tile (N columns) into a ring of stages;
+//   warp 9   MMA issuer: four MMAs per k-step into one of two accumulators
+//            (tensor memory columns [0, N) and [N, 2N));
+//   warps 0-7  epilogue: warp w reads lanes 32 (w % 4).. and half w / 4 of
+//            the accumulator's columns.
+// Operand majorness: dgrad reads A (dy2 or du, rows of the permuted tokens)
+// K-major and B (the expert's weights, stored [K][N]) MN-major; wgrad reads
+// both operands MN-major (the contraction runs over the expert's rows).  An
+// MN-major tile is stored as 64-column chunks of 64 rows x 128 bytes, one TMA
+// box each; the descriptor's leading offset is the chunk stride and its
+// stride offset the 8-row group stride (1024 bytes).
+//
+// Every wait is bounded; on expiry the kernel raises MOE_STATUS_TIMEOUT,
+// lets its own copies and MMAs land, frees tensor memory and returns.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BK = 64;                 // BK BF16 elements = one 128-byte row
+constexpr int A_TILE = BM * BK * 2;              // 16 KB
+constexpr int CHUNK = 64 * 128;                  // one MN-major 64 x 64 box: 8 KB
+constexpr int NEPI = 8;                          // epilogue warps
+constexpr int PROD_WARP = 8, MMA_WARP = 9;
+constexpr int THREADS = 320;
+constexpr int MAX_STAGES = 8;
+constexpr int TMEM_COLS = 512;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+struct BTail {
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+#pragma unroll 1
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      set_status(status, MOE_STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool bwarp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = bwait(bar, parity, abort_flag, status);
+  ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+  if (ok) (void)mbar_try_wait(bar, parity);
+  return ok;
+}
+
+// Descriptor of an MN-major operand: 64-column chunks `chunk` bytes apart
+// (leading byte offset), 8-row groups of 1024 bytes (stride byte offset).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t chunk) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((chunk >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+__device__ __forceinline__ void bf16_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void bcommit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Expert owning 128-row tile mt of the permuted rows.
+__device__ __forceinline__ int expert_of_tile(const int32_t* off, int E, int mt) {
+  const int row0 = mt * BM;
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(off + mid) <= row0) lo = mid + 1; else hi = mid;
+  }
+  return lo - 1;
+}
+
+struct Unit {
+  int e, mt, nt;  // expert, 128-row output tile, N tile
+  int k0, nk;     // first contraction row (wgrad) and number of 64-deep k-steps
+};
+
+struct Plan {
+  int units, ntn;
+  __device__ Unit unit(const BwdGemmArgs& a, int u) const {
+    Unit U;
+    if (a.mode != BWD_WGRAD) {
+      U.mt = u / ntn;
+      U.nt = u - U.mt * ntn;
+      U.e = expert_of_tile(a.offsets, a.E, U.mt);
+      U.k0 = 0;
+      U.nk = a.K / BK;
+    } else {
+      const int per_e = (a.Mo / BM) * ntn;
+      U.e = u / per_e;
+      const int rem = u - U.e * per_e;
+      U.mt = rem / ntn;
+      U.nt = rem - U.mt * ntn;
+      U.k0 = __ldg(a.offsets + U.e);
+      U.nk = (__ldg(a.offsets + U.e + 1) - U.k0) / BK;
+    }
+    return U;
+  }
+};
+
+__device__ __forceinline__ Plan make_plan(const BwdGemmArgs& a) {
+  Plan p;
+  p.ntn = a.N / a.bn;
+  if (a.mode != BWD_WGRAD)
+    p.units = (__ldg(a.offsets + a.E) / BM) * p.ntn;
+  else
+    p.units = a.E * (a.Mo / BM) * p.ntn;
+  return p;
+}
+
+__device__ void producer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTail* tl, volatile int* abort_flag) {
+  const uint32_t stage_bytes = A_TILE + a.bn * 128;
+  const uint32_t tx = stage_bytes;
+  uint32_t kc = 0;
+  uint32_t last_use[MAX_STAGES];
+  for (int i = 0; i < MAX_STAGES; ++i) last_use[i] = 0xFFFFFFFFu;
+  bool aborted = false;
+  for (int u = blockIdx.x; u < P.units && !aborted; u += gridDim.x) {
+    const Unit U = P.unit(a, u);
+    const int brow0 = a.mode == BWD_WGRAD ? U.k0 : U.e * a.K;
+    for (int ks = 0; ks < U.nk; ++ks, ++kc) {
+      const uint32_t s = kc % (uint32_t)a.stages, use = kc / (uint32_t)a.stages;
+      if (!bwait(smem_u32(&tl->empty[s]), (use & 1u) ^ 1u, abort_flag, a.status)) { aborted = true; break; }
+      const uint32_t st = ring + s * stage_bytes;
+      const uint32_t fb = smem_u32(&tl->full[s]);
+      mbar_arrive_expect_tx(fb, tx);
+      if (a.a_mn) {
+        tma_load_2d(st, &a.tmap_a, U.mt * BM, U.k0 + ks * BK, fb);
+        tma_load_2d(st + CHUNK, &a.tmap_a, U.mt * BM + 64, U.k0 + ks * BK, fb);
+      } else {
+        tma_load_2d(st, &a.tmap_a, ks * BK, U.mt * BM, fb);
+      }
+      for (int c = 0; c < a.bn / 64; ++c)
+        tma_load_2d(st + A_TILE + c * CHUNK, &a.tmap_b, U.nt * a.bn + c * 64, brow0 + ks * BK, fb);
+      last_use[s] = use;
+    }
+  }
+  if (aborted) {
+    for (int s = 0; s < MAX_STAGES; ++s)
+      if (last_use[s] != 0xFFFFFFFFu) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(smem_u32(&tl->full[s]), last_use[s] & 1u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
+        }
+      }
+  }
+}
+
+__device__ void mma_issuer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTail* tl, uint32_t tmem,
+                           volatile int* abort_flag) {
+  const uint32_t stage_bytes = A_TILE + a.bn * 128;
+  const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((a.a_mn ? 1u : 0u) << 15) | (1u << 16) |
+                         ((uint32_t)(a.bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  uint32_t kc = 0, it = 0;
+  bool aborted = false;
+  for (int u = blockIdx.x; u < P.units && !aborted; u += gridDim.x) {
+    const Unit U = P.unit(a, u);
+    if (U.nk == 0) continue;
+    const uint32_t acc = it & 1u, ause = it >> 1;
+    if (!bwait(smem_u32(&tl->tempty[acc]), (ause & 1u) ^ 1u, abort_flag, a.status)) { aborted = true; break; }
+    tc_fence_after();
+    const uint32_t d = tmem + acc * (uint32_t)a.bn;
+    for (int ks = 0; ks < U.nk; ++ks, ++kc) {
+      const uint32_t s = kc % (uint32_t)a.stages, use = kc / (uint32_t)a.stages;
+      if (!bwait(smem_u32(&tl->full[s]), use & 1u, abort_flag, a.status)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t st = ring + s * stage_bytes;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // K = 16 per instruction: 32 bytes along a K-major row, or two
+        // 8-row groups (2048 bytes) down an MN-major tile
+        const uint64_t ad = a.a_mn ? sdesc_mn_sw128(st + i * 2048, CHUNK) : sdesc_k_sw128(st + i * 32);
+        const uint64_t bd = sdesc_mn_sw128(st + A_TILE + i * 2048, CHUNK);
+        bf16_mma(d, ad, bd, idesc, (ks | i) != 0 ? 1u : 0u);
+      }
+      bcommit(smem_u32(&tl->empty[s]));
+    }
+    if (aborted) break;
+    bcommit(smem_u32(&tl->tfull[acc]));
+    ++it;
+  }
+  bcommit(smem_u32(&tl->done));
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(smem_u32(&tl->done), 0u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
+  }
+}
+
+// SwiGLU backward of 32 columns f0.. of one row (FP32 dh in v).
+__device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint16_t* urow, uint16_t* durow, int F,
+                                             int f0) {
+  const uint4* gp = reinterpret_cast<const uint4*>(urow + f0);
+  const uint4* up = reinterpret_cast<const uint4*>(urow + F + f0);
+  uint4* dg = reinterpret_cast<uint4*>(durow + f0);
+  uint4* du = reinterpret_cast<uint4*>(durow + F + f0);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 g4 = __ldg(gp + q), u4 = __ldg(up + q);
+    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
+    uint32_t og[4], ou[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      float rg[2], ru[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float g = h ? bf16_hi(gw[p]) : bf16_lo(gw[p]);
+        const float x = h ? bf16_hi(uw[p]) : bf16_lo(uw[p]);
+        const float dh = __uint_as_float(v[q * 8 + p * 2 + h]);
+        const float s = 1.0f / (1.0f + __expf(-g));
+        rg[h] = dh * x * (s * (1.0f + g * (1.0f - s)));
+        ru[h] = dh * (g * s);
+      }
+      og[p] = pack2_rn(rg[0], rg[1]);
+      ou[p] = pack2_rn(ru[0], ru[1]);
+    }
+    dg[q] = make_uint4(og[0], og[1], og[2], og[3]);
+    du[q] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+  }
+}
+
+__device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_t tmem, volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q4 = warp & 3, part = warp >> 2;
+  const int rl = q4 * 32 + lane;
+  const int half = a.bn / 2;
+  uint32_t it = 0;
+  for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
+    const Unit U = P.unit(a, u);
+    const int c0 = U.nt * a.bn + part * half;  // first output column of this thread
+    if (U.nk == 0) {  // wgrad of an expert without rows: zero gradient
+      float4* o = reinterpret_cast<float4*>(a.out + ((int64_t)U.e * a.Mo + U.mt * BM + rl) * a.N + c0);
+      for (int i = 0; i < half / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      continue;
+    }
+    const uint32_t acc = it & 1u, ause = it >> 1;
+    ++it;
+    if (!bwarp_wait(smem_u32(&tl->tfull[acc]), ause & 1u, abort_flag, a.status)) break;
+    tc_fence_after();
+    const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + acc * (uint32_t)a.bn + part * half;
+    for (int c = 0; c < half; c += 32) {
+      uint32_t v[32];
+      tld32(tbase + c, v);
+      if (a.mode == BWD_DGRAD_SWIGLU) {
+        const int64_t row = (int64_t)U.mt * BM + rl;
+        swiglu_bwd32(v, a.u + row * 2 * a.F, a.du + row * 2 * a.F, a.F, c0 + c);
+      } else {
+        const int64_t orow = a.mode == BWD_WGRAD ? (int64_t)U.e * a.Mo + U.mt * BM + rl : (int64_t)U.mt * BM + rl;
+        float4* o = reinterpret_cast<float4*>(a.out + orow * a.N + c0 + c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                             __uint_as_float(v[4 * i + 3]));
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[acc]));
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage_bytes = A_TILE + a.bn * 128;
+  BTail* tl = reinterpret_cast<BTail*>(smem + (size_t)a.stages * stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
+      mbar_init(smem_u32(&tl->full[s]), 1);
+      mbar_init(smem_u32(&tl->empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&tl->tfull[s]), 1);
+      mbar_init(smem_u32(&tl->tempty[s]), NEPI);
+    }
+    mbar_init(smem_u32(&tl->done), 1);
+    tl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const Plan P = make_plan(a);
+  volatile int* abort_flag = &tl->abort_flag;
+  const uint32_t ring = smem_u32(smem);
+  if (warp == PROD_WARP) {
+    if (lane == 0) {
+      prefetch_tmap(&a.tmap_a);
+      prefetch_tmap(&a.tmap_b);
+      producer(a, P, ring, tl, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) mma_issuer(a, P, ring, tl, tl->tmem_base, abort_flag);
+    __syncwarp();
+  } else {
+    epilogue(a, P, tl, tl->tmem_base, abort_flag);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == MMA_WARP)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
+                 : "memory");
+}
+
+int bwd_gemm_smem_bytes(int bn, int stages) { return 1024 + stages * (A_TILE + bn * 128) + (int)sizeof(BTail); }
+
+// max_row_tiles: for dgrad, an upper bound of offsets[E] / 128 (the number
+// of units is read on the device); ignored for wgrad.
+int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream) {
+  a.bn = a.N % 256 == 0 ? 256 : 128;
+  a.stages = a.bn == 256 ? 4 : 6;
+  const int ntn = a.N / a.bn;
+  const int64_t max_units = a.mode == BWD_WGRAD ? (int64_t)a.E * (a.Mo / BM) * ntn : (int64_t)max_row_tiles * ntn;
+  const int smem = bwd_gemm_smem_bytes(a.bn, a.stages);
+  if (cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return -1;
+  int grid = gemm_num_ctas();
+  if (grid <= 0) return -1;
+  if (max_units < grid) grid = (int)max_units;
+  if (grid < 1) return 0;
+  bwd_gemm_kernel<<<grid, THREADS, smem, stream>>>(a);
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Row, logit and dx kernels (HBM-bound, one warp per row or token)
+// ---------------------------------------------------------------------------
+// Permuted row r: slot j of token t = row_to_token[r] (found among the k
+// entries of token_slot_row[t]); pad rows are zeroed (dy2, xp); rows at or
+// past offsets[E] are left alone.  d % 8 == 0.
+__global__ void __launch_bounds__(256) bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ x,
+                                                       const float* __restrict__ y2, const float* __restrict__ topk_w,
+                                                       const int32_t* __restrict__ row_to_token,
+                                                       const int32_t* __restrict__ token_slot_row,
+                                                       const int32_t* __restrict__ offsets, int E, int T, int k, int d,
+                                                       int64_t m_rows, uint16_t* __restrict__ dy2,
+                                                       uint16_t* __restrict__ xp, float* __restrict__ dw) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= m_rows) return;
+  const int n8 = d / 8;
+  uint4* drow = reinterpret_cast<uint4*>(dy2 + r * d);
+  uint4* xrow = reinterpret_cast<uint4*>(xp + r * d);
+  if (r >= __ldg(offsets + E)) return;  // past the padded rows: never read
+  const int t = __ldg(row_to_token + r);
+  if (t < 0 || t >= T) {
+    for (int i = lane; i < n8; i += 32) {
+      drow[i] = make_uint4(0u, 0u, 0u, 0u);
+      xrow[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
+  int j = 0;
+  for (int jj = 0; jj < k; ++jj)
+    if (__ldg(token_slot_row + (int64_t)t * k + jj) == r) j = jj;
+  const float w = __ldg(topk_w + (int64_t)t * k + j);
+  const uint4* yrow = reinterpret_cast<const uint4*>(dY + (int64_t)t * d);
+  const uint4* xsrc = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
+  const float4* y2row = reinterpret_cast<const float4*>(y2 + r * d);
+  float dot = 0.0f;
+  for (int i = lane; i < n8; i += 32) {
+    const uint4 g = __ldg(yrow + i);
+    const float4 p0 = __ldg(y2row + 2 * i), p1 = __ldg(y2row + 2 * i + 1);
+    const float gv[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                         bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+    const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = pack2_rn(__fmul_rn(w, gv[2 * q]), __fmul_rn(w, gv[2 * q + 1]));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) dot = fmaf(gv[q], pv[q], dot);
+    drow[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    xrow[i] = __ldg(xsrc + i);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+  if (lane == 0) dw[(int64_t)t * k + j] = dot;
+}
+
+// dlogits[t][:] = 0, then w_j (dw_j - sum_i w_i dw_i) at the selected ids.
+__global__ void __launch_bounds__(256) bwd_logits_kernel(const float* __restrict__ dw, const float* __restrict__ topk_w,
+                                                         const int32_t* __restrict__ topk_ids, int T, int E, int k,
+                                                         float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float mean = 0.0f;
+  for (int j = 0; j < k; ++j) mean = fmaf(__ldg(topk_w + t * k + j), __ldg(dw + t * k + j), mean);
+  for (int e = lane; e < E; e += 32) dlogits[t * E + e] = 0.0f;
+  __syncwarp();
+  for (int j = lane; j < k; j += 32) {
+    const int e = __ldg(topk_ids + t * k + j);
+    if (e >= 0 && e < E) dlogits[t * E + e] = __ldg(topk_w + t * k + j) * (__ldg(dw + t * k + j) - mean);
+  }
+}
+
+// dx[t] = sum_j dxr[token_slot_row[t][j]] (FP32, ascending j).  d % 4 == 0.
+__global__ void __launch_bounds__(256) bwd_dx_kernel(const float* __restrict__ dxr,
+                                                     const int32_t* __restrict__ token_slot_row, int T, int k, int d,
+                                                     float* __restrict__ dx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int n4 = d / 4;
+  int rows[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) rows[j] = j < k ? __ldg(token_slot_row + t * k + j) : 0;
+  for (int i = lane; i < n4; i += 32) {
+    float4 s = __ldg(reinterpret_cast<const float4*>(dxr + (int64_t)rows[0] * d) + i);
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {
+      if (j < k) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(dxr + (int64_t)rows[j] * d) + i);
+        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      }
+    }
+    reinterpret_cast<float4*>(dx + t * d)[i] = s;
+  }
+}
+
+int launch_bwd_rows(const uint16_t* dY, const uint16_t* x, const float* y2, const float* topk_w,
+                    const int32_t* row_to_token, const int32_t* token_slot_row, const int32_t* offsets, int E, int T,
+                    int k, int d, int64_t m_rows, uint16_t* dy2, uint16_t* xp, float* dw, cudaStream_t stream) {
+  if (m_rows <= 0) return 0;
+  bwd_rows_kernel<<<(unsigned)((m_rows + 7) / 8), 256, 0, stream>>>(dY, x, y2, topk_w, row_to_token, token_slot_row,
+                                                                     offsets, E, T, k, d, m_rows, dy2, xp, dw);
+  return 0;
+}
+
+int launch_bwd_logits(const float* dw, const float* topk_w, const int32_t* topk_ids, int T, int E, int k,
+                      float* dlogits, cudaStream_t stream) {
+  if (T <= 0) return 0;
+  bwd_logits_kernel<<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(dw, topk_w, topk_ids, T, E, k, dlogits);
+  return 0;
+}
+
+int launch_bwd_dx(const float* dxr, const int32_t* token_slot_row, int T, int k, int d, float* dx, cudaStream_t stream) {
+  if (T <= 0) return 0;
+  bwd_dx_kernel<<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(dxr, token_slot_row, T, k, d, dx);
+  return 0;
+}
+
+}  // namespace moe

@@ -660,6 +660,11 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
                   du[nh + m] = yg0; du[nh + m + 1] = yg1;
                   du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
                 }
+                if (DBG && args.save_u) {
+                  uint16_t* su = args.save_u + row * 2 * d_ff;
+                  *reinterpret_cast<uint32_t*>(su + nh + m) = ugp;
+                  *reinterpret_cast<uint32_t*>(su + d_ff + nh + m) = uup;
+                }
               }
             }
             if (DBG && args.dbg_h) {
@@ -887,7 +892,7 @@ static int set_smem(const void* kernel, size_t smem) {
 int launch_fc1(Fc1Args& a, cudaStream_t stream) {
   size_t smem;
   if (!plan(a.d, 2 * (a.d_ff / BN), 2 * a.d_ff, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem)) return -1;
-  const bool dbg = a.dbg_u != nullptr || a.dbg_h != nullptr;
+  const bool dbg = a.dbg_u != nullptr || a.dbg_h != nullptr || a.save_u != nullptr;
   void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true> : fc1_swiglu_kernel<false>;
   if (set_smem((const void*)kern, smem) != 0) return -1;
   const int grid = gemm_num_ctas();

@@ -59,6 +59,7 @@ struct Fc1Args {
   float* h_g;
   float* dbg_u;
   uint16_t* dbg_h;
+  uint16_t* save_u;  // BF16 u [rows][2 d_ff] for the backward, or NULL
   uint16_t* scratch;
   int* status;
   int rings, na, nb, resident;  // pipeline plan, set by launch_fc1
@@ -79,6 +80,31 @@ struct Fc2Args {
   int* status;
   int rings, na, nb, resident;  // pipeline plan, set by launch_fc2
 };
+
+// BF16 grouped GEMMs of the backward (bwd.cu).
+enum { BWD_DGRAD_SWIGLU = 0, BWD_DGRAD = 1, BWD_WGRAD = 2 };
+struct BwdGemmArgs {
+  CUtensorMap tmap_a, tmap_b;  // A: K-major box 64 x 128 (dgrad) or MN-major 64 x 64 (wgrad); B: MN-major 64 x 64
+  int mode, a_mn;
+  int E;
+  const int32_t* offsets;
+  int N;        // output columns
+  int K;        // dgrad: contraction length (rows of B per expert)
+  int Mo;       // wgrad: output rows per expert
+  int F;        // DGRAD_SWIGLU: d_ff
+  const uint16_t* u;  // DGRAD_SWIGLU: saved u [rows][2F]
+  uint16_t* du;       // DGRAD_SWIGLU: out [rows][2F]
+  float* out;         // DGRAD: [rows][N]; WGRAD: [E][Mo][N]
+  int* status;
+  int bn, stages;     // set by launch_bwd_gemm
+};
+int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream);
+int launch_bwd_rows(const uint16_t* dY, const uint16_t* x, const float* y2, const float* topk_w,
+                    const int32_t* row_to_token, const int32_t* token_slot_row, const int32_t* offsets, int E, int T,
+                    int k, int d, int64_t m_rows, uint16_t* dy2, uint16_t* xp, float* dw, cudaStream_t stream);
+int launch_bwd_logits(const float* dw, const float* topk_w, const int32_t* topk_ids, int T, int E, int k,
+                      float* dlogits, cudaStream_t stream);
+int launch_bwd_dx(const float* dxr, const int32_t* token_slot_row, int T, int k, int d, float* dx, cudaStream_t stream);
 
 int gemm_num_ctas();  // persistent grid size on the current device
 int launch_fc1(Fc1Args& a, cudaStream_t stream);

@@ -16,11 +16,12 @@ def L():
 
 def test_exports_every_header_function(L):
     names = M.header_functions()
-    assert len(names) == 16, names
+    assert len(names) == 19, names
     for n in names:
         assert hasattr(L, n), n
     for n in ["moe_nvfp4_quantize_weights", "moe_nvfp4_quantize_weights_per_expert", "moe_permute_amax", "nvfp4_quantize_rows",
-              "nvfp4_grouped_gemm_fc1_swiglu", "nvfp4_grouped_gemm_fc2_unpermute", "moe_expert_forward"]:
+              "nvfp4_grouped_gemm_fc1_swiglu", "nvfp4_grouped_gemm_fc2_unpermute", "moe_expert_forward",
+              "moe_expert_forward_train", "moe_expert_backward", "moe_expert_backward_workspace_bytes"]:
         assert n in names
 
 
@@ -33,6 +34,9 @@ def test_helpers_match_oracle(L, orc):
     assert M.sf_bytes(10, 48) == 0
     assert M.status_string(-3) == "workspace too small"
     assert M.fc1_workspace_bytes(768) == 256 * 2 * 128 * 768 * 2
+    mc = M.m_cap(65536, 128, 8)
+    assert M.backward_workspace_bytes(65536, 128, 8, 2048, 768) == mc * 2048 * 2 * 2 + mc * 1536 * 2 + mc * 2048 * 4
+    assert M.backward_workspace_bytes(10, 4, 2, 200, 128) == 0
 
 
 def test_workspace_layout_is_disjoint_and_aligned(L):
@@ -75,6 +79,20 @@ def test_entry_points_reject_bad_arguments(L):
     assert L.moe_nvfp4_quantize_weights(FAKE, 2, 100, 64, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert L.moe_nvfp4_quantize_weights(FAKE, 2, 128, 48, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert L.moe_nvfp4_quantize_weights(None, 2, 128, 64, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_POINTER
+    # backward: shape, pointer and workspace checks before any CUDA call
+    bw = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 13 + [None, FAKE, FAKE]
+    assert L.moe_expert_backward(*bw, 16, None, None) == M.MOE_ERR_WORKSPACE
+    bad = list(bw)
+    bad[5] = 200
+    assert L.moe_expert_backward(*bad, 1 << 40, None, None) == M.MOE_ERR_SHAPE
+    bad = list(bw)
+    bad[7] = None  # W1
+    assert L.moe_expert_backward(*bad, 1 << 40, None, None) == M.MOE_ERR_POINTER
+    bad = list(bw)
+    bad[16] = MIS  # y2
+    assert L.moe_expert_backward(*bad, 1 << 40, None, None) == M.MOE_ERR_POINTER
+    ft = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 7 + [FAKE, 1 << 40, None, FAKE, FAKE, None, None]
+    assert L.moe_expert_forward_train(*ft) == M.MOE_ERR_POINTER
     qe = L.moe_nvfp4_quantize_weights_per_expert
     assert qe(FAKE, 2, 100, 64, FAKE, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert qe(FAKE, 0, 128, 64, FAKE, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE

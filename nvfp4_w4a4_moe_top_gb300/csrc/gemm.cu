@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
             tmem_ld16(tmem + su * BN + hh * 16, Uv);
             tmem_wait_ld();
             const int nh = n0 + hh * 16;
-            uint32_t hp[8];
+            uint32_t hp[8], ugw[8], uuw[8];
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
               const float4 fg = *reinterpret_cast<const float4*>(gws + nh + i);
@@ -660,12 +660,17 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
                   du[nh + m] = yg0; du[nh + m + 1] = yg1;
                   du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
                 }
-                if (DBG && args.save_u) {
-                  uint16_t* su = args.save_u + row * 2 * d_ff;
-                  *reinterpret_cast<uint32_t*>(su + nh + m) = ugp;
-                  *reinterpret_cast<uint32_t*>(su + d_ff + nh + m) = uup;
-                }
+                ugw[m >> 1] = ugp;
+                uuw[m >> 1] = uup;
               }
+            }
+            if (DBG && args.save_u) {  // 32-byte sectors: gate, then up
+              uint4* sg4 = reinterpret_cast<uint4*>(args.save_u + row * 2 * d_ff + nh);
+              uint4* su4 = reinterpret_cast<uint4*>(args.save_u + row * 2 * d_ff + d_ff + nh);
+              sg4[0] = make_uint4(ugw[0], ugw[1], ugw[2], ugw[3]);
+              sg4[1] = make_uint4(ugw[4], ugw[5], ugw[6], ugw[7]);
+              su4[0] = make_uint4(uuw[0], uuw[1], uuw[2], uuw[3]);
+              su4[1] = make_uint4(uuw[4], uuw[5], uuw[6], uuw[7]);
             }
             if (DBG && args.dbg_h) {
               uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
@@ -797,6 +802,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
           for (int hf = 0; hf < 4; ++hf) {
             const int n0 = nt * BN + part * 64 + hf * 16;
             uint32_t zp[8];
+            float yv[16];
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
               const float4 f4 = *reinterpret_cast<const float4*>(gws + n0 + i);
@@ -807,11 +813,14 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
                 const float y0 = __fmul_rn(__uint_as_float(R[hf][m]), __fmul_rn(gh, f[jj]));
                 const float y1 = __fmul_rn(__uint_as_float(R[hf][m + 1]), __fmul_rn(gh, f[jj + 1]));
                 zp[m >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
-                if (DBG && args.dbg_y && t >= 0) {
-                  args.dbg_y[row * d + n0 + m] = y0;
-                  args.dbg_y[row * d + n0 + m + 1] = y1;
-                }
+                yv[m] = y0;
+                yv[m + 1] = y1;
               }
+            }
+            if (DBG && args.dbg_y && t >= 0) {  // two 32-byte sectors
+              float4* y4 = reinterpret_cast<float4*>(args.dbg_y + row * d + n0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) y4[q] = make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
             }
             sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf) ^ (lane & 7)), zp[0], zp[1], zp[2], zp[3]);
             sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf + 1) ^ (lane & 7)), zp[4], zp[5], zp[6], zp[7]);

@@ -281,6 +281,9 @@ def native(args):
     wq_bytes = sum(W.numel() * 2 + W.numel() // 2 + W.numel() // 16 + W.shape[0] * W.shape[1] * 4 for W in (W1, W2))
     t_fwd_exp = timed(lambda: M.moe_expert_forward(x, lg, T, E, k, d, F, w1e["codes"], w1e["sf"], w1e["g"],
                                                    w2e["codes"], w2e["sf"], w2e["g"], out, ws, status, stream))
+    t_fwd_gather = timed(lambda: M.moe_expert_forward_gather(x, lg, T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"],
+                                                             w2q["codes"], w2q["sf"], w2q["g"], out, ws, status,
+                                                             stream))
     # ---- forward + straight-through BF16 backward of the layer (training
     # step; weights quantised beforehand, as for the forward) ----
     mc = M.m_cap(T, E, k)
@@ -324,6 +327,9 @@ def native(args):
                                                  note="two passes over W: expert amax, then encode"),
                  "forward_per_expert_weights": {"value": round(T / t_fwd_exp, 1), "unit": UNIT,
                                                 "ms_per_step": round(t_fwd_exp * 1e3, 4)},
+                 "forward_gather_on_load": {"value": round(T / t_fwd_gather, 1), "unit": UNIT,
+                                            "ms_per_step": round(t_fwd_gather * 1e3, 4),
+                                            "note": "codes quantised once per token, FC1 A rows by tile::gather4"},
                  "algorithmic_bytes_weight_quant": int(wq_bytes), "forward_backward": fb}
     alg = algorithmic(lay)
     fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16

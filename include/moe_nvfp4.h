@@ -288,6 +288,26 @@ int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E,
                        const float* w2_g, uint16_t* out, void* ws,
                        size_t ws_bytes, int* status, void* stream);
 
+/* moe_expert_forward with gather-on-load FC1, a step toward the single-pass
+ * fusion the pages name as future work (AI summary, "Future Directions":
+ * fuse amax, quantisation and GEMM; main paper, section 5.6 "Exploring
+ * Single-Pass Fusion", title only).  Each token is quantised ONCE: its codes
+ * go to token row t of the x_codes workspace entry (rows 0..T-1, row T all
+ * zero) instead of k row copies, and FC1's producer fetches the A rows of
+ * each 128-row tile by row_to_token with TMA tile::gather4 (pad rows read
+ * the zero row).  Block scales and g stay one copy per routed row (x_sf,
+ * x_g), as in moe_expert_forward.  Same arguments, workspace and results
+ * (bit for bit) as moe_expert_forward; only the content of the x_codes
+ * workspace entry differs.  Needs d >= 256 (a code row must span the
+ * 128-byte gather box), else MOE_ERR_SHAPE. */
+int moe_expert_forward_gather(const uint16_t* x, const float* logits, int T,
+                              int E, int k, int d, int d_ff,
+                              const uint8_t* w1_codes, const uint8_t* w1_sf,
+                              const float* w1_g, const uint8_t* w2_codes,
+                              const uint8_t* w2_sf, const float* w2_g,
+                              uint16_t* out, void* ws, size_t ws_bytes,
+                              int* status, void* stream);
+
 /* moe_expert_forward that also keeps what the straight-through backward
  * needs (main paper, contributions list: BF16 backward on saved operands;
  * Technical Report section 4.3, text below the table: the layer bypass saves

@@ -55,6 +55,7 @@ _SIGS = {
     "nvfp4_grouped_gemm_fc1_swiglu": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
     "nvfp4_grouped_gemm_fc2_unpermute": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, I32, I32, P, P, P, P, P]),
     "moe_expert_forward": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
+    "moe_expert_forward_gather": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_expert_forward_train": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P]),
     "moe_expert_backward_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
     "moe_expert_backward": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ,
@@ -197,6 +198,16 @@ def nvfp4_grouped_gemm_fc2_unpermute(h_codes, h_sf, h_g, offsets, E, M_cap, d_ff
 def moe_expert_forward(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws,
                        status=None, stream=None):
     _check("moe_expert_forward", lib().moe_expert_forward(
+        _p(x), _p(logits), T, E, k, d, d_ff, _p(w1_codes), _p(w1_sf), _p(w1_g), _p(w2_codes), _p(w2_sf),
+        _p(w2_g), _p(out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+        _s(stream)))
+
+
+def moe_expert_forward_gather(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws,
+                              status=None, stream=None):
+    """moe_expert_forward with gather-on-load FC1 (codes quantised once per
+    token, fetched by row_to_token with TMA tile::gather4)."""
+    _check("moe_expert_forward_gather", lib().moe_expert_forward_gather(
         _p(x), _p(logits), T, E, k, d, d_ff, _p(w1_codes), _p(w1_sf), _p(w1_g), _p(w2_codes), _p(w2_sf),
         _p(w2_g), _p(out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
         _s(stream)))

@@ -93,6 +93,19 @@ int encode_bf16(CUtensorMap* map, const void* base, int64_t rows, int cols, int 
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Token-ordered codes (`rows` rows of `row_bytes`) read by tile::gather4:
+// boxes of one row x 128 bytes, 128-byte swizzle.
+int encode_gather_rows(CUtensorMap* map, const void* base, int64_t rows, int row_bytes) {
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {128u, 1u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int finish() {
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -144,7 +157,7 @@ BwdLayout bwd_layout(int T, int E, int k, int d, int d_ff) {
 int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
                  const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g, const uint8_t* w2_codes,
                  const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, uint16_t* save_u,
-                 uint16_t* save_h, float* save_y2, int* status, void* stream);
+                 uint16_t* save_h, float* save_y2, bool gather, int* status, void* stream);
 
 }  // namespace
 
@@ -334,7 +347,17 @@ int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E, int
                        const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, int* status,
                        void* stream) {
   return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
-                      nullptr, nullptr, nullptr, status, stream);
+                      nullptr, nullptr, nullptr, false, status, stream);
+}
+
+int moe_expert_forward_gather(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
+                              const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g,
+                              const uint8_t* w2_codes, const uint8_t* w2_sf, const float* w2_g, uint16_t* out,
+                              void* ws, size_t ws_bytes, int* status, void* stream) {
+  // a code row of d/2 bytes must cover the 128-byte gather box
+  if (d < 256) return MOE_ERR_SHAPE;
+  return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
+                      nullptr, nullptr, nullptr, true, status, stream);
 }
 
 int moe_expert_forward_train(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
@@ -344,7 +367,7 @@ int moe_expert_forward_train(const uint16_t* x, const float* logits, int T, int 
                              int* status, void* stream) {
   if (T > 0 && (!ok_ptr(save_u) || !ok_ptr(save_h) || !ok_ptr(save_y2))) return MOE_ERR_POINTER;
   return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
-                      save_u, save_h, save_y2, status, stream);
+                      save_u, save_h, save_y2, false, status, stream);
 }
 
 size_t moe_expert_backward_workspace_bytes(int T, int E, int k, int d, int d_ff) {
@@ -426,7 +449,7 @@ namespace {
 int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
                  const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g, const uint8_t* w2_codes,
                  const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, uint16_t* save_u,
-                 uint16_t* save_h, float* save_y2, int* status, void* stream) {
+                 uint16_t* save_h, float* save_y2, bool gather, int* status, void* stream) {
   if (!ok_model_shape(T, E, k, d, d_ff)) return MOE_ERR_SHAPE;
   if (!ok_ptr(w1_codes) || !ok_ptr(w1_sf) || !ok_ptr(w1_g) || !ok_ptr(w2_codes) || !ok_ptr(w2_sf) || !ok_ptr(w2_g) ||
       !ok_opt(status))
@@ -460,12 +483,22 @@ int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, in
 
   moe::launch_route(logits, nullptr, nullptr, T, E, k, topk_ids, topk_w, tsr, hist, status, s);
   moe::launch_scan(hist, C, E, counts, offsets, s);
-  moe::launch_pad_rows(offsets, counts, E, mc, r2t, nullptr, x_codes, d, x_sf, x_g, s);
-  moe::launch_permute_quant(topk_ids, tsr, hist, offsets, T, E, k, x, d, r2t, amax_tok, x_codes, x_sf, x_g, status, s);
+  // gather: x_codes holds the codes once per token (rows 0..T-1) and a zero
+  // row T, which the pad rows gather; otherwise one copy per routed row
+  moe::launch_pad_rows(offsets, counts, E, mc, r2t, nullptr, gather ? nullptr : x_codes, d, x_sf, x_g, s);
+  if (moe::launch_permute_quant(topk_ids, tsr, hist, offsets, T, E, k, x, d, r2t, amax_tok, gather ? nullptr : x_codes,
+                                gather ? x_codes : nullptr, x_sf, x_g, status, s) != 0)
+    return MOE_ERR_CUDA;
 
   moe::Fc1Args a1;
   std::memset(&a1, 0, sizeof(a1));
-  if (encode_operand(&a1.tmap_a, x_codes, mc, d / 2) != MOE_OK) return MOE_ERR_CUDA;
+  if (gather) {
+    if (encode_gather_rows(&a1.tmap_a, x_codes, (int64_t)T + 1, d / 2) != MOE_OK) return MOE_ERR_CUDA;
+    a1.a_rows = r2t;
+    a1.zero_row = T;
+  } else if (encode_operand(&a1.tmap_a, x_codes, mc, d / 2) != MOE_OK) {
+    return MOE_ERR_CUDA;
+  }
   if (encode_operand(&a1.tmap_b, w1_codes, (int64_t)E * 2 * d_ff, d / 2) != MOE_OK) return MOE_ERR_CUDA;
   a1.a_sf = x_sf; a1.a_g = x_g; a1.w_sf = w1_sf; a1.w_g = w1_g; a1.offsets = offsets;
   a1.E = E; a1.d = d; a1.d_ff = d_ff;

@@ -240,6 +240,23 @@ struct ItemRows {
   }
 };
 
+// A slice (128 rows x 128 bytes) of unit u at byte column x: one 128-row box,
+// or, gathered, 32 four-row copies of the rows' tokens (negative -> zero_row).
+__device__ __forceinline__ void load_a_slice(uint32_t dst, const CUtensorMap* tmap_a, int x, int u,
+                                             const int32_t* a_rows, int zero_row, uint32_t bar) {
+  if (!a_rows) {
+    tma_load_2d(dst, tmap_a, x, u * BM, bar);
+    return;
+  }
+  const int4* r4 = reinterpret_cast<const int4*>(a_rows + (int64_t)u * BM);
+#pragma unroll 4
+  for (int i = 0; i < BM / 4; ++i) {
+    const int4 r = __ldg(r4 + i);
+    tma_gather4(dst + i * 4 * BK_BYTES, tmap_a, x, r.x < 0 ? zero_row : r.x, r.y < 0 ? zero_row : r.y,
+                r.z < 0 ? zero_row : r.z, r.w < 0 ? zero_row : r.w, bar);
+  }
+}
+
 // Producer r of R.  The CTA's k-steps (over units, items, K) are numbered
 // kc = 0, 1, ...; k-step kc travels through ring kc % R, position kc / R.
 // Each ring has one producer and is consumed in order, so every barrier sees
@@ -249,7 +266,8 @@ struct ItemRows {
 // owns that k-step) alias an older phase.
 __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const uint8_t* a_sf,
                               const uint8_t* b_sf, const Geometry& G, const ItemRows& rows, const int32_t* off, int E,
-                              uint32_t a_base, uint32_t ring_base, Tail* tl, volatile int* abort_flag, int* status) {
+                              uint32_t a_base, uint32_t ring_base, Tail* tl, volatile int* abort_flag, int* status,
+                              const int32_t* a_rows, int zero_row) {
   const uint32_t b_off = G.b_off();
   uint32_t kc = 0;
   uint32_t last_stage_use[MAX_STAGES], last_a_use[MAX_A_SLOTS];
@@ -277,11 +295,11 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
           if (!wait_bounded(smem_u32(&tl->a_empty[ks]), (unit_use & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
           const uint32_t ab = smem_u32(&tl->a_full[ks]);
           mbar_arrive_expect_tx(ab, A_SLICE);
-          tma_load_2d(a_base + ks * A_SLICE, tmap_a, ks * BK_BYTES, u * BM, ab);
+          load_a_slice(a_base + ks * A_SLICE, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, ab);
           last_a_use[ks] = unit_use;
         }
         mbar_arrive_expect_tx(fb, B_BYTES + 2 * nsf * 512 + b_off);
-        if (!G.resident) tma_load_2d(st, tmap_a, ks * BK_BYTES, u * BM, fb);
+        if (!G.resident) load_a_slice(st, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, fb);
         tma_load_2d(st + b_off, tmap_b, ks * BK_BYTES, br, fb);
         bulk_load(st + b_off + B_BYTES, b_sf + (sfb_row + 4 * ks) * 512, nsf * 512, fb);
         bulk_load(st + b_off + B_BYTES + SF_STAGE, a_sf + (sfa_row + 4 * ks) * 512, nsf * 512, fb);
@@ -532,7 +550,8 @@ template <int NE>
 __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b,
                                                    const uint8_t* a_sf, const uint8_t* b_sf, const Geometry& G,
                                                    const ItemRows& rows, const int32_t* off, int E, uint32_t a_base,
-                                                   uint32_t ring_base, Tail* tl, int* status) {
+                                                   uint32_t ring_base, Tail* tl, int* status,
+                                                   const int32_t* a_rows = nullptr, int zero_row = 0) {
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   using RL = Roles<NE>;
@@ -541,7 +560,7 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
       prefetch_tmap(tmap_a);
       prefetch_tmap(tmap_b);
       producer_loop(warp - RL::PROD, tmap_a, tmap_b, a_sf, b_sf, G, rows, off, E, a_base, ring_base, tl,
-                    abort_flag, status);
+                    abort_flag, status, a_rows, zero_row);
     }
     __syncwarp();
     return false;
@@ -592,7 +611,7 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
   const ItemRows rows{true, 2 * d_ff, d_ff};
 
   if (run_pipeline_roles<FC1_NE>(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
-                         ring_base, tl, args.status)) {
+                         ring_base, tl, args.status, args.a_rows, args.zero_row)) {
     // ---------------- epilogue warps ----------------
     const int q4 = warp & 3, part = warp >> 2;  // part: columns FC1_PART_COLS*part.. of each chunk
     const int rl = q4 * 32 + lane;              // row within the tile = TMEM lane

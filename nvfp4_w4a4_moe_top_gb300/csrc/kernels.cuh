@@ -40,9 +40,11 @@ int launch_pad_rows(const int32_t* offsets, const int32_t* counts, int E, int64_
 
 // Fused permute + amax + quantise of the forward: x read once, codes written
 // into the k destination rows of each token.
+// tok_codes: NULL, or token-ordered codes [T + 1][d/2] (row T zeroed here)
+// written instead of the k row copies of `codes`.
 int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const int32_t* hist, const int32_t* offsets,
                          int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
-                         uint8_t* codes, uint8_t* sf, float* g, int* status, cudaStream_t stream);
+                         uint8_t* codes, uint8_t* tok_codes, uint8_t* sf, float* g, int* status, cudaStream_t stream);
 
 int launch_unpermute_reduce(const uint16_t* slots, int T, int k, int d, uint16_t* out, cudaStream_t stream);
 
@@ -60,6 +62,11 @@ struct Fc1Args {
   float* dbg_u;
   uint16_t* dbg_h;
   uint16_t* save_u;  // BF16 u [rows][2 d_ff] for the backward, or NULL
+  // Gather-on-load A: tmap_a then maps token-ordered codes [zero_row + 1]
+  // rows with 1-row boxes; row r of a unit is token a_rows[r] (zero_row when
+  // negative).  NULL: tmap_a maps the permuted rows (128-row boxes).
+  const int32_t* a_rows;
+  int zero_row;
   uint16_t* scratch;
   int* status;
   int rings, na, nb, resident;  // pipeline plan, set by launch_fc1

@@ -259,6 +259,8 @@ __global__ void __launch_bounds__(128) pad_rows_kernel(const int32_t* __restrict
     if (codes) {
       uint4* cr = reinterpret_cast<uint4*>(codes + r * (K / 2));
       for (int i = 0; i < K / 32; ++i) cr[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (sf) {
       const int kg = K / 64;
       for (int c4 = 0; c4 < kg; ++c4)
         *reinterpret_cast<uint32_t*>(sf + ((r >> 7) * kg + c4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) = 0u;
@@ -282,7 +284,9 @@ int launch_pad_rows(const int32_t* offsets, const int32_t* counts, int E, int64_
 
 // One warp per token: rows of its k slots, amax of x (read once into
 // registers), quantisation, and the same codes / block scales / outer scale
-// written into each of the k destination rows.  Lane L holds, for each group
+// written into each of the k destination rows.  With tok_codes set, the
+// codes go once to token row t of tok_codes instead (the grouped GEMM then
+// gathers them by row_to_token); scales and g still go to the k rows.  Lane L holds, for each group
 // of 1024 columns, the 32 consecutive columns from 32*L (two whole 16-element
 // blocks), so a block never spans lanes, its codes go out as one 16-byte
 // store per row, and lanes L, L ^ 1 together form one 32-bit scale word.
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     const int32_t* __restrict__ topk_ids, int32_t* __restrict__ tsr, const int32_t* __restrict__ hist,
     const int32_t* __restrict__ offsets, int T, int E, int k, const uint16_t* __restrict__ x, int d,
     int32_t* __restrict__ row_to_token, float* __restrict__ amax_tok, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ sf, float* __restrict__ gout, int* status) {
+    uint8_t* __restrict__ tok_codes, uint8_t* __restrict__ sf, float* __restrict__ gout, int* status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -357,14 +361,22 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     cw[g] = make_uint4(c[0], c[1], c[2], c[3]);
     sfw[g] = sb2 | (__shfl_xor_sync(0xFFFFFFFFu, sb2, 1) << 16);
   }
+  if (tok_codes) {
+    uint4* crow = reinterpret_cast<uint4*>(tok_codes + (int64_t)t * (d / 2));
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const int e8 = g * 128 + 4 * lane;
+      if (e8 < n8) crow[e8 >> 2] = cw[g];
+    }
+  }
   for (int j = 0; j < k; ++j) {
     const int64_t r = __shfl_sync(0xFFFFFFFFu, row, j);
-    uint4* crow = reinterpret_cast<uint4*>(codes + r * (d / 2));
+    uint4* crow = tok_codes ? nullptr : reinterpret_cast<uint4*>(codes + r * (d / 2));
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       const int e8 = g * 128 + 4 * lane;
       if (e8 < n8) {
-        crow[e8 >> 2] = cw[g];
+        if (crow) crow[e8 >> 2] = cw[g];
         if ((lane & 1) == 0)
           *reinterpret_cast<uint32_t*>(sf + ((r >> 7) * kg + (e8 >> 3)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) =
               sfw[g];
@@ -376,13 +388,15 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
 
 int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const int32_t* hist, const int32_t* offsets,
                          int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
-                         uint8_t* codes, uint8_t* sf, float* g, int* status, cudaStream_t stream) {
+                         uint8_t* codes, uint8_t* tok_codes, uint8_t* sf, float* g, int* status, cudaStream_t stream) {
   if (T == 0) return 0;
   const int ng = (d + 1023) / 1024;
   const dim3 grid((T + 7) / 8);
+  // row T of the token-ordered codes is the all-zero row the pad rows gather
+  if (tok_codes && cudaMemsetAsync(tok_codes + (int64_t)T * (d / 2), 0, (size_t)d / 2, stream) != cudaSuccess) return -1;
 #define MOE_PQ(N)                                                                                       \
   permute_quant_kernel<N><<<grid, 256, 0, stream>>>(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d, \
-                                                    row_to_token, amax_tok, codes, sf, g, status)
+                                                    row_to_token, amax_tok, codes, tok_codes, sf, g, status)
   if (ng <= 1) MOE_PQ(1);
   else if (ng <= 2) MOE_PQ(2);
   else MOE_PQ(4);

@@ -16,12 +16,13 @@ def L():
 
 def test_exports_every_header_function(L):
     names = M.header_functions()
-    assert len(names) == 19, names
+    assert len(names) == 20, names
     for n in names:
         assert hasattr(L, n), n
     for n in ["moe_nvfp4_quantize_weights", "moe_nvfp4_quantize_weights_per_expert", "moe_permute_amax", "nvfp4_quantize_rows",
               "nvfp4_grouped_gemm_fc1_swiglu", "nvfp4_grouped_gemm_fc2_unpermute", "moe_expert_forward",
-              "moe_expert_forward_train", "moe_expert_backward", "moe_expert_backward_workspace_bytes"]:
+              "moe_expert_forward_train", "moe_expert_backward", "moe_expert_backward_workspace_bytes",
+              "moe_expert_forward_gather"]:
         assert n in names
 
 
@@ -73,6 +74,11 @@ def test_forward_rejects_bad_arguments(L):
     assert _fwd(L, x=MIS) == M.MOE_ERR_POINTER
     assert _fwd(L, w=None) == M.MOE_ERR_POINTER
     assert _fwd(L, ws_bytes=1024) == M.MOE_ERR_WORKSPACE
+    # the gather-on-load forward validates identically
+    g = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 7
+    assert L.moe_expert_forward_gather(*g, FAKE, 1024, None, None) == M.MOE_ERR_WORKSPACE
+    assert L.moe_expert_forward_gather(*(g[:5] + [200] + g[6:]), FAKE, 1 << 40, None, None) == M.MOE_ERR_SHAPE
+    assert L.moe_expert_forward_gather(*(g[:5] + [128] + g[6:]), FAKE, 1 << 40, None, None) == M.MOE_ERR_SHAPE
 
 
 def test_entry_points_reject_bad_arguments(L):

@@ -368,6 +368,52 @@ int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E,
                         float* dW1, float* dW2, float* dlogits, float* dw,
                         void* ws, size_t ws_bytes, int* status, void* stream);
 
+/* ---------------------------------------------------------------------- */
+/* Pipelined forward on host-resident batches (a runtime around the         */
+/* entry points; the pages have no counterpart: it serves callers whose     */
+/* token batches live in host memory).                                      */
+/* ---------------------------------------------------------------------- */
+#define MOE_PIPELINE_MAX_DEPTH 4
+
+typedef struct moe_pipeline moe_pipeline;  /* opaque, owned by the library */
+
+/* Device bytes moe_pipeline_create needs: `depth` slots of x (bf16 [T][d]),
+ * logits (f32 [T][E]) and out (bf16 [T][d]), then one
+ * moe_expert_forward_workspace_bytes workspace.  0 for an unsupported shape
+ * (as moe_expert_forward, plus T >= 1 and 1 <= depth <=
+ * MOE_PIPELINE_MAX_DEPTH). */
+size_t moe_pipeline_device_bytes(int T, int E, int k, int d, int d_ff, int depth);
+
+/* Create a pipeline on the current device over the caller's device buffer
+ * (1024-byte aligned, at least moe_pipeline_device_bytes; owned by the
+ * caller, who keeps it until moe_pipeline_destroy).  Creates three
+ * non-blocking streams (copy-in, compute, copy-out) and three events per
+ * slot; allocates no device memory.  Errors: MOE_ERR_POINTER (null `out` or
+ * buffer, misaligned buffer), MOE_ERR_SHAPE, MOE_ERR_WORKSPACE,
+ * MOE_ERR_CUDA. */
+int moe_pipeline_create(int T, int E, int k, int d, int d_ff, int depth,
+                        void* device_buffer, size_t bytes, moe_pipeline** out);
+
+/* Enqueue one step and return: copy host_x (bf16 [T][d]) and host_logits
+ * (f32 [T][E]) to the step's slot, run moe_expert_forward with the given
+ * quantised weights (device pointers), copy the output to host_out (bf16
+ * [T][d]).  Step i uses slot i % depth; its copy-in overlaps the forward of
+ * step i - 1 and its copy-out the forward of step i + 1.  The host buffers
+ * must stay untouched until moe_pipeline_synchronize returns (pinned memory
+ * makes the copies asynchronous).  Must be called with the creating device
+ * current (else MOE_ERR_DEVICE).  Errors as moe_expert_forward. */
+int moe_pipeline_submit(moe_pipeline* p, const uint16_t* host_x,
+                        const float* host_logits, uint16_t* host_out,
+                        const uint8_t* w1_codes, const uint8_t* w1_sf,
+                        const float* w1_g, const uint8_t* w2_codes,
+                        const uint8_t* w2_sf, const float* w2_g, int* status);
+
+/* Block until every submitted step, copies included, has finished. */
+int moe_pipeline_synchronize(moe_pipeline* p);
+
+/* Synchronize, then release the streams and events (not the buffer). */
+int moe_pipeline_destroy(moe_pipeline* p);
+
 #ifdef __cplusplus
 }
 #endif

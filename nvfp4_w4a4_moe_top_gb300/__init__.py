@@ -55,6 +55,11 @@ _SIGS = {
     "nvfp4_grouped_gemm_fc1_swiglu": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
     "nvfp4_grouped_gemm_fc2_unpermute": (I32, [P, P, P, P, I32, I64, I32, I32, P, P, P, P, P, P, I32, I32, P, P, P, P, P]),
     "moe_expert_forward": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
+    "moe_pipeline_device_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
+    "moe_pipeline_create": (I32, [I32, I32, I32, I32, I32, I32, P, SZ, P]),
+    "moe_pipeline_submit": (I32, [P, P, P, P, P, P, P, P, P, P, P]),
+    "moe_pipeline_synchronize": (I32, [P]),
+    "moe_pipeline_destroy": (I32, [P]),
     "moe_expert_forward_gather": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_expert_forward_train": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P]),
     "moe_expert_backward_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
@@ -231,6 +236,37 @@ def moe_expert_backward(dY, x, T, E, k, d, d_ff, W1, W2, topk_ids, topk_w, offse
 
 def backward_workspace_bytes(T, E, k, d, d_ff):
     return int(lib().moe_expert_backward_workspace_bytes(T, E, k, d, d_ff))
+
+
+class Pipeline:
+    """moe_pipeline_*: the forward on host-resident batches, with the copies
+    of neighbouring steps overlapping the forward (three streams, `depth`
+    slots).  Host tensors should be pinned."""
+
+    def __init__(self, T, E, k, d, d_ff, depth=2, device="cuda"):
+        import torch
+        n = int(lib().moe_pipeline_device_bytes(T, E, k, d, d_ff, depth))
+        if n == 0:
+            raise MoeError("moe_pipeline_device_bytes", MOE_ERR_SHAPE)
+        self.buf = torch.empty(n + 1024, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 1024
+        self._h = ctypes.c_void_p()
+        _check("moe_pipeline_create", lib().moe_pipeline_create(
+            T, E, k, d, d_ff, depth, ctypes.c_void_p(self.buf.data_ptr() + off), n, ctypes.byref(self._h)))
+
+    def submit(self, x_host, logits_host, out_host, w1q, w2q, status=None):
+        _check("moe_pipeline_submit", lib().moe_pipeline_submit(
+            self._h, _p(x_host), _p(logits_host), _p(out_host), _p(w1q["codes"]), _p(w1q["sf"]), _p(w1q["g"]),
+            _p(w2q["codes"]), _p(w2q["sf"]), _p(w2q["g"]), _p(status)))
+
+    def synchronize(self):
+        _check("moe_pipeline_synchronize", lib().moe_pipeline_synchronize(self._h))
+
+    def close(self):
+        if self._h:
+            rc = lib().moe_pipeline_destroy(self._h)
+            self._h = ctypes.c_void_p()
+            _check("moe_pipeline_destroy", rc)
 
 
 # --------------------------------------------------------------------------

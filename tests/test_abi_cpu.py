@@ -16,13 +16,14 @@ def L():
 
 def test_exports_every_header_function(L):
     names = M.header_functions()
-    assert len(names) == 20, names
+    assert len(names) == 25, names
     for n in names:
         assert hasattr(L, n), n
     for n in ["moe_nvfp4_quantize_weights", "moe_nvfp4_quantize_weights_per_expert", "moe_permute_amax", "nvfp4_quantize_rows",
               "nvfp4_grouped_gemm_fc1_swiglu", "nvfp4_grouped_gemm_fc2_unpermute", "moe_expert_forward",
               "moe_expert_forward_train", "moe_expert_backward", "moe_expert_backward_workspace_bytes",
-              "moe_expert_forward_gather"]:
+              "moe_expert_forward_gather", "moe_pipeline_device_bytes", "moe_pipeline_create",
+              "moe_pipeline_submit", "moe_pipeline_synchronize", "moe_pipeline_destroy"]:
         assert n in names
 
 
@@ -99,6 +100,20 @@ def test_entry_points_reject_bad_arguments(L):
     assert L.moe_expert_backward(*bad, 1 << 40, None, None) == M.MOE_ERR_POINTER
     ft = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 7 + [FAKE, 1 << 40, None, FAKE, FAKE, None, None]
     assert L.moe_expert_forward_train(*ft) == M.MOE_ERR_POINTER
+    # pipeline: sizes and argument checks before any CUDA call
+    ws = M.forward_workspace_bytes(256, 8, 2, 256, 128)
+    up = lambda n: (n + 1023) // 1024 * 1024
+    slot = up(256 * 256 * 2) * 2 + up(256 * 8 * 4)
+    assert L.moe_pipeline_device_bytes(256, 8, 2, 256, 128, 3) == 3 * slot + up(ws)
+    assert L.moe_pipeline_device_bytes(256, 8, 2, 256, 128, 5) == 0
+    assert L.moe_pipeline_device_bytes(0, 8, 2, 256, 128, 2) == 0
+    h = ctypes.c_void_p()
+    assert L.moe_pipeline_create(256, 8, 2, 256, 128, 2, FAKE, 16, ctypes.byref(h)) == M.MOE_ERR_WORKSPACE
+    assert L.moe_pipeline_create(256, 8, 2, 256, 128, 2, MIS, 1 << 40, ctypes.byref(h)) == M.MOE_ERR_POINTER
+    assert L.moe_pipeline_create(256, 8, 2, 200, 128, 2, FAKE, 1 << 40, ctypes.byref(h)) == M.MOE_ERR_SHAPE
+    assert L.moe_pipeline_create(256, 8, 2, 256, 128, 2, FAKE, 1 << 40, None) == M.MOE_ERR_POINTER
+    assert L.moe_pipeline_submit(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == M.MOE_ERR_POINTER
+    assert L.moe_pipeline_destroy(None) == M.MOE_OK
     qe = L.moe_nvfp4_quantize_weights_per_expert
     assert qe(FAKE, 2, 100, 64, FAKE, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert qe(FAKE, 0, 128, 64, FAKE, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE

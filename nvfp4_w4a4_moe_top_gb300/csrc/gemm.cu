@@ -240,35 +240,46 @@ struct ItemRows {
   }
 };
 
-// A slice (128 rows x 128 bytes) of unit u at byte column x: one 128-row box,
-// or, gathered, 32 four-row copies of the rows' tokens (negative -> zero_row).
+// A slice (128 rows x 128 bytes) of unit u at byte column x: one 128-row box
+// (GATHER false, issued by the one producer lane), or, gathered, lane i's
+// four-row copy of rows 4i..4i+3 (their tokens; negative -> zero_row), all
+// 32 lanes of the producer warp issuing together.
+template <bool GATHER>
 __device__ __forceinline__ void load_a_slice(uint32_t dst, const CUtensorMap* tmap_a, int x, int u,
-                                             const int32_t* a_rows, int zero_row, uint32_t bar) {
-  if (!a_rows) {
+                                             const int32_t* a_rows, int zero_row, uint32_t bar, int lane) {
+  if (!GATHER) {
     tma_load_2d(dst, tmap_a, x, u * BM, bar);
     return;
   }
-  const int4* r4 = reinterpret_cast<const int4*>(a_rows + (int64_t)u * BM);
-#pragma unroll 4
-  for (int i = 0; i < BM / 4; ++i) {
-    const int4 r = __ldg(r4 + i);
-    tma_gather4(dst + i * 4 * BK_BYTES, tmap_a, x, r.x < 0 ? zero_row : r.x, r.y < 0 ? zero_row : r.y,
-                r.z < 0 ? zero_row : r.z, r.w < 0 ? zero_row : r.w, bar);
-  }
+  const int4 r = __ldg(reinterpret_cast<const int4*>(a_rows + (int64_t)u * BM) + lane);
+  tma_gather4(dst + lane * 4 * BK_BYTES, tmap_a, x, r.x < 0 ? zero_row : r.x, r.y < 0 ? zero_row : r.y,
+              r.z < 0 ? zero_row : r.z, r.w < 0 ? zero_row : r.w, bar);
 }
 
-// Producer r of R.  The CTA's k-steps (over units, items, K) are numbered
+// Barrier wait of a producer: the single producer lane polls alone; with
+// GATHER the whole warp takes part (lane 0 polls).
+template <bool GATHER>
+__device__ __forceinline__ bool producer_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  return GATHER ? warp_wait(bar, parity, abort_flag, status) : wait_bounded(bar, parity, abort_flag, status);
+}
+
+// Producer r of R: lane 0 of warp PROD + r alone, or, with GATHER, all 32
+// lanes (lane 0 polls the barriers and issues the box and bulk copies, every
+// lane its share of a gathered A slice; the extra lanes cost the epilogue
+// warps issue slots, so the box path keeps one lane).  The CTA's k-steps (over units, items, K) are numbered
 // kc = 0, 1, ...; k-step kc travels through ring kc % R, position kc / R.
 // Each ring has one producer and is consumed in order, so every barrier sees
 // its phases in order.  A producer runs at most R*S k-steps ahead of the
 // MMAs; the plan keeps that below the reach that would let a resident A
 // slot's a_empty wait (at the first item of a unit, by whichever producer
 // owns that k-step) alias an older phase.
+template <bool GATHER>
 __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const uint8_t* a_sf,
                               const uint8_t* b_sf, const Geometry& G, const ItemRows& rows, const int32_t* off, int E,
                               uint32_t a_base, uint32_t ring_base, Tail* tl, volatile int* abort_flag, int* status,
                               const int32_t* a_rows, int zero_row) {
   const uint32_t b_off = G.b_off();
+  const int lane = threadIdx.x & 31;
   uint32_t kc = 0;
   uint32_t last_stage_use[MAX_STAGES], last_a_use[MAX_A_SLOTS];
   for (int i = 0; i < MAX_STAGES; ++i) last_stage_use[i] = 0xFFFFFFFFu;
@@ -287,22 +298,32 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
         if (ring % (uint32_t)NPROD_WARPS != (uint32_t)r) continue;
         uint32_t slot, use;
         G.slot_of(kc, slot, use);
-        if (!wait_bounded(smem_u32(&tl->b_empty[slot]), (use & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
+        if (!producer_wait<GATHER>(smem_u32(&tl->b_empty[slot]), (use & 1u) ^ 1u, abort_flag, status)) {
+          aborted = true;
+          break;
+        }
         const int nsf = min(4, G.kgroups - 4 * ks);
         const uint32_t st = ring_base + slot * G.stage_bytes;
         const uint32_t fb = smem_u32(&tl->b_full[slot]);
         if (G.resident && q == 0) {
-          if (!wait_bounded(smem_u32(&tl->a_empty[ks]), (unit_use & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
+          if (!producer_wait<GATHER>(smem_u32(&tl->a_empty[ks]), (unit_use & 1u) ^ 1u, abort_flag, status)) {
+            aborted = true;
+            break;
+          }
           const uint32_t ab = smem_u32(&tl->a_full[ks]);
-          mbar_arrive_expect_tx(ab, A_SLICE);
-          load_a_slice(a_base + ks * A_SLICE, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, ab);
+          if (lane == 0) mbar_arrive_expect_tx(ab, A_SLICE);
+          if (GATHER) __syncwarp();
+          load_a_slice<GATHER>(a_base + ks * A_SLICE, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, ab, lane);
           last_a_use[ks] = unit_use;
         }
-        mbar_arrive_expect_tx(fb, B_BYTES + 2 * nsf * 512 + b_off);
-        if (!G.resident) load_a_slice(st, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, fb);
-        tma_load_2d(st + b_off, tmap_b, ks * BK_BYTES, br, fb);
-        bulk_load(st + b_off + B_BYTES, b_sf + (sfb_row + 4 * ks) * 512, nsf * 512, fb);
-        bulk_load(st + b_off + B_BYTES + SF_STAGE, a_sf + (sfa_row + 4 * ks) * 512, nsf * 512, fb);
+        if (lane == 0) mbar_arrive_expect_tx(fb, B_BYTES + 2 * nsf * 512 + b_off);
+        if (GATHER) __syncwarp();
+        if (!G.resident) load_a_slice<GATHER>(st, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, fb, lane);
+        if (lane == 0) {
+          tma_load_2d(st + b_off, tmap_b, ks * BK_BYTES, br, fb);
+          bulk_load(st + b_off + B_BYTES, b_sf + (sfb_row + 4 * ks) * 512, nsf * 512, fb);
+          bulk_load(st + b_off + B_BYTES + SF_STAGE, a_sf + (sfa_row + 4 * ks) * 512, nsf * 512, fb);
+        }
         last_stage_use[slot] = use;
       }
     }
@@ -559,9 +580,13 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
     if (lane == 0) {
       prefetch_tmap(tmap_a);
       prefetch_tmap(tmap_b);
-      producer_loop(warp - RL::PROD, tmap_a, tmap_b, a_sf, b_sf, G, rows, off, E, a_base, ring_base, tl,
-                    abort_flag, status, a_rows, zero_row);
     }
+    if (a_rows)
+      producer_loop<true>(warp - RL::PROD, tmap_a, tmap_b, a_sf, b_sf, G, rows, off, E, a_base, ring_base, tl,
+                          abort_flag, status, a_rows, zero_row);
+    else if (lane == 0)
+      producer_loop<false>(warp - RL::PROD, tmap_a, tmap_b, a_sf, b_sf, G, rows, off, E, a_base, ring_base, tl,
+                           abort_flag, status, nullptr, 0);
     __syncwarp();
     return false;
   }

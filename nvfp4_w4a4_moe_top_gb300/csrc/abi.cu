@@ -106,6 +106,19 @@ int encode_gather_rows(CUtensorMap* map, const void* base, int64_t rows, int row
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// FP32 output [rows][cols] written by TMA stores of 32 x 32 boxes (128-byte
+// rows, 128-byte swizzle).
+int encode_f32_out(CUtensorMap* map, void* base, int64_t rows, int cols) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint32_t box[2] = {32u, 32u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int finish() {
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -421,6 +434,7 @@ int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int
   std::memset(&g, 0, sizeof(g));
   if (encode_bf16(&g.tmap_a, dy2, mc, d, 64) != MOE_OK || encode_bf16(&g.tmap_b, h, mc, F, 64) != MOE_OK)
     return MOE_ERR_CUDA;
+  if (encode_f32_out(&g.tmap_out, dW2, (int64_t)E * d, F) != MOE_OK) return MOE_ERR_CUDA;
   g.mode = moe::BWD_WGRAD; g.a_mn = 1; g.E = E; g.offsets = offsets; g.N = F; g.Mo = d; g.out = dW2; g.status = status;
   if (moe::launch_bwd_gemm(g, 0, s) != 0) return MOE_ERR_CUDA;
   // dxr = du . W1_e
@@ -428,6 +442,7 @@ int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int
   if (encode_bf16(&g.tmap_a, du, mc, 2 * F, 128) != MOE_OK ||
       encode_bf16(&g.tmap_b, W1, (int64_t)E * 2 * F, d, 64) != MOE_OK)
     return MOE_ERR_CUDA;
+  if (encode_f32_out(&g.tmap_out, dxr, mc, d) != MOE_OK) return MOE_ERR_CUDA;
   g.mode = moe::BWD_DGRAD; g.a_mn = 0; g.E = E; g.offsets = offsets; g.N = d; g.K = 2 * F; g.out = dxr;
   g.status = status;
   if (moe::launch_bwd_gemm(g, (int)(mc / 128), s) != 0) return MOE_ERR_CUDA;
@@ -435,6 +450,7 @@ int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int
   std::memset(&g, 0, sizeof(g));
   if (encode_bf16(&g.tmap_a, du, mc, 2 * F, 64) != MOE_OK || encode_bf16(&g.tmap_b, xp, mc, d, 64) != MOE_OK)
     return MOE_ERR_CUDA;
+  if (encode_f32_out(&g.tmap_out, dW1, (int64_t)E * 2 * F, d) != MOE_OK) return MOE_ERR_CUDA;
   g.mode = moe::BWD_WGRAD; g.a_mn = 1; g.E = E; g.offsets = offsets; g.N = d; g.Mo = 2 * F; g.out = dW1;
   g.status = status;
   if (moe::launch_bwd_gemm(g, 0, s) != 0) return MOE_ERR_CUDA;

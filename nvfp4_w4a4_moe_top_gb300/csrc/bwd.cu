@@ -54,6 +54,7 @@ constexpr int PROD_WARP = 8, MMA_WARP = 9;
 constexpr int THREADS = 320;
 constexpr int MAX_STAGES = 8;
 constexpr int TMEM_COLS = 512;
+constexpr int STAGE_TILE = 32 * 128;             // FP32 output staging per epilogue warp
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 struct BTail {
@@ -125,6 +126,21 @@ __device__ __forceinline__ void tld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+// Shared -> global tensor store of one box, in this thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack2_rn(float lo, float hi) {
   uint32_t r;
@@ -289,11 +305,18 @@ __device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint
   }
 }
 
-__device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_t tmem, volatile int* abort_flag) {
+// FP32 outputs leave through a per-warp staging tile (32 rows x 128 bytes,
+// 16-byte chunk j of row r at chunk j ^ (r % 8), the 128-byte swizzle of the
+// output tensor map) and one TMA store per 32 x 32 chunk, instead of each
+// lane writing its own row.
+__device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_t tmem, uint32_t staging,
+                         volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q4 = warp & 3, part = warp >> 2;
   const int rl = q4 * 32 + lane;
   const int half = a.bn / 2;
+  const uint32_t stg = staging + (uint32_t)warp * STAGE_TILE;
+  bool pending = false;  // lane 0: a store from stg may still be reading it
   uint32_t it = 0;
   for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
     const Unit U = P.unit(a, u);
@@ -315,18 +338,26 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
         const int64_t row = (int64_t)U.mt * BM + rl;
         swiglu_bwd32(v, a.u + row * 2 * a.F, a.du + row * 2 * a.F, a.F, c0 + c);
       } else {
-        const int64_t orow = a.mode == BWD_WGRAD ? (int64_t)U.e * a.Mo + U.mt * BM + rl : (int64_t)U.mt * BM + rl;
-        float4* o = reinterpret_cast<float4*>(a.out + orow * a.N + c0 + c);
+        const int orow0 = a.mode == BWD_WGRAD ? U.e * a.Mo + U.mt * BM + q4 * 32 : U.mt * BM + q4 * 32;
+        if (lane == 0 && pending) bulk_wait_read0();
+        __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                             __uint_as_float(v[4 * i + 3]));
+        for (int j = 0; j < 8; ++j)
+          sts128(stg + lane * 128 + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&a.tmap_out, stg, c0 + c, orow0);
+          pending = true;
+        }
       }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[acc]));
   }
+  if (lane == 0 && pending) bulk_wait0();  // the last stores complete before the CTA exits
+  __syncwarp();
 }
 
 }  // namespace
@@ -335,7 +366,8 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t stage_bytes = A_TILE + a.bn * 128;
-  BTail* tl = reinterpret_cast<BTail*>(smem + (size_t)a.stages * stage_bytes);
+  uint8_t* staging = smem + (size_t)a.stages * stage_bytes;
+  BTail* tl = reinterpret_cast<BTail*>(staging + NEPI * STAGE_TILE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
@@ -366,6 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
     if (lane == 0) {
       prefetch_tmap(&a.tmap_a);
       prefetch_tmap(&a.tmap_b);
+      if (a.mode != BWD_DGRAD_SWIGLU) prefetch_tmap(&a.tmap_out);
       producer(a, P, ring, tl, abort_flag);
     }
     __syncwarp();
@@ -373,7 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
     if (lane == 0) mma_issuer(a, P, ring, tl, tl->tmem_base, abort_flag);
     __syncwarp();
   } else {
-    epilogue(a, P, tl, tl->tmem_base, abort_flag);
+    epilogue(a, P, tl, tl->tmem_base, smem_u32(staging), abort_flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -383,7 +416,9 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
                  : "memory");
 }
 
-int bwd_gemm_smem_bytes(int bn, int stages) { return 1024 + stages * (A_TILE + bn * 128) + (int)sizeof(BTail); }
+int bwd_gemm_smem_bytes(int bn, int stages) {
+  return 1024 + stages * (A_TILE + bn * 128) + NEPI * STAGE_TILE + (int)sizeof(BTail);
+}
 
 // max_row_tiles: for dgrad, an upper bound of offsets[E] / 128 (the number
 // of units is read on the device); ignored for wgrad.

@@ -92,6 +92,7 @@ struct Fc2Args {
 enum { BWD_DGRAD_SWIGLU = 0, BWD_DGRAD = 1, BWD_WGRAD = 2 };
 struct BwdGemmArgs {
   CUtensorMap tmap_a, tmap_b;  // A: K-major box 64 x 128 (dgrad) or MN-major 64 x 64 (wgrad); B: MN-major 64 x 64
+  CUtensorMap tmap_out;        // DGRAD / WGRAD: FP32 `out`, boxes of 32 x 32, 128-byte swizzle
   int mode, a_mn;
   int E;
   const int32_t* offsets;

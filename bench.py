@@ -173,6 +173,55 @@ def algorithmic(lay):
                 bytes_reduce=bytes_reduce, bytes_quant=bytes_quant, bytes_route=bytes_route)
 
 
+def tiny_latency(dev, reps=200):
+    """Per-forward latency of the tiny layer (T=256, d=256, E=8, top-2,
+    d_ff=128), launch-bound: eager calls against one CUDA-graph replay per
+    forward (the forward is captured once)."""
+    import numpy as np
+    import torch
+
+    import nvfp4_w4a4_moe_top_gb300 as M
+    import synth
+    lay = synth.layer("tiny")
+    T, E, k, d, F = lay.T, lay.E, lay.k, lay.d, lay.d_ff
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    w1q, w2q = M.quantize_weights(to_dev(lay.w1())), M.quantize_weights(to_dev(lay.w2()))
+    x, lg = to_dev(lay.x()), to_dev(lay.logits())
+    out = torch.empty((T, d), dtype=torch.int16, device=dev)
+    ws = M.forward_workspace(T, E, k, d, F, dev)
+    s = torch.cuda.Stream(dev)
+
+    def fwd():
+        M.moe_expert_forward(x, lg, T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"], w2q["sf"],
+                             w2q["g"], out, ws, None, s)
+
+    def per_call(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(10):
+            fn()
+        e0.record(s)
+        for _ in range(reps):
+            fn()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    with torch.cuda.stream(s):
+        fwd()
+    torch.cuda.synchronize()
+    eager = per_call(fwd)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fwd()
+    with torch.cuda.stream(s):  # replay() launches on the current stream
+        graph = per_call(g.replay)
+    return {"workload": "tiny", "eager_us": round(eager, 2), "graph_us": round(graph, 2), "launches": 7}
+
+
 def native(args):
     import numpy as np
     import torch
@@ -314,6 +363,7 @@ def native(args):
     alg0 = algorithmic(lay)
     bwd_flops = 2.0 * (alg0["fc1_flops"] + alg0["fc2_flops"])  # dgrad + wgrad of both GEMMs
     del W1, W2, su, sh, sy, bws, gW1, gW2
+    latency = tiny_latency(dev)
     fb = {"value": round(T / t_fb, 1), "unit": UNIT, "ms_per_step": round(t_fb * 1e3, 4),
           "forward_train_ms": round(t_ftrain * 1e3, 4), "backward_ms": round(t_bwd * 1e3, 4),
           "backward_gemm_tflop": round(bwd_flops / 1e12, 3),
@@ -396,7 +446,7 @@ def native(args):
             "config": {"workload": args.workload, "T": T, "d": d, "E": E, "k": k, "d_ff": F,
                        "parallelism": "token data parallel x%d" % world, "l2": "inputs larger than L2 (no flush)"},
             "gpu_launches": 7 * args.steps, "roofline": roofline, "roofline_hbm": roofline_hbm,
-            "clocks": clocks, "e2e": e2e, "next_rows": next_rows}
+            "clocks": clocks, "e2e": e2e, "next_rows": next_rows, "latency_tiny": latency}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(lay, args)
     if rank == 0:

@@ -321,7 +321,7 @@ int nvfp4_grouped_gemm_fc1_swiglu(const uint8_t* a_codes, const uint8_t* a_sf, c
   a.h_codes = h_codes; a.h_sf = h_sf; a.h_g = h_g; a.dbg_u = dbg_u_f32; a.dbg_h = dbg_h;
   a.scratch = static_cast<uint16_t*>(ws);
   a.status = status;
-  if (moe::launch_fc1(a, (cudaStream_t)stream) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_fc1(a, M_cap, (cudaStream_t)stream) != 0) return MOE_ERR_CUDA;
   return finish();
 }
 
@@ -350,7 +350,7 @@ int nvfp4_grouped_gemm_fc2_unpermute(const uint8_t* h_codes, const uint8_t* h_sf
   a.row_to_token = row_to_token; a.token_slot_row = token_slot_row; a.topk_w = topk_w;
   a.slots = slots; a.dbg_y = dbg_y_f32; a.status = status;
   cudaStream_t s = (cudaStream_t)stream;
-  if (moe::launch_fc2(a, s) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_fc2(a, M_cap, s) != 0) return MOE_ERR_CUDA;
   moe::launch_unpermute_reduce(slots, T, k, d, out, s);
   return finish();
 }
@@ -520,7 +520,7 @@ int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, in
   a1.E = E; a1.d = d; a1.d_ff = d_ff;
   a1.h_codes = h_codes; a1.h_sf = h_sf; a1.h_g = h_g; a1.scratch = scratch; a1.status = status;
   a1.save_u = save_u; a1.dbg_h = save_h;
-  if (moe::launch_fc1(a1, s) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_fc1(a1, mc, s) != 0) return MOE_ERR_CUDA;
 
   moe::Fc2Args a2;
   std::memset(&a2, 0, sizeof(a2));
@@ -530,7 +530,7 @@ int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, in
   a2.E = E; a2.d_ff = d_ff; a2.d = d; a2.k = k;
   a2.row_to_token = r2t; a2.token_slot_row = tsr; a2.topk_w = topk_w; a2.slots = slots; a2.status = status;
   a2.dbg_y = save_y2;
-  if (moe::launch_fc2(a2, s) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_fc2(a2, mc, s) != 0) return MOE_ERR_CUDA;
   moe::launch_unpermute_reduce(slots, T, k, d, out, s);
   return finish();
 }

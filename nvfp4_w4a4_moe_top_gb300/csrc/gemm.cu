@@ -942,25 +942,35 @@ static int set_smem(const void* kernel, size_t smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess ? 0 : -1;
 }
 
-int launch_fc1(Fc1Args& a, cudaStream_t stream) {
+// Persistent grid: one CTA per SM, but no more CTAs than the m_cap / 128
+// row tiles the launch can have (the actual count is read on the device).
+static int fc_grid(int64_t m_cap) {
+  int grid = gemm_num_ctas();
+  if (grid <= 0) return -1;
+  const int64_t tiles = m_cap / BM;
+  if (tiles < grid) grid = tiles < 1 ? 1 : (int)tiles;
+  return grid;
+}
+
+int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
   size_t smem;
   if (!plan(a.d, 2 * (a.d_ff / BN), 2 * a.d_ff, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem)) return -1;
   const bool dbg = a.dbg_u != nullptr || a.dbg_h != nullptr || a.save_u != nullptr;
   void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true> : fc1_swiglu_kernel<false>;
   if (set_smem((const void*)kern, smem) != 0) return -1;
-  const int grid = gemm_num_ctas();
+  const int grid = fc_grid(m_cap);
   if (grid <= 0) return -1;
   kern<<<grid, Roles<FC1_NE>::THREADS, smem, stream>>>(a);
   return 0;
 }
 
-int launch_fc2(Fc2Args& a, cudaStream_t stream) {
+int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream) {
   size_t smem;
   if (!plan(a.d_ff, a.d / BN, a.d, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident, &smem))
     return -1;
   void (*kern)(const Fc2Args) = a.dbg_y != nullptr ? fc2_scatter_kernel<true> : fc2_scatter_kernel<false>;
   if (set_smem((const void*)kern, smem) != 0) return -1;
-  const int grid = gemm_num_ctas();
+  const int grid = fc_grid(m_cap);
   if (grid <= 0) return -1;
   kern<<<grid, Roles<FC2_NE>::THREADS, smem, stream>>>(a);
   return 0;

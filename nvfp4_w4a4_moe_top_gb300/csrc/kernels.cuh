@@ -115,8 +115,8 @@ int launch_bwd_logits(const float* dw, const float* topk_w, const int32_t* topk_
 int launch_bwd_dx(const float* dxr, const int32_t* token_slot_row, int T, int k, int d, float* dx, cudaStream_t stream);
 
 int gemm_num_ctas();  // persistent grid size on the current device
-int launch_fc1(Fc1Args& a, cudaStream_t stream);
-int launch_fc2(Fc2Args& a, cudaStream_t stream);
+int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream);
+int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream);
 constexpr int kMaxGemmCtas = 256;
 
 }  // namespace moe

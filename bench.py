@@ -338,7 +338,6 @@ def native(args):
     mc = M.m_cap(T, E, k)
     su = torch.empty((mc, 2 * F), dtype=torch.int16, device=dev)
     sh = torch.empty((mc, F), dtype=torch.int16, device=dev)
-    sy = torch.empty((mc, d), dtype=torch.float32, device=dev)
     dY = to_dev(synth.layer(args.workload, seed=shard_seed(args.seed, rank)).grad_out())
     gx = torch.empty((T, d), dtype=torch.float32, device=dev)
     gW1 = torch.empty((E, 2 * F, d), dtype=torch.float32, device=dev)
@@ -350,26 +349,26 @@ def native(args):
 
     def fwd_train():
         M.moe_expert_forward_train(x, lg, T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"], w2q["sf"],
-                                   w2q["g"], out, ws, su, sh, sy, status, stream)
+                                   w2q["g"], out, ws, su, sh, status, stream)
 
     def bwd():
-        M.moe_expert_backward(dY, x, T, E, k, d, F, W1, W2, fv["topk_ids"], fv["topk_w"], fv["offsets"],
-                              fv["row_to_token"], fv["token_slot_row"], su, sh, sy, gx, gW1, gW2, gl, gw, bws, status,
-                              stream)
+        M.moe_expert_backward(dY, x, T, E, k, d, F, W1, W2, w2q["codes"], w2q["sf"], w2q["g"], fv["topk_ids"],
+                              fv["topk_w"], fv["offsets"], fv["row_to_token"], fv["token_slot_row"], su, sh,
+                              fv["h_codes"], fv["h_sf"], fv["h_g"], gx, gW1, gW2, gl, gw, bws, status, stream)
 
     t_ftrain = timed(fwd_train)
     t_bwd = timed(bwd)
     t_fb = timed(lambda: (fwd_train(), bwd()))
     alg0 = algorithmic(lay)
     bwd_flops = 2.0 * (alg0["fc1_flops"] + alg0["fc2_flops"])  # dgrad + wgrad of both GEMMs
-    del W1, W2, su, sh, sy, bws, gW1, gW2
+    del W1, W2, su, sh, bws, gW1, gW2
     latency = tiny_latency(dev)
     fb = {"value": round(T / t_fb, 1), "unit": UNIT, "ms_per_step": round(t_fb * 1e3, 4),
           "forward_train_ms": round(t_ftrain * 1e3, 4), "backward_ms": round(t_bwd * 1e3, 4),
           "backward_gemm_tflop": round(bwd_flops / 1e12, 3),
           "backward_bf16_tflops": round(bwd_flops / t_bwd / 1e12, 1),
           "backward_frac_of_bf16_peak": round(bwd_flops / t_bwd / 1e12 / peaks["bf16_tflops"], 4),
-          "launches": 13, "workload": "forward with saved values + BF16 backward, dY ~ N(0, 1e-3)"}
+          "launches": 14, "workload": "forward with saved values + BF16 backward, dY ~ N(0, 1e-3)"}
     wq = lambda t: {"ms": round(t * 1e3, 4), "achieved": round(wq_bytes / t / 1e9, 1), "unit": "GB/s",
                     "frac": round(wq_bytes / t / 1e9 / peaks["hbm_gbs"], 4)}
     next_rows = {"weight_quant_per_row": dict(wq(t_wq_row), launches=2),

@@ -315,28 +315,27 @@ int moe_expert_forward_gather(const uint16_t* x, const float* logits, int T,
  *   save_u   bf16 [M_cap][2 d_ff] (out) u = BF16(FC1 output), gate half first
  *   save_h   bf16 [M_cap][d_ff]   (out) h = BF16(silu(u_gate) u_up) before
  *            requantisation
- *   save_y2  f32  [M_cap][d]      (out) expert outputs before the router
- *            weighting
- * Rows below offsets[E] are written (pad rows: u = h = 0; y2 of pad rows is
- * not written); rows at or past offsets[E] are untouched.  The routing and
- * permutation the backward needs stay in `ws` (moe_expert_forward_workspace_
- * layout entries 0, 1, 2, 4, 5).  M_cap = moe_m_cap(T, E, k).  Errors as
- * moe_expert_forward, plus MOE_ERR_POINTER for a missing save buffer. */
+ * Rows below offsets[E] are written (pad rows: u = h = 0); rows at or past
+ * offsets[E] are untouched.  The routing, the permutation and the
+ * requantised h that the backward needs stay in `ws`
+ * (moe_expert_forward_workspace_layout entries 0, 1, 2, 4, 5, 10, 11, 12).
+ * M_cap = moe_m_cap(T, E, k).  Errors as moe_expert_forward, plus
+ * MOE_ERR_POINTER for a missing save buffer. */
 int moe_expert_forward_train(const uint16_t* x, const float* logits, int T,
                              int E, int k, int d, int d_ff,
                              const uint8_t* w1_codes, const uint8_t* w1_sf,
                              const float* w1_g, const uint8_t* w2_codes,
                              const uint8_t* w2_sf, const float* w2_g,
                              uint16_t* out, void* ws, size_t ws_bytes,
-                             uint16_t* save_u, uint16_t* save_h,
-                             float* save_y2, int* status, void* stream);
+                             uint16_t* save_u, uint16_t* save_h, int* status,
+                             void* stream);
 
 /* Straight-through BF16 backward of the expert layer (main paper,
  * contributions list; AI summary, "Methodology in Plain English": a
  * straight-through estimator on the saved BF16 activations and weights, no
  * backward quantisation; rainbus summary, method step 5: BF16 GEMMs on the
- * saved BF16 operands).  With y2, u, h from moe_expert_forward_train and
- * w = topk_w:
+ * saved BF16 operands).  With u, h from moe_expert_forward_train, y2 the
+ * forward's FP32 expert outputs and w = topk_w:
  *   dw[t][j]    = sum_n dY[t][n] y2[row(t,j)][n]                      (FP32)
  *   dlogits[t][ids[t][j]] = w_j (dw_j - sum_i w_i dw_i), 0 elsewhere   (FP32)
  *   dy2[row]    = BF16(RN_f32(w_tj dY[t]))                (BF16 GEMM operand)
@@ -345,26 +344,36 @@ int moe_expert_forward_train(const uint16_t* x, const float* logits, int T,
  *                 g = u[gate], up = u[up], s = sigmoid(g) (BF16 GEMM operand)
  *   dW2_e       = dy2_e^T . h_e,   dW1_e = du_e^T . x_e   (FP32 out)
  *   dx[t]       = sum_j (du . W1_e)[row(t,j)], ascending j (FP32 out)
+ * y2 is not stored by the forward: the backward recomputes it with the
+ * forward's own FC2 kernel from the requantised h and the quantised W2
+ * (bit-identical), taking the dot products with dY in that kernel's
+ * epilogue.
  *   dY        bf16 [T][d];  x bf16 [T][d] (the forward's input)
  *   W1, W2    bf16 [E][2 d_ff][d], [E][d][d_ff]: the ORIGINAL weights
- *   topk_ids, topk_w, offsets, row_to_token, token_slot_row: the forward's
- *             routing and permutation
- *   u, h, y2  the forward's saved values
+ *   w2_codes, w2_sf, w2_g   the quantised W2 the forward used
+ *   topk_ids, topk_w, offsets, row_to_token, token_slot_row, h_codes, h_sf,
+ *   h_g       the forward's routing, permutation and requantised h
+ *             (moe_expert_forward_workspace_layout entries 0, 1, 4, 5, 2,
+ *             10, 11, 12 of the training forward's workspace)
+ *   u, h      the forward's saved values
  *   dx f32 [T][d], dW1 f32 [E][2 d_ff][d], dW2 f32 [E][d][d_ff],
  *   dw f32 [T][k] (out); dlogits f32 [T][E] (out, or NULL to skip)
  *   ws        moe_expert_backward_workspace_bytes(...) bytes
- * Seven launches on `stream` (rows, logits, four tcgen05 BF16 grouped GEMMs,
- * dx reduce), no host synchronisation.  Experts without rows get zero
- * weight gradients.  Errors: MOE_ERR_SHAPE as moe_expert_forward,
- * MOE_ERR_POINTER, MOE_ERR_WORKSPACE, MOE_ERR_DEVICE, MOE_ERR_CUDA; a wait
- * that runs out sets MOE_STATUS_TIMEOUT. */
+ * Eight launches on `stream` (FC2 recomputation with dw and dy2, x rows,
+ * logits, four tcgen05 BF16 grouped GEMMs, dx reduce), no host
+ * synchronisation.  Experts without rows get zero weight gradients.
+ * Errors: MOE_ERR_SHAPE as moe_expert_forward, MOE_ERR_POINTER,
+ * MOE_ERR_WORKSPACE, MOE_ERR_DEVICE, MOE_ERR_CUDA; a wait that runs out sets
+ * MOE_STATUS_TIMEOUT. */
 int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E,
                         int k, int d, int d_ff, const uint16_t* W1,
-                        const uint16_t* W2, const int32_t* topk_ids,
-                        const float* topk_w, const int32_t* offsets,
-                        const int32_t* row_to_token,
+                        const uint16_t* W2, const uint8_t* w2_codes,
+                        const uint8_t* w2_sf, const float* w2_g,
+                        const int32_t* topk_ids, const float* topk_w,
+                        const int32_t* offsets, const int32_t* row_to_token,
                         const int32_t* token_slot_row, const uint16_t* u,
-                        const uint16_t* h, const float* y2, float* dx,
+                        const uint16_t* h, const uint8_t* h_codes,
+                        const uint8_t* h_sf, const float* h_g, float* dx,
                         float* dW1, float* dW2, float* dlogits, float* dw,
                         void* ws, size_t ws_bytes, int* status, void* stream);
 

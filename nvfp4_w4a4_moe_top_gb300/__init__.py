@@ -61,10 +61,9 @@ _SIGS = {
     "moe_pipeline_synchronize": (I32, [P]),
     "moe_pipeline_destroy": (I32, [P]),
     "moe_expert_forward_gather": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
-    "moe_expert_forward_train": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P, P, P, P]),
+    "moe_expert_forward_train": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P, P, P]),
     "moe_expert_backward_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
-    "moe_expert_backward": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ,
-                                  P, P]),
+    "moe_expert_backward": (I32, [P, P, I32, I32, I32, I32, I32] + [P] * 21 + [SZ, P, P]),
 }
 
 _lib = None
@@ -219,18 +218,20 @@ def moe_expert_forward_gather(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g
 
 
 def moe_expert_forward_train(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws,
-                             save_u, save_h, save_y2, status=None, stream=None):
+                             save_u, save_h, status=None, stream=None):
     _check("moe_expert_forward_train", lib().moe_expert_forward_train(
         _p(x), _p(logits), T, E, k, d, d_ff, _p(w1_codes), _p(w1_sf), _p(w1_g), _p(w2_codes), _p(w2_sf),
         _p(w2_g), _p(out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(save_u), _p(save_h),
-        _p(save_y2), _p(status), _s(stream)))
+        _p(status), _s(stream)))
 
 
-def moe_expert_backward(dY, x, T, E, k, d, d_ff, W1, W2, topk_ids, topk_w, offsets, row_to_token, token_slot_row,
-                        u, h, y2, dx, dW1, dW2, dlogits, dw, ws, status=None, stream=None):
+def moe_expert_backward(dY, x, T, E, k, d, d_ff, W1, W2, w2_codes, w2_sf, w2_g, topk_ids, topk_w, offsets,
+                        row_to_token, token_slot_row, u, h, h_codes, h_sf, h_g, dx, dW1, dW2, dlogits, dw, ws,
+                        status=None, stream=None):
     _check("moe_expert_backward", lib().moe_expert_backward(
-        _p(dY), _p(x), T, E, k, d, d_ff, _p(W1), _p(W2), _p(topk_ids), _p(topk_w), _p(offsets), _p(row_to_token),
-        _p(token_slot_row), _p(u), _p(h), _p(y2), _p(dx), _p(dW1), _p(dW2), _p(dlogits), _p(dw), _p(ws),
+        _p(dY), _p(x), T, E, k, d, d_ff, _p(W1), _p(W2), _p(w2_codes), _p(w2_sf), _p(w2_g), _p(topk_ids),
+        _p(topk_w), _p(offsets), _p(row_to_token), _p(token_slot_row), _p(u), _p(h), _p(h_codes), _p(h_sf),
+        _p(h_g), _p(dx), _p(dW1), _p(dW2), _p(dlogits), _p(dw), _p(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _p(status), _s(stream)))
 
 

@@ -376,11 +376,11 @@ int moe_expert_forward_gather(const uint16_t* x, const float* logits, int T, int
 int moe_expert_forward_train(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
                              const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g,
                              const uint8_t* w2_codes, const uint8_t* w2_sf, const float* w2_g, uint16_t* out,
-                             void* ws, size_t ws_bytes, uint16_t* save_u, uint16_t* save_h, float* save_y2,
-                             int* status, void* stream) {
-  if (T > 0 && (!ok_ptr(save_u) || !ok_ptr(save_h) || !ok_ptr(save_y2))) return MOE_ERR_POINTER;
+                             void* ws, size_t ws_bytes, uint16_t* save_u, uint16_t* save_h, int* status,
+                             void* stream) {
+  if (T > 0 && (!ok_ptr(save_u) || !ok_ptr(save_h))) return MOE_ERR_POINTER;
   return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
-                      save_u, save_h, save_y2, false, status, stream);
+                      save_u, save_h, nullptr, false, status, stream);
 }
 
 size_t moe_expert_backward_workspace_bytes(int T, int E, int k, int d, int d_ff) {
@@ -389,16 +389,19 @@ size_t moe_expert_backward_workspace_bytes(int T, int E, int k, int d, int d_ff)
 }
 
 int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int k, int d, int d_ff,
-                        const uint16_t* W1, const uint16_t* W2, const int32_t* topk_ids, const float* topk_w,
-                        const int32_t* offsets, const int32_t* row_to_token, const int32_t* token_slot_row,
-                        const uint16_t* u, const uint16_t* h, const float* y2, float* dx, float* dW1, float* dW2,
-                        float* dlogits, float* dw, void* ws, size_t ws_bytes, int* status, void* stream) {
+                        const uint16_t* W1, const uint16_t* W2, const uint8_t* w2_codes, const uint8_t* w2_sf,
+                        const float* w2_g, const int32_t* topk_ids, const float* topk_w, const int32_t* offsets,
+                        const int32_t* row_to_token, const int32_t* token_slot_row, const uint16_t* u,
+                        const uint16_t* h, const uint8_t* h_codes, const uint8_t* h_sf, const float* h_g, float* dx,
+                        float* dW1, float* dW2, float* dlogits, float* dw, void* ws, size_t ws_bytes, int* status,
+                        void* stream) {
   if (!ok_model_shape(T, E, k, d, d_ff)) return MOE_ERR_SHAPE;
   if (!ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(dW1) || !ok_ptr(dW2) || !ok_opt(dlogits) || !ok_opt(status))
     return MOE_ERR_POINTER;
-  if (T > 0 && (!ok_ptr(dY) || !ok_ptr(x) || !ok_ptr(topk_ids) || !ok_ptr(topk_w) || !ok_ptr(offsets) ||
-                !ok_ptr(row_to_token) || !ok_ptr(token_slot_row) || !ok_ptr(u) || !ok_ptr(h) || !ok_ptr(y2) ||
-                !ok_ptr(dx) || !ok_ptr(dw) || !ok_ptr(ws)))
+  if (T > 0 && (!ok_ptr(dY) || !ok_ptr(x) || !ok_ptr(w2_codes) || !ok_ptr(w2_sf) || !ok_ptr(w2_g) ||
+                !ok_ptr(topk_ids) || !ok_ptr(topk_w) || !ok_ptr(offsets) || !ok_ptr(row_to_token) ||
+                !ok_ptr(token_slot_row) || !ok_ptr(u) || !ok_ptr(h) || !ok_ptr(h_codes) || !ok_ptr(h_sf) ||
+                !ok_ptr(h_g) || !ok_ptr(dx) || !ok_ptr(dw) || !ok_ptr(ws)))
     return MOE_ERR_POINTER;
   const BwdLayout L = bwd_layout(T, E, k, d, d_ff);
   if (T > 0 && ws_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -419,7 +422,17 @@ int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int
   const int64_t mc = m_cap_of(T, E, k);
   const int F = d_ff;
 
-  moe::launch_bwd_rows(dY, x, y2, topk_w, row_to_token, token_slot_row, offsets, E, T, k, d, mc, dy2, xp, dw, s);
+  // the forward's FC2 again (same kernel, same y2), against dY: dw and dy2
+  moe::Fc2Args a2;
+  std::memset(&a2, 0, sizeof(a2));
+  if (encode_operand(&a2.tmap_a, h_codes, mc, F / 2) != MOE_OK) return MOE_ERR_CUDA;
+  if (encode_operand(&a2.tmap_b, w2_codes, (int64_t)E * d, F / 2) != MOE_OK) return MOE_ERR_CUDA;
+  a2.a_sf = h_sf; a2.a_g = h_g; a2.w_sf = w2_sf; a2.w_g = w2_g; a2.offsets = offsets;
+  a2.E = E; a2.d_ff = F; a2.d = d; a2.k = k;
+  a2.row_to_token = row_to_token; a2.token_slot_row = token_slot_row; a2.topk_w = topk_w;
+  a2.dY = dY; a2.dy2 = dy2; a2.dw = dw; a2.status = status;
+  if (moe::launch_fc2(a2, mc, s) != 0) return MOE_ERR_CUDA;
+  moe::launch_bwd_xrows(x, row_to_token, offsets, E, T, d, mc, xp, s);
   if (dlogits) moe::launch_bwd_logits(dw, topk_w, topk_ids, T, E, k, dlogits, s);
 
   moe::BwdGemmArgs g;

@@ -6,11 +6,13 @@
 // the table: the layer bypass saves the original BF16 operands).
 //
 // Launch sequence of moe_expert_backward:
-//   bwd_rows_kernel     per permuted row r of token t, slot j:
-//                         dy2[r] = BF16(RN_f32(w_tj * dY[t]))  (GEMM operand)
-//                         xp[r]  = x[t]                        (GEMM operand)
+//   fc2_scatter_kernel<2> (gemm.cu) recomputes the forward's expert outputs
+//                       y2 from the saved FP4 operands (bit-identical) and,
+//                       per permuted row r of token t, slot j:
 //                         dw[t][j] = <dY[t], y2[r]>            (FP32)
-//                       pad rows of dy2 and xp are zeroed.
+//                         dy2[r] = BF16(RN_f32(w_tj * dY[t]))  (GEMM operand)
+//                       with dy2 zero on pad rows.
+//   bwd_xrows_kernel    xp[r] = x[t] (GEMM operand), zero on pad rows.
 //   bwd_logits_kernel   dlogits[t][e_j] = w_j (dw_j - sum_i w_i dw_i).
 //   bwd_gemm (DGRAD_SWIGLU)  dh = dy2 . W2_e (FP32 in tensor memory), then
 //                       SwiGLU backward in the epilogue against the saved u:
@@ -441,56 +443,25 @@ int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream) {
 // ---------------------------------------------------------------------------
 // Row, logit and dx kernels (HBM-bound, one warp per row or token)
 // ---------------------------------------------------------------------------
-// Permuted row r: slot j of token t = row_to_token[r] (found among the k
-// entries of token_slot_row[t]); pad rows are zeroed (dy2, xp); rows at or
-// past offsets[E] are left alone.  d % 8 == 0.
-__global__ void __launch_bounds__(256) bwd_rows_kernel(const uint16_t* __restrict__ dY, const uint16_t* __restrict__ x,
-                                                       const float* __restrict__ y2, const float* __restrict__ topk_w,
-                                                       const int32_t* __restrict__ row_to_token,
-                                                       const int32_t* __restrict__ token_slot_row,
-                                                       const int32_t* __restrict__ offsets, int E, int T, int k, int d,
-                                                       int64_t m_rows, uint16_t* __restrict__ dy2,
-                                                       uint16_t* __restrict__ xp, float* __restrict__ dw) {
+// xp[r] = x[row_to_token[r]] (the wgrad operand of FC1), zero on pad rows;
+// rows at or past offsets[E] are left alone.  d % 8 == 0.
+__global__ void __launch_bounds__(256) bwd_xrows_kernel(const uint16_t* __restrict__ x,
+                                                        const int32_t* __restrict__ row_to_token,
+                                                        const int32_t* __restrict__ offsets, int E, int T, int d,
+                                                        int64_t m_rows, uint16_t* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= m_rows) return;
-  const int n8 = d / 8;
-  uint4* drow = reinterpret_cast<uint4*>(dy2 + r * d);
-  uint4* xrow = reinterpret_cast<uint4*>(xp + r * d);
   if (r >= __ldg(offsets + E)) return;  // past the padded rows: never read
+  const int n8 = d / 8;
+  uint4* xrow = reinterpret_cast<uint4*>(xp + r * d);
   const int t = __ldg(row_to_token + r);
   if (t < 0 || t >= T) {
-    for (int i = lane; i < n8; i += 32) {
-      drow[i] = make_uint4(0u, 0u, 0u, 0u);
-      xrow[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int i = lane; i < n8; i += 32) xrow[i] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  int j = 0;
-  for (int jj = 0; jj < k; ++jj)
-    if (__ldg(token_slot_row + (int64_t)t * k + jj) == r) j = jj;
-  const float w = __ldg(topk_w + (int64_t)t * k + j);
-  const uint4* yrow = reinterpret_cast<const uint4*>(dY + (int64_t)t * d);
   const uint4* xsrc = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
-  const float4* y2row = reinterpret_cast<const float4*>(y2 + r * d);
-  float dot = 0.0f;
-  for (int i = lane; i < n8; i += 32) {
-    const uint4 g = __ldg(yrow + i);
-    const float4 p0 = __ldg(y2row + 2 * i), p1 = __ldg(y2row + 2 * i + 1);
-    const float gv[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
-                         bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
-    const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) o[q] = pack2_rn(__fmul_rn(w, gv[2 * q]), __fmul_rn(w, gv[2 * q + 1]));
-#pragma unroll
-    for (int q = 0; q < 8; ++q) dot = fmaf(gv[q], pv[q], dot);
-    drow[i] = make_uint4(o[0], o[1], o[2], o[3]);
-    xrow[i] = __ldg(xsrc + i);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-  if (lane == 0) dw[(int64_t)t * k + j] = dot;
+  for (int i = lane; i < n8; i += 32) xrow[i] = __ldg(xsrc + i);
 }
 
 // dlogits[t][:] = 0, then w_j (dw_j - sum_i w_i dw_i) at the selected ids.
@@ -534,12 +505,10 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(const float* __restrict__ d
   }
 }
 
-int launch_bwd_rows(const uint16_t* dY, const uint16_t* x, const float* y2, const float* topk_w,
-                    const int32_t* row_to_token, const int32_t* token_slot_row, const int32_t* offsets, int E, int T,
-                    int k, int d, int64_t m_rows, uint16_t* dy2, uint16_t* xp, float* dw, cudaStream_t stream) {
+int launch_bwd_xrows(const uint16_t* x, const int32_t* row_to_token, const int32_t* offsets, int E, int T, int d,
+                     int64_t m_rows, uint16_t* xp, cudaStream_t stream) {
   if (m_rows <= 0) return 0;
-  bwd_rows_kernel<<<(unsigned)((m_rows + 7) / 8), 256, 0, stream>>>(dY, x, y2, topk_w, row_to_token, token_slot_row,
-                                                                     offsets, E, T, k, d, m_rows, dy2, xp, dw);
+  bwd_xrows_kernel<<<(unsigned)((m_rows + 7) / 8), 256, 0, stream>>>(x, row_to_token, offsets, E, T, d, m_rows, xp);
   return 0;
 }
 

@@ -762,10 +762,15 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
 // ---------------------------------------------------------------------------
 // FC2 + router-weighted scatter
 // ---------------------------------------------------------------------------
-// DBG: also write the debug output (pre-weighting FP32 y2) when its pointer
-// is set.
-template <bool DBG>
+// MODE 0: the forward (z to the slots).  MODE 1: also the debug output
+// (pre-weighting FP32 y2).  MODE 2: the straight-through backward's
+// recomputation of the same y2 (same code, same results) against the output
+// gradient: dw[t][j] = sum_n dY[t][n] y2[row][n] (FP32) and the BF16 dgrad
+// operand dy2[row] = BF16(w_tj dY[t]) written in place of the slots (zero on
+// pad rows); no slots.
+template <int MODE>
 __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(const __grid_constant__ Fc2Args args) {
+  constexpr bool DBG = MODE == 1, DW = MODE == 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int d = args.d, k = args.k;
@@ -821,7 +826,9 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
       float* gws = gw_s + (uc & 1) * d;
       stage_scales<FC2_NE>(gws, args.w_g + (int64_t)e * d, d, threadIdx.x);
       epi_barrier<FC2_NE>();
-      uint16_t* dst_row = args.slots + ((int64_t)(t < 0 ? 0 : t) * k + j) * d;
+      uint16_t* dst_row = DW ? args.dy2 + row * d : args.slots + ((int64_t)(t < 0 ? 0 : t) * k + j) * d;
+      const uint16_t* dy_row = DW ? args.dY + (int64_t)(t < 0 ? 0 : t) * d : nullptr;
+      float dot = 0.0f;
       for (int nt = 0; nt < G.items; ++nt, ++it) {
         const uint32_t slot = it % FC2_NSLOT;
         bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
@@ -856,9 +863,24 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
                 const int m = i + jj;
                 const float y0 = __fmul_rn(__uint_as_float(R[hf][m]), __fmul_rn(gh, f[jj]));
                 const float y1 = __fmul_rn(__uint_as_float(R[hf][m + 1]), __fmul_rn(gh, f[jj + 1]));
-                zp[m >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
+                if (!DW) zp[m >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
                 yv[m] = y0;
                 yv[m + 1] = y1;
+              }
+            }
+            if (DW) {  // the output gradient's 16 columns of this token
+              uint4 g0 = make_uint4(0u, 0u, 0u, 0u), g1 = g0;
+              if (t >= 0) {
+                g0 = __ldg(reinterpret_cast<const uint4*>(dy_row + n0));
+                g1 = __ldg(reinterpret_cast<const uint4*>(dy_row + n0) + 1);
+              }
+              const uint32_t gw4[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const float d0 = bf16_lo(gw4[q]), d1 = bf16_hi(gw4[q]);
+                dot = fmaf(d0, yv[2 * q], dot);
+                dot = fmaf(d1, yv[2 * q + 1], dot);
+                zp[q] = bf16x2_rn(__fmul_rn(w, d0), __fmul_rn(w, d1));
               }
             }
             if (DBG && args.dbg_y && t >= 0) {  // two 32-byte sectors
@@ -871,7 +893,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
           }
           __syncwarp();
           const unsigned long long my_dst =
-              t >= 0 ? reinterpret_cast<unsigned long long>(dst_row + nt * BN + part * 64) : 0ull;
+              (DW || t >= 0) ? reinterpret_cast<unsigned long long>(dst_row + nt * BN + part * 64) : 0ull;
           const int sub = lane >> 3, ch = lane & 7;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -882,6 +904,11 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
           }
           __syncwarp();
         }
+      }
+      if (DW) {  // dw of the row: the two column parts' sums, part 0 + part 1
+        tl->rowmax[part][rl] = dot;
+        epi_barrier<FC2_NE>();
+        if (part == 0 && t >= 0) args.dw[(int64_t)t * k + j] = dot + tl->rowmax[1][rl];
       }
     }
   }
@@ -968,7 +995,9 @@ int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream) {
   size_t smem;
   if (!plan(a.d_ff, a.d / BN, a.d, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident, &smem))
     return -1;
-  void (*kern)(const Fc2Args) = a.dbg_y != nullptr ? fc2_scatter_kernel<true> : fc2_scatter_kernel<false>;
+  void (*kern)(const Fc2Args) = a.dw != nullptr      ? fc2_scatter_kernel<2>
+                                 : a.dbg_y != nullptr ? fc2_scatter_kernel<1>
+                                                      : fc2_scatter_kernel<0>;
   if (set_smem((const void*)kern, smem) != 0) return -1;
   const int grid = fc_grid(m_cap);
   if (grid <= 0) return -1;

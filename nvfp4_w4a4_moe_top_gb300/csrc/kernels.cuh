@@ -84,6 +84,11 @@ struct Fc2Args {
   const float* topk_w;
   uint16_t* slots;
   float* dbg_y;
+  // backward recomputation (dw set): dY bf16 [T][d] in, dy2 bf16 [rows][d]
+  // and dw f32 [T][k] out, no slots
+  const uint16_t* dY;
+  uint16_t* dy2;
+  float* dw;
   int* status;
   int rings, na, nb, resident;  // pipeline plan, set by launch_fc2
 };
@@ -107,9 +112,8 @@ struct BwdGemmArgs {
   int bn, stages;     // set by launch_bwd_gemm
 };
 int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream);
-int launch_bwd_rows(const uint16_t* dY, const uint16_t* x, const float* y2, const float* topk_w,
-                    const int32_t* row_to_token, const int32_t* token_slot_row, const int32_t* offsets, int E, int T,
-                    int k, int d, int64_t m_rows, uint16_t* dy2, uint16_t* xp, float* dw, cudaStream_t stream);
+int launch_bwd_xrows(const uint16_t* x, const int32_t* row_to_token, const int32_t* offsets, int E, int T, int d,
+                     int64_t m_rows, uint16_t* xp, cudaStream_t stream);
 int launch_bwd_logits(const float* dw, const float* topk_w, const int32_t* topk_ids, int T, int E, int k,
                       float* dlogits, cudaStream_t stream);
 int launch_bwd_dx(const float* dxr, const int32_t* token_slot_row, int T, int k, int d, float* dx, cudaStream_t stream);

@@ -87,7 +87,7 @@ def test_entry_points_reject_bad_arguments(L):
     assert L.moe_nvfp4_quantize_weights(FAKE, 2, 128, 48, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_SHAPE
     assert L.moe_nvfp4_quantize_weights(None, 2, 128, 64, FAKE, FAKE, FAKE, None, None) == M.MOE_ERR_POINTER
     # backward: shape, pointer and workspace checks before any CUDA call
-    bw = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 13 + [None, FAKE, FAKE]
+    bw = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 18 + [None, FAKE, FAKE]
     assert L.moe_expert_backward(*bw, 16, None, None) == M.MOE_ERR_WORKSPACE
     bad = list(bw)
     bad[5] = 200
@@ -96,9 +96,9 @@ def test_entry_points_reject_bad_arguments(L):
     bad[7] = None  # W1
     assert L.moe_expert_backward(*bad, 1 << 40, None, None) == M.MOE_ERR_POINTER
     bad = list(bw)
-    bad[16] = MIS  # y2
+    bad[19] = MIS  # h codes
     assert L.moe_expert_backward(*bad, 1 << 40, None, None) == M.MOE_ERR_POINTER
-    ft = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 7 + [FAKE, 1 << 40, None, FAKE, FAKE, None, None]
+    ft = [FAKE, FAKE, 256, 8, 2, 256, 128] + [FAKE] * 7 + [FAKE, 1 << 40, None, FAKE, None, None]
     assert L.moe_expert_forward_train(*ft) == M.MOE_ERR_POINTER
     # pipeline: sizes and argument checks before any CUDA call
     ws = M.forward_workspace_bytes(256, 8, 2, 256, 128)

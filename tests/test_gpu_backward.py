@@ -1,5 +1,7 @@
 """Parity of the straight-through BF16 backward (moe_expert_forward_train +
-moe_expert_backward) with the oracle.
+moe_expert_backward) with the oracle.  The backward recomputes the
+forward's expert outputs y2 (FC2 again on the saved FP4 operands); the
+oracle gets the forward's y2 from the modular FC2's debug output.
 
 Stage-wise, the oracle fed the GPU's own saved forward values (u, h, y2 and
 the routing, which are bit-exact with the oracle's forward):
@@ -49,19 +51,26 @@ def gpu_train_step(lay, x, lg, W1, W2, dY):
     ws = M.forward_workspace(T, E, k, d, F)
     su = torch.full((mc, 2 * F), 0x7FC0, dtype=torch.int16, device="cuda")
     sh = torch.full((mc, F), 0x7FC0, dtype=torch.int16, device="cuda")
-    sy = torch.full((mc, d), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     M.moe_expert_forward_train(dev(x), dev(lg), T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"],
-                               w2q["sf"], w2q["g"], out, ws, su, sh, sy, st)
+                               w2q["sf"], w2q["g"], out, ws, su, sh, st)
     v = M.forward_views(ws, T, E, k, d, F)
+    # the forward's FP32 expert outputs, for the oracle only: the modular FC2
+    # on the same requantised h (its debug output), into scratch buffers
+    sy = torch.full((mc, d), float("nan"), dtype=torch.float32, device="cuda")
+    M.nvfp4_grouped_gemm_fc2_unpermute(v["h_codes"], v["h_sf"], v["h_g"], v["offsets"], E, mc, F, d, w2q["codes"],
+                                       w2q["sf"], w2q["g"], v["row_to_token"], v["token_slot_row"], v["topk_w"], T,
+                                       k, torch.empty((T, k, d), dtype=torch.int16, device="cuda"),
+                                       torch.empty((T, d), dtype=torch.int16, device="cuda"), sy)
     dx = torch.full((T, d), float("nan"), dtype=torch.float32, device="cuda")
     dW1 = torch.full((E, 2 * F, d), float("nan"), dtype=torch.float32, device="cuda")
     dW2 = torch.full((E, d, F), float("nan"), dtype=torch.float32, device="cuda")
     dl = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
     dw = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
     bws = torch.empty(M.backward_workspace_bytes(T, E, k, d, F), dtype=torch.uint8, device="cuda")
-    M.moe_expert_backward(dev(dY), dev(x), T, E, k, d, F, W1d, W2d, v["topk_ids"], v["topk_w"], v["offsets"],
-                          v["row_to_token"], v["token_slot_row"], su, sh, sy, dx, dW1, dW2, dl, dw, bws, st)
+    M.moe_expert_backward(dev(dY), dev(x), T, E, k, d, F, W1d, W2d, w2q["codes"], w2q["sf"], w2q["g"], v["topk_ids"],
+                          v["topk_w"], v["offsets"], v["row_to_token"], v["token_slot_row"], su, sh, v["h_codes"],
+                          v["h_sf"], v["h_g"], dx, dW1, dW2, dl, dw, bws, st)
     torch.cuda.synchronize()
     mp = int(host(v["offsets"])[-1])
     r = {n: host(t) for n, t in v.items() if n in ("topk_ids", "topk_w", "offsets", "row_to_token",

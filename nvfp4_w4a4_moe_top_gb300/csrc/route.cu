@@ -16,8 +16,15 @@ namespace moe {
 
 constexpr int kChunk = kRouteChunk;
 
-__device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
-  return va > vb || (va == vb && ea < eb);
+// Order-preserving map of a float (finite or -inf, with -0 taken as +0) to
+// an unsigned key: a > b as floats iff key(a) > key(b).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x7FFFFFFFu) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // One CTA per chunk of 256 tokens, 32 warps, one warp per token at a time.
@@ -54,23 +61,26 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
         }
       }
       if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, MOE_STATUS_NONFINITE_LOGITS);
+      // k rounds: the lane's best untaken logit (its ids ascend with i, so
+      // the first of equal keys has the smaller id), then the warp's largest
+      // key and, among lanes holding it, the smallest id -- two redux.sync
+      // maxima (logit descending, id ascending).
+      uint32_t key[NPL];
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) key[i] = (i * 32 + lane < E) ? order_key(v[i]) : 0u;
       uint32_t taken = 0u;
       float my_v = NEG_INF, vmax = NEG_INF;
       for (int j = 0; j < k; ++j) {
-        float bv = NEG_INF;
-        int be = 0x7FFFFFFF;
+        uint32_t bk = 0u;
+        int bi = -1;
 #pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-          const int e = i * 32 + lane;
-          if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, be)) { bv = v[i]; be = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-          const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-          if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        for (int i = 0; i < NPL; ++i)
+          if (!((taken >> i) & 1u) && (bi < 0 || key[i] > bk) && i * 32 + lane < E) { bk = key[i]; bi = i; }
+        const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bi >= 0 ? bk : 0u);
+        const uint32_t my_inv = (bi >= 0 && bk == mk) ? 0xFFFFFFFFu - (uint32_t)(bi * 32 + lane) : 0u;
+        const int be = (int)(0xFFFFFFFFu - __reduce_max_sync(0xFFFFFFFFu, my_inv));
+        if (bi >= 0 && bi * 32 + lane == be) taken |= 1u << bi;
+        const float bv = key_value(mk);
         if (lane == j) { my_id = be; my_v = bv; }
         if (j == 0) vmax = bv;
       }
@@ -405,6 +415,8 @@ int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const
 }
 
 // out[t] = BF16(sum_j FP32(slots[t][j])), j ascending; 8 columns per thread.
+// KMAX >= k: all k slot loads are issued before the ordered sum.
+template <int KMAX>
 __global__ void __launch_bounds__(256) unpermute_reduce_kernel(const uint16_t* __restrict__ slots, int T, int k,
                                                                int d, uint16_t* __restrict__ out) {
   const int c8n = d / 8;
@@ -413,20 +425,25 @@ __global__ void __launch_bounds__(256) unpermute_reduce_kernel(const uint16_t* _
   const int64_t t = idx / c8n;
   const int c8 = (int)(idx - t * c8n);
   const uint4* base = reinterpret_cast<const uint4*>(slots + t * k * (int64_t)d) + c8;
+  uint4 v[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if (j < k) v[j] = __ldg(base + (int64_t)j * c8n);
   float s[8];
   {
-    const uint4 v = __ldg(base);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t w[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) { s[2 * q] = bf16_lo(w[q]); s[2 * q + 1] = bf16_hi(w[q]); }
   }
-  for (int j = 1; j < k; ++j) {
-    const uint4 v = __ldg(base + (int64_t)j * c8n);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      s[2 * q] = __fadd_rn(s[2 * q], bf16_lo(w[q]));
-      s[2 * q + 1] = __fadd_rn(s[2 * q + 1], bf16_hi(w[q]));
+  for (int j = 1; j < KMAX; ++j) {
+    if (j < k) {
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        s[2 * q] = __fadd_rn(s[2 * q], bf16_lo(w[q]));
+        s[2 * q + 1] = __fadd_rn(s[2 * q + 1], bf16_hi(w[q]));
+      }
     }
   }
   uint4 o;
@@ -440,7 +457,11 @@ __global__ void __launch_bounds__(256) unpermute_reduce_kernel(const uint16_t* _
 int launch_unpermute_reduce(const uint16_t* slots, int T, int k, int d, uint16_t* out, cudaStream_t stream) {
   const int64_t n = (int64_t)T * (d / 8);
   if (n == 0) return 0;
-  unpermute_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(slots, T, k, d, out);
+  const unsigned grid = (unsigned)((n + 255) / 256);
+  if (k <= 4) unpermute_reduce_kernel<4><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
+  else if (k <= 8) unpermute_reduce_kernel<8><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
+  else if (k <= 16) unpermute_reduce_kernel<16><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
+  else unpermute_reduce_kernel<32><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
   return 0;
 }
 

@@ -98,7 +98,8 @@ float orc_e2m1_value(uint8_t code) {
 /* E2M1 round-to-nearest-even with saturation: the code whose value is
  * nearest to |q|, exact ties to the even code, |q| >= 6 gives 6; the sign bit
  * is the sign bit of q, so -0 and small negatives give 0x8 ([TR 5.1] Q_E2M1;
- * RNE from the execution specification; sign-of-zero reading in the design doc). */
+ * RNE from the execution specification; the sign of a zero code is a
+ * reading: the pages leave it open). */
 uint8_t orc_e2m1_encode(float q) {
     if (std::isnan(q)) return 0;  /* out of contract; the GPU flags it */
     const double a = std::fabs((double)q);

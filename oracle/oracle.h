@@ -35,8 +35,8 @@
  *              Hadamard and stochastic rounding off; sort fused with amax,
  *              padding carries the statistics, device-side offsets).
  *
- * Readings where the pages are silent are listed in the design doc and restated at
- * each function below.
+ * Where the pages are silent, the reading taken is stated at each function
+ * below.
  *
  * Parity pins: every function here is pinned by tests/test_oracle_*.py.
  */

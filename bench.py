@@ -39,7 +39,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum), keyed to the kernel source it was taken on; it is
 # reported only while that source is unchanged.  Filled from
 # profiles/*.md summaries.
-NCU_TRAFFIC = {}
+# DRAM bytes per launch of the dominant kernel, from one ncu capture of the
+# source whose hash is recorded (profiles/fc1_dram_traffic_qwen64k.md); the
+# bench reports null once the kernel source differs.
+NCU_TRAFFIC = {"fc1": {"src_sha": "6f906b8b3179b138", "bytes_per_launch": 1285574656 + 950483968,
+                       "workload": "qwen64k"}}
 
 
 def src_sha(*names):

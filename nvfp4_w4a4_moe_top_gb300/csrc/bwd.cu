@@ -482,6 +482,8 @@ __global__ void __launch_bounds__(256) bwd_logits_kernel(const float* __restrict
 }
 
 // dx[t] = sum_j dxr[token_slot_row[t][j]] (FP32, ascending j).  d % 4 == 0.
+// KMAX >= k: the k row loads of a column group are issued before the sum.
+template <int KMAX>
 __global__ void __launch_bounds__(256) bwd_dx_kernel(const float* __restrict__ dxr,
                                                      const int32_t* __restrict__ token_slot_row, int T, int k, int d,
                                                      float* __restrict__ dx) {
@@ -489,16 +491,19 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(const float* __restrict__ d
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   const int n4 = d / 4;
-  int rows[32];
+  int rows[KMAX];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) rows[j] = j < k ? __ldg(token_slot_row + t * k + j) : 0;
+  for (int j = 0; j < KMAX; ++j) rows[j] = j < k ? __ldg(token_slot_row + t * k + j) : 0;
   for (int i = lane; i < n4; i += 32) {
-    float4 s = __ldg(reinterpret_cast<const float4*>(dxr + (int64_t)rows[0] * d) + i);
+    float4 v[KMAX];
 #pragma unroll
-    for (int j = 1; j < 32; ++j) {
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) v[j] = __ldg(reinterpret_cast<const float4*>(dxr + (int64_t)rows[j] * d) + i);
+    float4 s = v[0];
+#pragma unroll
+    for (int j = 1; j < KMAX; ++j) {
       if (j < k) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(dxr + (int64_t)rows[j] * d) + i);
-        s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        s.x += v[j].x; s.y += v[j].y; s.z += v[j].z; s.w += v[j].w;
       }
     }
     reinterpret_cast<float4*>(dx + t * d)[i] = s;
@@ -521,7 +526,11 @@ int launch_bwd_logits(const float* dw, const float* topk_w, const int32_t* topk_
 
 int launch_bwd_dx(const float* dxr, const int32_t* token_slot_row, int T, int k, int d, float* dx, cudaStream_t stream) {
   if (T <= 0) return 0;
-  bwd_dx_kernel<<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(dxr, token_slot_row, T, k, d, dx);
+  const unsigned grid = (unsigned)((T + 7) / 8);
+  if (k <= 4) bwd_dx_kernel<4><<<grid, 256, 0, stream>>>(dxr, token_slot_row, T, k, d, dx);
+  else if (k <= 8) bwd_dx_kernel<8><<<grid, 256, 0, stream>>>(dxr, token_slot_row, T, k, d, dx);
+  else if (k <= 16) bwd_dx_kernel<16><<<grid, 256, 0, stream>>>(dxr, token_slot_row, T, k, d, dx);
+  else bwd_dx_kernel<32><<<grid, 256, 0, stream>>>(dxr, token_slot_row, T, k, d, dx);
   return 0;
 }
 

@@ -846,6 +846,22 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[slot]));
         if (ok) {
+          if (DW) {
+            // the warp's 32 output-gradient row segments (64 columns each)
+            // into the staging tile, 8 lanes per row, 4 rows per load
+            const unsigned long long my_src =
+                t >= 0 ? reinterpret_cast<unsigned long long>(dy_row + nt * BN + part * 64) : 0ull;
+            const int sub = lane >> 3, ch = lane & 7;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = i * 4 + sub;
+              const unsigned long long sp = __shfl_sync(0xFFFFFFFFu, my_src, rr);
+              uint4 g = make_uint4(0u, 0u, 0u, 0u);
+              if (sp) g = __ldg(reinterpret_cast<const uint4*>(sp) + ch);
+              sts128(stg + rr * FC2_STAGE_ROW + 16 * (ch ^ (rr & 7)), g.x, g.y, g.z, g.w);
+            }
+            __syncwarp();
+          }
           // scale and weight into the staging tile, then write each row's 64
           // columns as one 128-byte segment (8 lanes per row, 4 rows per
           // instruction); pad rows (t < 0) are not stored
@@ -868,12 +884,9 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
                 yv[m + 1] = y1;
               }
             }
-            if (DW) {  // the output gradient's 16 columns of this token
-              uint4 g0 = make_uint4(0u, 0u, 0u, 0u), g1 = g0;
-              if (t >= 0) {
-                g0 = __ldg(reinterpret_cast<const uint4*>(dy_row + n0));
-                g1 = __ldg(reinterpret_cast<const uint4*>(dy_row + n0) + 1);
-              }
+            if (DW) {  // this row's 16 output-gradient columns, from the staging tile
+              const uint4 g0 = lds128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf) ^ (lane & 7)));
+              const uint4 g1 = lds128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf + 1) ^ (lane & 7)));
               const uint32_t gw4[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
               for (int q = 0; q < 8; ++q) {

@@ -309,6 +309,17 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
+  // the row's loads go out first, so their latency overlaps the dependent
+  // loads that place the token's k rows
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
+  const int n8 = d / 8;  // 8-column vectors of the row
+  uint4 v[NG][4];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const int e8 = g * 128 + 4 * lane;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[g][q] = e8 < n8 ? __ldg(xr + e8 + q) : make_uint4(0u, 0u, 0u, 0u);
+  }
   int row = -1;
   if (lane < k) {
     const int64_t i = (int64_t)t * k + lane;
@@ -316,9 +327,6 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     tsr[i] = row;
     row_to_token[row] = t;
   }
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
-  const int n8 = d / 8;  // 8-column vectors of the row
-  uint4 v[NG][4];
   float a = 0.0f;
   bool fin = true;
 #pragma unroll
@@ -326,9 +334,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     const int e8 = g * 128 + 4 * lane;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      v[g][q] = make_uint4(0u, 0u, 0u, 0u);
       if (e8 < n8) {
-        v[g][q] = __ldg(xr + e8 + q);
         const uint32_t w[4] = {v[g][q].x, v[g][q].y, v[g][q].z, v[g][q].w};
 #pragma unroll
         for (int m = 0; m < 4; ++m) {

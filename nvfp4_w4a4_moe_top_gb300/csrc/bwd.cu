@@ -276,15 +276,37 @@ __device__ void mma_issuer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, B
 }
 
 // SwiGLU backward of 32 columns f0.. of one row (FP32 dh in v).
-__device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint16_t* urow, uint16_t* durow, int F,
-                                             int f0) {
-  const uint4* gp = reinterpret_cast<const uint4*>(urow + f0);
-  const uint4* up = reinterpret_cast<const uint4*>(urow + F + f0);
-  uint4* dg = reinterpret_cast<uint4*>(durow + f0);
-  uint4* du = reinterpret_cast<uint4*>(durow + F + f0);
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
+// SwiGLU backward of the 32 columns f0.. of a warp's 32 rows (FP32 dh of the
+// lane's row in v).  The rows' gate and up segments (64 bytes each) pass
+// through the warp's staging tile both ways: gate of row r at stg + 64 r,
+// up at stg + 2048 + 64 r, 16-byte chunk j at chunk j ^ ((r / 2) % 4) (eight
+// consecutive rows cover all eight 16-byte bank groups).  Loads and stores
+// go four lanes per row, eight rows per instruction, instead of one row per
+// lane.
+__device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint16_t* u_row0, uint16_t* du_row0,
+                                             int F, int f0, uint32_t stg, int lane) {
+  const int64_t ld = 2 * (int64_t)F;  // elements per row of u and du
+  const int cj = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rr = i * 8 + (lane >> 2);
+    const uint32_t off = rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4);
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + f0) + cj);
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + F + f0) + cj);
+    sts128(stg + off, g.x, g.y, g.z, g.w);
+    sts128(stg + 2048 + off, x.x, x.y, x.z, x.w);
+  }
+  __syncwarp();
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 g4 = __ldg(gp + q), u4 = __ldg(up + q);
+    const uint32_t off = lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
+    const uint4 g4 = lds128(stg + off), u4 = lds128(stg + 2048 + off);
     const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
     uint32_t og[4], ou[4];
 #pragma unroll
@@ -302,9 +324,18 @@ __device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint
       og[p] = pack2_rn(rg[0], rg[1]);
       ou[p] = pack2_rn(ru[0], ru[1]);
     }
-    dg[q] = make_uint4(og[0], og[1], og[2], og[3]);
-    du[q] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+    sts128(stg + off, og[0], og[1], og[2], og[3]);
+    sts128(stg + 2048 + off, ou[0], ou[1], ou[2], ou[3]);
   }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rr = i * 8 + (lane >> 2);
+    const uint32_t off = rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4);
+    reinterpret_cast<uint4*>(du_row0 + rr * ld + f0)[cj] = lds128(stg + off);
+    reinterpret_cast<uint4*>(du_row0 + rr * ld + F + f0)[cj] = lds128(stg + 2048 + off);
+  }
+  __syncwarp();
 }
 
 // FP32 outputs leave through a per-warp staging tile (32 rows x 128 bytes,
@@ -337,8 +368,8 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
       uint32_t v[32];
       tld32(tbase + c, v);
       if (a.mode == BWD_DGRAD_SWIGLU) {
-        const int64_t row = (int64_t)U.mt * BM + rl;
-        swiglu_bwd32(v, a.u + row * 2 * a.F, a.du + row * 2 * a.F, a.F, c0 + c);
+        const int64_t row0 = (int64_t)U.mt * BM + q4 * 32;
+        swiglu_bwd32(v, a.u + row0 * 2 * a.F, a.du + row0 * 2 * a.F, a.F, c0 + c, stg, lane);
       } else {
         const int orow0 = a.mode == BWD_WGRAD ? U.e * a.Mo + U.mt * BM + q4 * 32 : U.mt * BM + q4 * 32;
         if (lane == 0 && pending) bulk_wait_read0();

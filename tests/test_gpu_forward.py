@@ -69,10 +69,15 @@ def layer_of(name):
         return synth.custom(T=200, d=128, E=1, k=1, d_ff=128, seed=3)
     if name == "all_experts":
         return synth.custom(T=64, d=256, E=6, k=6, d_ff=256, seed=8)
+    if name == "max_experts":  # E and k at their limits: ~2 rows per expert, mostly pad rows
+        return synth.custom(T=64, d=128, E=1024, k=32, d_ff=128, seed=13)
+    if name == "max_width":  # d and d_ff at their limits: A streams through the stages in both GEMMs
+        return synth.custom(T=160, d=4096, E=2, k=1, d_ff=4096, seed=14)
     return synth.layer(name)
 
 
-@pytest.mark.parametrize("name", ["tiny", "small", "ragged", "k1", "single_expert", "all_experts"])
+@pytest.mark.parametrize("name", ["tiny", "small", "ragged", "k1", "single_expert", "all_experts", "max_experts",
+                                  "max_width"])
 def test_forward_against_oracle(orc, name):
     lay = layer_of(name)
     x, lg, W1, W2 = lay.x(), lay.logits(), lay.w1(), lay.w2()

@@ -201,3 +201,34 @@ def test_full_size_sampled(orc):
     assert e_dx <= 3e-4
     for a1, a2 in errs:
         assert a1 <= 3e-4 and a2 <= 1e-5
+
+
+def test_training_forward_output_equals_the_forward(orc):
+    """moe_expert_forward_train returns what moe_expert_forward returns, bit
+    for bit (the saves do not change the arithmetic)."""
+    import torch
+    from gpu_util import dev, host
+    lay = layer_of("ragged")
+    x, lg, W1, W2, dY = lay.x(), lay.logits(), lay.w1(), lay.w2(), lay.grad_out()
+    r = gpu_train_step(lay, x, lg, W1, W2, dY)
+    T, E, k, d, F = lay.T, lay.E, lay.k, lay.d, lay.d_ff
+    w1q, w2q = M.quantize_weights(dev(W1)), M.quantize_weights(dev(W2))
+    out = torch.empty((T, d), dtype=torch.int16, device="cuda")
+    M.moe_expert_forward(dev(x), dev(lg), T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"], w2q["sf"],
+                         w2q["g"], out, M.forward_workspace(T, E, k, d, F))
+    torch.cuda.synchronize()
+    assert np.array_equal(r["out"], host(out, np.uint16))
+
+
+def test_backward_of_an_empty_batch_zeroes_the_weight_gradients(orc):
+    import torch
+    lay = layer_of("tiny")
+    E, k, d, F = lay.E, lay.k, lay.d, lay.d_ff
+    W1 = torch.ones((E, 2 * F, d), dtype=torch.int16, device="cuda")
+    W2 = torch.ones((E, d, F), dtype=torch.int16, device="cuda")
+    dW1 = torch.full((E, 2 * F, d), float("nan"), dtype=torch.float32, device="cuda")
+    dW2 = torch.full((E, d, F), float("nan"), dtype=torch.float32, device="cuda")
+    M.moe_expert_backward(None, None, 0, E, k, d, F, W1, W2, None, None, None, None, None, None, None, None, None,
+                          None, None, None, None, None, dW1, dW2, None, None, None)
+    torch.cuda.synchronize()
+    assert not dW1.any() and not dW2.any()

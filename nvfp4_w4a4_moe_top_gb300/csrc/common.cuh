@@ -86,6 +86,39 @@ __device__ __forceinline__ bool bf16x2_finite(uint32_t p) {
   return ((p & 0x7F80u) != 0x7F80u) && ((p & 0x7F800000u) != 0x7F800000u);
 }
 
+// Largest magnitude among 16 BF16 values (two uint4), as the BF16 bit
+// pattern with the sign cleared.  For finite values and +inf the integer
+// order of these patterns is the order of the magnitudes, and any NaN
+// compares above +inf (0x7F80), so a result >= 0x7F80 means a non-finite
+// value is present.
+__device__ __forceinline__ uint32_t absmax_bits16(const uint4 p0, const uint4 p1) {
+  uint32_t m = __vmaxu2(p0.x & 0x7FFF7FFFu, p0.y & 0x7FFF7FFFu);
+  m = __vmaxu2(m, __vmaxu2(p0.z & 0x7FFF7FFFu, p0.w & 0x7FFF7FFFu));
+  m = __vmaxu2(m, __vmaxu2(p1.x & 0x7FFF7FFFu, p1.y & 0x7FFF7FFFu));
+  m = __vmaxu2(m, __vmaxu2(p1.z & 0x7FFF7FFFu, p1.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// Largest magnitude among a lane's BF16 values with NaNs left out (the
+// maximum fmaxf would give), as magnitude bits.
+template <int NG>
+__device__ __forceinline__ uint32_t absmax_bits_no_nan(const uint4 (&v)[NG][4]) {
+  uint32_t fm = 0;
+#pragma unroll
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w[4] = {v[g][q].x, v[g][q].y, v[g][q].z, v[g][q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = w[i] & 0x7FFFu, hi = (w[i] >> 16) & 0x7FFFu;
+        if (lo <= 0x7F80u) fm = max(fm, lo);
+        if (hi <= 0x7F80u) fm = max(fm, hi);
+      }
+    }
+  return fm;
+}
+
 // Eight FP32 -> eight E2M1 codes with the hardware conversion (nearest
 // even, saturating; element 0 in the low nibble).  Its equality with
 // e2m1_encode over every float is part of the codec parity test.
@@ -102,6 +135,40 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
   return r;
 }
 
+// Two FP32 values in one 64-bit register (first argument in the low half),
+// the operand form of the packed f32x2 arithmetic.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Element-wise product of two FP32 pairs, each rounded to nearest even: the
+// same two results as two __fmul_rn, in one instruction.
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// e2m1x8 of four FP32 pairs (pair i holds elements 2i, 2i+1).
+__device__ __forceinline__ uint32_t e2m1x8_pairs(const uint64_t (&p)[4]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .f32 x0, x1, x2, x3, x4, x5, x6, x7;\n\t"
+      "mov.b64 {x0, x1}, %1;\n\t"
+      "mov.b64 {x2, x3}, %2;\n\t"
+      "mov.b64 {x4, x5}, %3;\n\t"
+      "mov.b64 {x6, x7}, %4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, x1, x0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, x3, x2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, x5, x4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, x7, x6;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "l"(p[0]), "l"(p[1]), "l"(p[2]), "l"(p[3]));
+  return r;
+}
+
 // Codes of 8 BF16 values (4 packed words) for block scale S > 0:
 // c = Q_E2M1(RN(v / S)).  With R = RN(1/S), the products v*RN(R*(1-2^-21))
 // and v*RN(R*(1+2^-21)) bracket RN(v/S): each is within 3*2^-24 (relative)
@@ -110,23 +177,23 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
 // codes those are the codes of RN(v/S).  Otherwise (a quotient within about
 // 2^-21 of a rounding boundary, e.g. an exact tie) the codes are recomputed
 // from the correctly rounded division.  Quotients far below 0.25 encode to
-// zero on both sides, so subnormal products do not break the argument.
+// zero on both sides, so subnormal products do not break the argument.  The
+// bracket products go two at a time through the packed f32x2 multiply.
 __device__ __forceinline__ uint32_t e2m1_codes8(const uint32_t (&w)[4], float S) {
   if (S >= 7.52316384526264e-37f) {  // 2^-120: R and the products stay finite
     const float R = __frcp_rn(S);
     const float Rl = __fmul_rn(R, 0.99999952316284180f);  // 1 - 2^-21
     const float Rh = __fmul_rn(R, 1.00000047683715820f);  // 1 + 2^-21
-    float l[8], h[8];
+    const uint64_t rl = f32x2_pack(Rl, Rl), rh = f32x2_pack(Rh, Rh);
+    uint64_t l[4], h[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float v0 = bf16_lo(w[i]), v1 = bf16_hi(w[i]);
-      l[2 * i] = __fmul_rn(v0, Rl);
-      l[2 * i + 1] = __fmul_rn(v1, Rl);
-      h[2 * i] = __fmul_rn(v0, Rh);
-      h[2 * i + 1] = __fmul_rn(v1, Rh);
+      const uint64_t x = f32x2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
+      l[i] = mul_f32x2(x, rl);
+      h[i] = mul_f32x2(x, rh);
     }
-    const uint32_t cl = e2m1x8(l);
-    if (cl == e2m1x8(h)) return cl;
+    const uint32_t cl = e2m1x8_pairs(l);
+    if (cl == e2m1x8_pairs(h)) return cl;
   }
   float q[8];
 #pragma unroll
@@ -135,30 +202,6 @@ __device__ __forceinline__ uint32_t e2m1_codes8(const uint32_t (&w)[4], float S)
     q[2 * i + 1] = __fdiv_rn(bf16_hi(w[i]), S);
   }
   return e2m1x8(q);
-}
-
-// ---------------------------------------------------------------------------
-// Quantise 8 consecutive BF16 values (one uint4) that form half of a
-// 16-element block whose other half sits in lane (lane ^ 1).  Returns the 8
-// packed E2M1 codes (4 bytes, even element in the low nibble) and the block
-// scale byte.  g and den = 6*g are the row's outer scale and its divisor.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t quant_half_block(const uint4 v, float g, float den,
-                                                     uint32_t* sb_out) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
-  float a = __uint_as_float(__vmaxu2(m, m >> 16) << 16);
-  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-  uint32_t sb = 0, packed = 0;
-  if (g != 0.0f) {
-    sb = e4m3_encode(__fdiv_rn(a, den));
-    const float S = __fmul_rn(g, e4m3_decode(sb));
-    if (S != 0.0f) packed = e2m1_codes8(w, S);
-  }
-  *sb_out = sb;
-  return packed;
 }
 
 // ---------------------------------------------------------------------------

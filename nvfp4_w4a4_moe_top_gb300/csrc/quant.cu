@@ -10,12 +10,15 @@
 
 namespace moe {
 
-// Byte offset of the 4-byte word holding block scales (row, 4*c4 .. 4*c4+3).
-__device__ __forceinline__ int64_t sf_word_offset(int64_t row, int c4, int kgroups) {
-  return ((row >> 7) * kgroups + c4) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
-}
-
-template <int MAXCH>
+// One warp per destination row.  Lane L holds, for each group of 1024
+// columns, the 32 consecutive columns from 32*L: two whole 16-element blocks,
+// so every block's scale is computed once, its codes leave as one 16-byte
+// store and lanes L, L ^ 1 form one 32-bit scale word.  The blocks' largest
+// magnitudes, taken as BF16 bit patterns, give the block amax, the row amax
+// and the non-finite check at once.  A row holding a NaN takes its amax over
+// the other values, as fmaxf does; its codes are unspecified and the status
+// bit reports it.
+template <int NG>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(
     const uint16_t* __restrict__ src, int64_t src_rows, int K, const int32_t* __restrict__ row_map,
     const float* __restrict__ amax, int64_t amax_rows, int64_t dst_rows, uint8_t* __restrict__ codes,
@@ -24,75 +27,87 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= dst_rows) return;
   const int kg = K / 64;
+  const int n8 = K / 8;  // 8-column vectors of the row
   int64_t s = row_map ? (int64_t)row_map[r] : r;
   if (s >= src_rows) {  // invalid map entry: write a zero row and flag it
     if (lane == 0) set_status(status, MOE_STATUS_BAD_ROUTING);
     s = -1;
   }
-  uint8_t* crow = codes + r * (K / 2);
+  uint4* crow = reinterpret_cast<uint4*>(codes + r * (K / 2));
+  const int64_t sf_row = (r >> 7) * kg * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
   if (s < 0) {
-    for (int i = lane; i < K / 8; i += 32) reinterpret_cast<uint32_t*>(crow)[i] = 0u;
-    for (int c4 = lane; c4 < kg; c4 += 32) *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, c4, kg)) = 0u;
+    for (int i = lane; i < K / 32; i += 32) crow[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int c4 = lane; c4 < kg; c4 += 32) *reinterpret_cast<uint32_t*>(sf + sf_row + c4 * 512) = 0u;
     if (lane == 0) gout[r] = 0.0f;
     return;
   }
   const uint4* srow = reinterpret_cast<const uint4*>(src + s * (int64_t)K);
-  const int n8 = K / 8;  // 8-element groups in the row
-  uint4 v[MAXCH];
-  float a = 0.0f;
-  bool fin = true;
+  uint4 v[NG][4];
 #pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    const int e8 = i * 32 + lane;
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int g = 0; g < NG; ++g) {
+    const int e8 = g * 128 + 4 * lane;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[g][q] = e8 < n8 ? __ldg(srow + e8 + q) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  uint32_t bm[NG][2];  // magnitude bits of each block's largest |x|
+  uint32_t lm = 0;
+#pragma unroll
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      bm[g][b] = absmax_bits16(v[g][2 * b], v[g][2 * b + 1]);
+      lm = max(lm, bm[g][b]);
+    }
+  const uint32_t rm = __reduce_max_sync(0xFFFFFFFFu, lm);
+  if (rm >= 0x7F80u && lane == 0) set_status(status, nonfinite_bit);
+  float a;
+  if (amax)
+    a = amax[s / amax_rows];
+  else  // a NaN in the row (warp-uniform, rare): the largest other magnitude
+    a = __uint_as_float((rm <= 0x7F80u ? rm : __reduce_max_sync(0xFFFFFFFFu, absmax_bits_no_nan(v))) << 16);
+  const float gs = __fdiv_rn(a, 2688.0f);
+  const float den = __fmul_rn(6.0f, gs);
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const int e8 = g * 128 + 4 * lane;
+    if (g * 128 >= n8) break;  // warp-uniform
+    uint32_t c[4] = {0u, 0u, 0u, 0u}, sb2 = 0u;
+    if (e8 < n8 && gs != 0.0f) {
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {  // the lane's two blocks of 16
+        const uint4 p0 = v[g][2 * b], p1 = v[g][2 * b + 1];
+        const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w}, w1[4] = {p1.x, p1.y, p1.z, p1.w};
+        const uint32_t sb = e4m3_encode(__fdiv_rn(__uint_as_float(bm[g][b] << 16), den));
+        const float S = __fmul_rn(gs, e4m3_decode(sb));
+        if (S != 0.0f) {
+          c[2 * b] = e2m1_codes8(w0, S);
+          c[2 * b + 1] = e2m1_codes8(w1, S);
+        }
+        sb2 |= sb << (8 * b);
+      }
+    }
+    const uint32_t sfw = sb2 | (__shfl_xor_sync(0xFFFFFFFFu, sb2, 1) << 16);
     if (e8 < n8) {
-      v[i] = __ldg(srow + e8);
-      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        fin = fin && bf16x2_finite(w[q]);
-        a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
-      }
+      crow[e8 >> 2] = make_uint4(c[0], c[1], c[2], c[3]);
+      if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(sf + sf_row + (int64_t)(e8 >> 3) * 512) = sfw;
     }
   }
-  if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, nonfinite_bit);
-  a = amax ? amax[s / amax_rows] : warp_max(a);
-  const float g = __fdiv_rn(a, 2688.0f);
-  const float den = __fmul_rn(6.0f, g);
-#pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    if (i * 32 < n8) {  // warp-uniform
-      const int e8 = i * 32 + lane;
-      uint32_t sb;
-      const uint32_t packed = quant_half_block(v[i], g, den, &sb);
-      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
-      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
-      if (e8 < n8) {
-        reinterpret_cast<uint32_t*>(crow)[e8] = packed;
-        if ((lane & 7) == 0)
-          *reinterpret_cast<uint32_t*>(sf + sf_word_offset(r, e8 >> 3, kg)) = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-      }
-    }
-  }
-  if (lane == 0) gout[r] = g;
+  if (lane == 0) gout[r] = gs;
 }
 
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,
                          const float* amax, int64_t amax_rows, int64_t dst_rows, uint8_t* codes, uint8_t* sf,
                          float* g, int* status, int nonfinite_bit, cudaStream_t stream) {
   if (dst_rows <= 0) return 0;
-  const int nch = (K / 8 + 31) / 32;
+  const int ng = (K + 1023) / 1024;
   const dim3 grid((unsigned)((dst_rows + 7) / 8));
-  if (nch <= 4)
-    quantize_rows_kernel<4><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes, sf,
-                                                      g, status, nonfinite_bit);
-  else if (nch <= 8)
-    quantize_rows_kernel<8><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes, sf,
-                                                      g, status, nonfinite_bit);
-  else
-    quantize_rows_kernel<16><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes,
-                                                       sf, g, status, nonfinite_bit);
+#define MOE_QR(N)                                                                                            \
+  quantize_rows_kernel<N><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes, \
+                                                    sf, g, status, nonfinite_bit)
+  if (ng <= 1) MOE_QR(1);
+  else if (ng <= 2) MOE_QR(2);
+  else MOE_QR(4);
+#undef MOE_QR
   return 0;
 }
 

@@ -327,25 +327,20 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     tsr[i] = row;
     row_to_token[row] = t;
   }
-  float a = 0.0f;
-  bool fin = true;
+  uint32_t bm[NG][2];  // magnitude bits of each block's largest |x|
+  uint32_t lm = 0;
 #pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    const int e8 = g * 128 + 4 * lane;
+  for (int g = 0; g < NG; ++g)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (e8 < n8) {
-        const uint32_t w[4] = {v[g][q].x, v[g][q].y, v[g][q].z, v[g][q].w};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          fin = fin && bf16x2_finite(w[m]);
-          a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[m])), fabsf(bf16_hi(w[m]))));
-        }
-      }
+    for (int b = 0; b < 2; ++b) {
+      bm[g][b] = absmax_bits16(v[g][2 * b], v[g][2 * b + 1]);
+      lm = max(lm, bm[g][b]);
     }
-  }
-  if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, MOE_STATUS_NONFINITE_X);
-  a = warp_max(a);
+  const uint32_t rm = __reduce_max_sync(0xFFFFFFFFu, lm);
+  if (rm >= 0x7F80u && lane == 0) set_status(status, MOE_STATUS_NONFINITE_X);
+  // a NaN in the row (warp-uniform, rare): the largest other magnitude
+  const float a =
+      __uint_as_float((rm <= 0x7F80u ? rm : __reduce_max_sync(0xFFFFFFFFu, absmax_bits_no_nan(v))) << 16);
   if (lane == 0 && amax_tok) amax_tok[t] = a;
   const float gs = __fdiv_rn(a, 2688.0f);
   const float den = __fmul_rn(6.0f, gs);
@@ -359,10 +354,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     for (int b = 0; b < 2; ++b) {  // the lane's two blocks of 16
       const uint4 p0 = v[g][2 * b], p1 = v[g][2 * b + 1];
       const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w}, w1[4] = {p1.x, p1.y, p1.z, p1.w};
-      uint32_t m = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) m = __vmaxu2(__vmaxu2(m, w0[i] & 0x7FFF7FFFu), w1[i] & 0x7FFF7FFFu);
-      const float ab = __uint_as_float(__vmaxu2(m, m >> 16) << 16);
+      const float ab = __uint_as_float(bm[g][b] << 16);
       uint32_t sb = 0;
       if (gs != 0.0f) {
         sb = e4m3_encode(__fdiv_rn(ab, den));

@@ -43,6 +43,8 @@
 // Every wait is bounded (a few seconds of wall clock); on expiry the kernel
 // raises MOE_STATUS_TIMEOUT, drains its own copies and MMAs, frees tensor
 // memory and returns.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -55,6 +57,17 @@ constexpr int A_SLICE = BM * BK_BYTES;                 // 16 KB
 constexpr int B_BYTES = BN * BK_BYTES;                 // 16 KB
 constexpr int SF_STAGE = 4 * 512;                      // 2 KB per operand
 constexpr int B_STAGE = B_BYTES + 2 * SF_STAGE;        // 20 KB: B, SFB, SFA
+// CTA pairs (FC1): one MMA covers 256 rows (128 per CTA) and 256 columns,
+// a chunk's gate (columns 0-127, rank 0's B tile) and up (128-255, rank 1's
+// B tile) together, into one 256-column accumulator.  A stage holds the
+// CTA's B tile, the scale tiles of both B tiles and the CTA's A scales; the
+// scale buffers in tensor memory form a ring of their own, decoupled from
+// the stages.
+constexpr int PAIR_STAGE = B_BYTES + 3 * SF_STAGE;     // 22 KB: B, SFB gate, SFB up, SFA
+constexpr int PAIR_RINGS = 3, PAIR_LOG2_STAGES = 0;    // 3 rings x 1 stage
+constexpr int PAIR_SFBUF = 4;                          // tensor-memory scale buffers
+constexpr int PAIR_ACC_COLS = 2 * BN;                  // the 256-column accumulator
+constexpr int PAIR_SF_COLS = 64;                       // per buffer: [A scales 16 | B scales 32 | unused 16]
 constexpr int MAX_A_SLOTS = 16;
 constexpr int MAX_STAGES = 8;                          // over all rings (one TMEM scale buffer each)
 constexpr int NPROD_WARPS = 3;                         // producer warps: warp p feeds rings r with r % 3 == p
@@ -89,6 +102,11 @@ constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA
 // Instruction descriptor: E2M1 x E2M1, UE4M3 scales, both operands K-major,
 // N = 128 (bits 17-22 hold N/8), M = 128 (bits 24-28 hold M/16).
 constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// The same for a CTA pair: M = 256 (rows 0-127 from the issuing CTA's A,
+// 128-255 from the peer's), N = 256 (columns 0-127 from the issuing CTA's B
+// tile, 128-255 from the peer's).
+constexpr uint32_t IDESC_PAIR =
+    (1u << 7) | (1u << 10) | ((uint32_t)PAIR_ACC_COLS >> 3 << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 
 struct Tail {
   uint64_t a_full[MAX_A_SLOTS];
@@ -96,6 +114,7 @@ struct Tail {
   uint64_t b_full[MAX_STAGES];
   uint64_t b_empty[MAX_STAGES];
   uint64_t sf_full[MAX_STAGES];
+  uint64_t sf_empty[PAIR_SFBUF];  // CTA pairs: scale buffer free again
   uint64_t tfull[NSLOT_MAX];
   uint64_t tempty[NSLOT_MAX];
   uint64_t done;
@@ -141,6 +160,55 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// CTA pairs: the commit arrives on the barrier at the same offset in both
+// CTAs of the cluster.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(IDESC_PAIR), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on a barrier of another CTA of the cluster (or this one, by its
+// cluster address).  What the arrival orders is tensor-memory and tensor-core
+// work, which the tcgen05 fences around the wait and the arrival order; the
+// release/acquire forms at cluster scope cost FC1 a millisecond on the 64k
+// layer and are not needed for it.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -162,6 +230,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
@@ -199,7 +277,14 @@ __device__ __forceinline__ int expert_of(const int32_t* off, int E, int mt) {
 }
 
 struct Geometry {
-  int num_mt;      // 128-row units
+  int num_mt;      // 128-row tiles
+  bool pair;       // CTA pairs: units of two tiles, half of B per CTA
+  uint32_t rank;   // rank in the pair (0 issues the MMAs)
+  int cluster, nclusters;
+  int b_bytes;     // B bytes per stage
+  int sfb_tiles;   // B scale tiles per stage: 1, or 2 in a pair (gate and up)
+  int acc_cols;    // TMEM columns per accumulator: BN, or PAIR_ACC_COLS in a pair
+  int sf_cols;     // TMEM columns per scale buffer: SF_COLS, or PAIR_SF_COLS in a pair
   int items;       // accumulator tiles per unit
   int nk;          // k-steps of 256 elements
   int kgroups;     // K / 64 (block-scale 4-column groups)
@@ -209,8 +294,19 @@ struct Geometry {
   int nslot;       // accumulators (128 TMEM columns each)
   bool resident;   // A slices loaded once per unit into their own slots
   __device__ uint32_t b_off() const { return resident ? 0u : (uint32_t)A_SLICE; }
-  // first TMEM column of the scale buffers (one per stage, after the accumulators)
-  __device__ uint32_t sf_col() const { return (uint32_t)(nslot * BN); }
+  // first TMEM column of the scale buffers (after the accumulators; one per
+  // stage, or a ring of PAIR_SFBUF in a pair)
+  __device__ uint32_t sf_col() const { return (uint32_t)(nslot * acc_cols); }
+  // scale buffer of CTA-local k-step kc (stage slot `slot`) and its use count
+  __device__ void sfbuf_of(uint32_t kc, uint32_t slot, uint32_t use, uint32_t& buf, uint32_t& buse) const {
+    if (pair) {
+      buf = kc & (PAIR_SFBUF - 1);
+      buse = kc / PAIR_SFBUF;
+    } else {
+      buf = slot;
+      buse = use;
+    }
+  }
   // ring of CTA-local k-step kc and its position in the ring
   __device__ void ring_of(uint32_t kc, uint32_t& r, uint32_t& pos) const {
     if (rings == 4) {
@@ -229,6 +325,45 @@ struct Geometry {
     use = pos >> log2_stages;
   }
 };
+
+// The CTA's work units, in order (index iu = 0, 1, ...).  Single CTAs: a
+// unit is one 128-row tile; CTA i takes tiles i, i + gridDim.x, ...  CTA
+// pairs: a unit is two consecutive 128-row tiles of one expert; cluster c
+// takes pair units c, c + clusters, ... (numbered expert by expert, an
+// expert with n tiles owning ceil(n / 2)), and rank r of the pair owns the
+// unit's tile r.  When an expert's tile count is odd its last unit has no
+// second tile: rank 1 then repeats tile 0's operands (the MMA needs its half
+// of B all the same) and writes nothing (`ghost`).  The cursor walks the
+// experts forward, so each call continues where the previous one stopped.
+struct UnitCursor {
+  int e = 0, p0 = 0;  // expert under the cursor, its first pair-unit index
+};
+__device__ __forceinline__ bool unit_at(const Geometry& G, const int32_t* off, int E, int iu, UnitCursor& cur,
+                                        int& tile, int& e, bool& ghost) {
+  if (!G.pair) {
+    const int u = (int)blockIdx.x + iu * (int)gridDim.x;
+    if (u >= G.num_mt) return false;
+    tile = u;
+    e = expert_of(off, E, u);
+    ghost = false;
+    return true;
+  }
+  const int p = G.cluster + iu * G.nclusters;
+  while (cur.e < E) {
+    const int t0 = __ldg(off + cur.e) / BM, t1 = __ldg(off + cur.e + 1) / BM;
+    const int np = (t1 - t0 + 1) >> 1;
+    if (p < cur.p0 + np) {
+      e = cur.e;
+      tile = t0 + 2 * (p - cur.p0) + (int)G.rank;
+      ghost = tile >= t1;
+      if (ghost) tile -= 1;
+      return true;
+    }
+    cur.p0 += np;
+    ++cur.e;
+  }
+  return false;
+}
 
 // Weight row of item q of a unit of expert e.
 struct ItemRows {
@@ -285,13 +420,19 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
   for (int i = 0; i < MAX_STAGES; ++i) last_stage_use[i] = 0xFFFFFFFFu;
   for (int i = 0; i < MAX_A_SLOTS; ++i) last_a_use[i] = 0xFFFFFFFFu;
   bool aborted = false;
-  for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
-    const int e = expert_of(off, E, u);
-    const uint32_t unit_use = (uint32_t)((u - (int)blockIdx.x) / (int)gridDim.x);
+  UnitCursor cur;
+  int u, e;
+  bool ghost;
+  for (int iu = 0; !aborted && unit_at(G, off, E, iu, cur, u, e, ghost); ++iu) {
+    const uint32_t unit_use = (uint32_t)iu;
     const int64_t sfa_row = (int64_t)u * G.kgroups;
     for (int q = 0; q < G.items && !aborted; ++q) {
-      const int br = rows(e, q);
+      // a pair's item is chunk q: rank 0 loads its gate rows, rank 1 its up
+      // rows, and both load the scales of both
+      const int br = G.pair ? rows(e, 2 * q) : rows(e, q);
+      const int b_row = G.pair ? rows(e, 2 * q + (int)G.rank) : br;
       const int64_t sfb_row = (int64_t)(br / BM) * G.kgroups;
+      const int64_t sfb_row2 = G.pair ? (int64_t)(rows(e, 2 * q + 1) / BM) * G.kgroups : 0;
       for (int ks = 0; ks < G.nk; ++ks, ++kc) {
         uint32_t ring, pos;
         G.ring_of(kc, ring, pos);
@@ -316,13 +457,14 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
           load_a_slice<GATHER>(a_base + ks * A_SLICE, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, ab, lane);
           last_a_use[ks] = unit_use;
         }
-        if (lane == 0) mbar_arrive_expect_tx(fb, B_BYTES + 2 * nsf * 512 + b_off);
+        if (lane == 0) mbar_arrive_expect_tx(fb, G.b_bytes + (G.sfb_tiles + 1) * nsf * 512 + b_off);
         if (GATHER) __syncwarp();
         if (!G.resident) load_a_slice<GATHER>(st, tmap_a, ks * BK_BYTES, u, a_rows, zero_row, fb, lane);
         if (lane == 0) {
-          tma_load_2d(st + b_off, tmap_b, ks * BK_BYTES, br, fb);
-          bulk_load(st + b_off + B_BYTES, b_sf + (sfb_row + 4 * ks) * 512, nsf * 512, fb);
-          bulk_load(st + b_off + B_BYTES + SF_STAGE, a_sf + (sfa_row + 4 * ks) * 512, nsf * 512, fb);
+          tma_load_2d(st + b_off, tmap_b, ks * BK_BYTES, b_row, fb);
+          bulk_load(st + b_off + G.b_bytes, b_sf + (sfb_row + 4 * ks) * 512, nsf * 512, fb);
+          if (G.pair) bulk_load(st + b_off + G.b_bytes + SF_STAGE, b_sf + (sfb_row2 + 4 * ks) * 512, nsf * 512, fb);
+          bulk_load(st + b_off + G.b_bytes + G.sfb_tiles * SF_STAGE, a_sf + (sfa_row + 4 * ks) * 512, nsf * 512, fb);
         }
         last_stage_use[slot] = use;
       }
@@ -352,100 +494,156 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
 //     a 32x128b.warpx4 copy of the tile would place them in every quadrant;
 //   - the A scales on the diagonal only: column A0 + 4i + qd holds the four
 //     scale bytes of row 32*qd + l in A-scale tile i (bytes 16*l + 4*qd).
-// The stage's buffer is rewritten only after its next use has landed, which
-// the producer issues only after the MMAs of the previous use completed.
+// Single CTAs: the stage's buffer is rewritten only after its next use has
+// landed, which the producer issues only after the MMAs of the previous use
+// completed.  CTA pairs: the buffers form a ring of their own, and a buffer
+// is rewritten once the commit of its previous MMAs (sf_empty, arriving in
+// both CTAs) says they completed.
 // The writers also wait for the resident A slice of the k-step (first item of
 // a unit), so the MMA thread waits on sf_full alone: its completion implies
-// that the stage's operands and the A slice have landed.
-__device__ void sf_writer_loop(int qd, const Geometry& G, uint32_t ring_base, Tail* tl, uint32_t tmem,
-                               volatile int* abort_flag, int* status) {
+// that the stage's operands and the A slice have landed (in a pair, in both
+// CTAs: all eight writer warps arrive on rank 0's barrier).
+__device__ void sf_writer_loop(int qd, const Geometry& G, const int32_t* off, int E, uint32_t ring_base, Tail* tl,
+                               uint32_t tmem, volatile int* abort_flag, int* status) {
   const int lane = threadIdx.x & 31;
   const uint32_t b_off = G.b_off();
   const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16);
   uint32_t kc = 0;
   bool aborted = false;
-  for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
-    const uint32_t unit_use = (uint32_t)((u - (int)blockIdx.x) / (int)gridDim.x);
+  UnitCursor cur;
+  int u, e;
+  bool ghost;
+  for (int iu = 0; !aborted && unit_at(G, off, E, iu, cur, u, e, ghost); ++iu) {
+    const uint32_t unit_use = (uint32_t)iu;
     for (int q = 0; q < G.items && !aborted; ++q) {
       for (int ks = 0; ks < G.nk; ++ks, ++kc) {
-        uint32_t slot, use;
+        uint32_t slot, use, buf, buse;
         G.slot_of(kc, slot, use);
+        G.sfbuf_of(kc, slot, use, buf, buse);
         bool ok = warp_wait(smem_u32(&tl->b_full[slot]), use & 1u, abort_flag, status);
         if (ok && G.resident && q == 0) ok = warp_wait(smem_u32(&tl->a_full[ks]), unit_use & 1u, abort_flag, status);
+        if (ok && G.pair) ok = warp_wait(smem_u32(&tl->sf_empty[buf]), (buse & 1u) ^ 1u, abort_flag, status);
         if (!ok) { aborted = true; break; }
         tc_fence_after();
         const int nsf = min(4, G.kgroups - 4 * ks);
-        const uint32_t sfb_s = ring_base + slot * G.stage_bytes + b_off + B_BYTES;
-        const uint32_t sfa_s = sfb_s + SF_STAGE;
-        uint32_t wb[16], wa[4];
+        const uint32_t sfb_s = ring_base + slot * G.stage_bytes + b_off + G.b_bytes;
+        const uint32_t sfa_s = sfb_s + G.sfb_tiles * SF_STAGE;
+        const uint32_t col = tq + G.sf_col() + buf * G.sf_cols;
+        uint32_t wa[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          wa[i] = 0u;
-          if (i < nsf) {
-            v = lds128(sfb_s + 512 * i + 16 * lane);
-            wa[i] = lds32(sfa_s + 512 * i + 16 * lane + 4 * qd);
+        for (int i = 0; i < 4; ++i) wa[i] = i < nsf ? lds32(sfa_s + 512 * i + 16 * lane + 4 * qd) : 0u;
+        if (G.pair) {
+          // N = 256: the B scales of MMA i take 8 columns, B rows 0-127 (the
+          // gate tile) in the first 4 and rows 128-255 (the up tile) in the next
+          uint32_t wb[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const uint4 v = i < nsf ? lds128(sfb_s + t * SF_STAGE + 512 * i + 16 * lane) : make_uint4(0u, 0u, 0u, 0u);
+              wb[8 * i + 4 * t] = v.x; wb[8 * i + 4 * t + 1] = v.y; wb[8 * i + 4 * t + 2] = v.z; wb[8 * i + 4 * t + 3] = v.w;
+            }
+          tmem_st32(col + 16, wb);
+        } else {
+          uint32_t wb[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = i < nsf ? lds128(sfb_s + 512 * i + 16 * lane) : make_uint4(0u, 0u, 0u, 0u);
+            wb[4 * i] = v.x; wb[4 * i + 1] = v.y; wb[4 * i + 2] = v.z; wb[4 * i + 3] = v.w;
           }
-          wb[4 * i] = v.x; wb[4 * i + 1] = v.y; wb[4 * i + 2] = v.z; wb[4 * i + 3] = v.w;
+          tmem_st16(col + 16, wb);
         }
-        const uint32_t col = tq + G.sf_col() + slot * SF_COLS;
-        tmem_st16(col + 16, wb);
 #pragma unroll
         for (int i = 0; i < 4; ++i) tmem_st1(col + 4 * i + qd, wa[i]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tl->sf_full[slot]));
+        if (lane == 0) {
+          if (G.pair)
+            mbar_arrive_cluster(map_to_rank(smem_u32(&tl->sf_full[buf]), 0));
+          else
+            mbar_arrive(smem_u32(&tl->sf_full[buf]));
+        }
       }
     }
   }
 }
 
-__device__ void mma_loop(const Geometry& G, uint32_t a_base, uint32_t ring_base, Tail* tl, uint32_t tmem,
-                         volatile int* abort_flag, int* status) {
+// PAIR: issued by rank 0 of the pair alone, as cta_group::2 MMAs over both
+// CTAs' operands; every commit arrives in both CTAs.  Its waits (sf_full,
+// tempty) also count arrivals from the peer's threads.
+template <bool PAIR>
+__device__ void mma_loop(const Geometry& G, const int32_t* off, int E, uint32_t a_base, uint32_t ring_base, Tail* tl,
+                         uint32_t tmem, volatile int* abort_flag, int* status) {
   const uint32_t b_off = G.b_off();
   uint32_t kc = 0, it = 0;
   bool aborted = false;
-  for (int u = blockIdx.x; u < G.num_mt && !aborted; u += gridDim.x) {
+  UnitCursor cur;
+  int u, e;
+  bool ghost;
+  for (int iu = 0; !aborted && unit_at(G, off, E, iu, cur, u, e, ghost); ++iu) {
     for (int q = 0; q < G.items && !aborted; ++q, ++it) {
       const uint32_t acc_slot = it % (uint32_t)G.nslot, suse = it / (uint32_t)G.nslot;
-      if (!wait_bounded(smem_u32(&tl->tempty[acc_slot]), (suse & 1u) ^ 1u, abort_flag, status)) { aborted = true; break; }
+      if (!wait_bounded(smem_u32(&tl->tempty[acc_slot]), (suse & 1u) ^ 1u, abort_flag, status)) {
+        aborted = true;
+        break;
+      }
       tc_fence_after();
-      const uint32_t dacc = tmem + acc_slot * BN;
+      const uint32_t dacc = tmem + acc_slot * (uint32_t)G.acc_cols;
       for (int ks = 0; ks < G.nk; ++ks, ++kc) {
-        uint32_t slot, use;
+        uint32_t slot, use, buf, buse;
         G.slot_of(kc, slot, use);
-        if (!wait_bounded(smem_u32(&tl->sf_full[slot]), use & 1u, abort_flag, status)) { aborted = true; break; }
+        G.sfbuf_of(kc, slot, use, buf, buse);
+        if (!wait_bounded(smem_u32(&tl->sf_full[buf]), buse & 1u, abort_flag, status)) { aborted = true; break; }
         tc_fence_after();
         const int nmma = min(4, G.kgroups - 4 * ks);
         const uint32_t st = ring_base + slot * G.stage_bytes;
-        const uint32_t sf_a = tmem + G.sf_col() + slot * SF_COLS;
+        const uint32_t sf_a = tmem + G.sf_col() + buf * G.sf_cols;
         const uint32_t sf_b = sf_a + 16;
         const uint64_t adesc = sdesc_k_sw128(G.resident ? a_base + ks * A_SLICE : st);
         const uint64_t bdesc = sdesc_k_sw128(st + b_off);
-        if (nmma == 4) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
-        } else {
+        if constexpr (PAIR) {
           for (int i = 0; i < nmma; ++i)
-            tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
+            tc_mma_pair(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 8 * i, (ks | i) != 0 ? 1u : 0u);
+          tc_commit_pair(smem_u32(&tl->b_empty[slot]));
+          tc_commit_pair(smem_u32(&tl->sf_empty[buf]));
+          if (G.resident && q == G.items - 1) tc_commit_pair(smem_u32(&tl->a_empty[ks]));
+        } else {
+          if (nmma == 4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
+          } else {
+            for (int i = 0; i < nmma; ++i)
+              tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&tl->b_empty[slot]));
+          if (G.resident && q == G.items - 1) tc_commit(smem_u32(&tl->a_empty[ks]));
         }
-        tc_commit(smem_u32(&tl->b_empty[slot]));
-        if (G.resident && q == G.items - 1) tc_commit(smem_u32(&tl->a_empty[ks]));
       }
-      if (!aborted) tc_commit(smem_u32(&tl->tfull[acc_slot]));
+      if (!aborted) {
+        if constexpr (PAIR)
+          tc_commit_pair(smem_u32(&tl->tfull[acc_slot]));
+        else
+          tc_commit(smem_u32(&tl->tfull[acc_slot]));
+      }
     }
   }
-  // all MMAs of this CTA have completed once `done` fires
-  tc_commit(smem_u32(&tl->done));
+  // all MMAs of this CTA (pair) have completed once `done` fires
+  if constexpr (PAIR)
+    tc_commit_pair(smem_u32(&tl->done));
+  else
+    tc_commit(smem_u32(&tl->done));
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(smem_u32(&tl->done), 0u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
   }
 }
 
-// Prologue: barriers and tensor memory.
-template <int NE>
+// Prologue: barriers and tensor memory.  PAIR: sf_full collects the writers
+// of both CTAs and tempty the epilogue warps of both; the tensor memory is
+// allocated for the pair (one warp in each CTA), and the cluster barrier
+// makes both CTAs' barriers initialised before any arrival from the peer.
+template <int NE, bool PAIR = false>
 __device__ __forceinline__ Tail* setup(uint8_t* tail_ptr) {
   Tail* tl = reinterpret_cast<Tail*>(tail_ptr);
   const int warp = threadIdx.x >> 5;
@@ -457,36 +655,57 @@ __device__ __forceinline__ Tail* setup(uint8_t* tail_ptr) {
     for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(smem_u32(&tl->b_full[s]), 1);
       mbar_init(smem_u32(&tl->b_empty[s]), 1);
-      mbar_init(smem_u32(&tl->sf_full[s]), 4);
+      mbar_init(smem_u32(&tl->sf_full[s]), PAIR ? 8 : 4);
     }
+    for (int s = 0; s < PAIR_SFBUF; ++s) mbar_init(smem_u32(&tl->sf_empty[s]), 1);
     for (int s = 0; s < NSLOT_MAX; ++s) {
       mbar_init(smem_u32(&tl->tfull[s]), 1);
-      mbar_init(smem_u32(&tl->tempty[s]), NE);
+      mbar_init(smem_u32(&tl->tempty[s]), PAIR ? 2 * NE : NE);
     }
     mbar_init(smem_u32(&tl->done), 1);
     tl->abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == Roles<NE>::MMA) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after();
   return tl;
 }
 
-template <int NE>
+// PAIR: the cluster barrier holds both CTAs (their shared and tensor
+// memory, which the pair's MMAs read and write) until rank 0's MMA thread
+// has seen all MMAs complete.
+template <int NE, bool PAIR = false>
 __device__ __forceinline__ void teardown(Tail* tl) {
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after();
   if ((threadIdx.x >> 5) == Roles<NE>::MMA) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
-                 : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
+                   : "memory");
   }
 }
 
@@ -566,8 +785,8 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int part,
 }
 
 // Shared roles of both GEMMs.  Returns true for the epilogue warps, which
-// the caller then runs.
-template <int NE>
+// the caller then runs.  PAIR: rank 1's MMA warp has nothing to issue.
+template <int NE, bool PAIR = false>
 __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, const CUtensorMap* tmap_b,
                                                    const uint8_t* a_sf, const uint8_t* b_sf, const Geometry& G,
                                                    const ItemRows& rows, const int32_t* off, int E, uint32_t a_base,
@@ -591,12 +810,13 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
     return false;
   }
   if (warp == RL::MMA) {
-    if (lane == 0) mma_loop(G, a_base, ring_base, tl, tl->tmem_base, abort_flag, status);
+    if (lane == 0 && (!PAIR || G.rank == 0))
+      mma_loop<PAIR>(G, off, E, a_base, ring_base, tl, tl->tmem_base, abort_flag, status);
     __syncwarp();
     return false;
   }
   if (warp >= RL::SFW && warp < RL::SFW + 4) {
-    sf_writer_loop(warp - RL::SFW, G, ring_base, tl, tl->tmem_base, abort_flag, status);
+    sf_writer_loop(warp - RL::SFW, G, off, E, ring_base, tl, tl->tmem_base, abort_flag, status);
     return false;
   }
   return true;
@@ -609,34 +829,48 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
 // ---------------------------------------------------------------------------
 // DBG: also write the debug outputs (pre-cast FP32 u, h before
 // requantisation) when their pointers are set; the production launch uses
-// the instantiation without them.
-template <bool DBG>
+// the instantiation without them.  PAIR: launched in clusters of two CTAs
+// that compute 256-row units with cta_group::2 MMAs of N = 256 (A resident;
+// an item is one chunk, gate and up in one 256-column accumulator; rank 0
+// holds the gate rows of B, rank 1 the up rows); each CTA runs the epilogue
+// of its own 128 rows.
+template <bool DBG, bool PAIR>
 __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(const __grid_constant__ Fc1Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int d_ff = args.d_ff, nch = d_ff / BN;
   Geometry G;
   G.num_mt = __ldg(args.offsets + args.E) / BM;
-  G.items = 2 * nch;
+  G.pair = PAIR;
+  G.rank = PAIR ? cluster_rank() : 0u;
+  G.cluster = PAIR ? (int)cluster_id_x() : 0;
+  G.nclusters = PAIR ? (int)cluster_count_x() : 1;
+  G.b_bytes = B_BYTES;
+  G.sfb_tiles = PAIR ? 2 : 1;
+  G.acc_cols = PAIR ? PAIR_ACC_COLS : BN;
+  G.sf_cols = PAIR ? PAIR_SF_COLS : SF_COLS;
+  G.items = PAIR ? nch : 2 * nch;
   G.nk = (args.d + 255) / 256;
   G.kgroups = args.d / 64;
   G.rings = args.rings;
   G.log2_stages = args.nb == 2 ? 1 : 0;
-  G.nslot = FC1_NSLOT;
+  G.nslot = PAIR ? 1 : FC1_NSLOT;
   G.resident = args.resident != 0;
-  G.stage_bytes = G.resident ? B_STAGE : A_SLICE + B_STAGE;
+  G.stage_bytes = (G.resident ? 0 : A_SLICE) + G.b_bytes + (G.sfb_tiles + 1) * SF_STAGE;
   const uint32_t a_base = smem_u32(smem);
   const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
   const size_t ring_bytes = (size_t)G.rings * (1 << G.log2_stages) * G.stage_bytes;
   const uint32_t ring_base = a_base + (uint32_t)a_bytes;
-  Tail* tl = setup<FC1_NE>(smem + a_bytes + ring_bytes);
+  Tail* tl = setup<FC1_NE, PAIR>(smem + a_bytes + ring_bytes);
   float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
   volatile int* abort_flag = &tl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ItemRows rows{true, 2 * d_ff, d_ff};
+  // the accumulator release goes to rank 0's barrier, which counts both CTAs
+  const uint32_t tempty0 = PAIR ? map_to_rank(smem_u32(&tl->tempty[0]), 0) : smem_u32(&tl->tempty[0]);
 
-  if (run_pipeline_roles<FC1_NE>(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
-                         ring_base, tl, args.status, args.a_rows, args.zero_row)) {
+  if (run_pipeline_roles<FC1_NE, PAIR>(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets,
+                                       args.E, a_base, ring_base, tl, args.status, args.a_rows, args.zero_row)) {
     // ---------------- epilogue warps ----------------
     const int q4 = warp & 3, part = warp >> 2;  // part: columns FC1_PART_COLS*part.. of each chunk
     const int rl = q4 * 32 + lane;              // row within the tile = TMEM lane
@@ -647,39 +881,47 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
     // it wrote, so program order is the only ordering needed).
     uint4* scratch_cta = reinterpret_cast<uint4*>(args.scratch) + (size_t)blockIdx.x * 2 * (size_t)(d_ff / 8) * BM;
     const float NLOG2E = -1.4426950408889634f;
-    bool have_prev = false;
+    bool have_prev = false, ghost_prev = false;
     int64_t row_prev = 0;
     float g_prev = 0.0f, den_prev = 0.0f;
     const uint4* scr_prev = scratch_cta;
     uint32_t it = 0, uc = 0;
-    for (int u = blockIdx.x; u < G.num_mt; u += gridDim.x, ++uc) {
-      const int e = expert_of(args.offsets, args.E, u);
+    UnitCursor cur;
+    int u, e;
+    bool ghost;
+    for (int iu = 0; unit_at(G, args.offsets, args.E, iu, cur, u, e, ghost); ++iu, ++uc) {
       const int64_t row = (int64_t)u * BM + rl;
+      const bool out = !PAIR || !ghost;  // a ghost tile computes but writes nothing
       const float ga = args.a_g[row];
       uint4* scratch = scratch_cta + (size_t)(uc & 1) * (size_t)(d_ff / 8) * BM;
       float* gws = gw_s + (uc & 1) * 2 * d_ff;
       stage_scales<FC1_NE>(gws, args.w_g + (int64_t)e * 2 * d_ff, 2 * d_ff, threadIdx.x);
       epi_barrier<FC1_NE>();
       uint32_t amax2 = 0;  // packed BF16 magnitudes
-      for (int c = 0; c < nch; ++c, it += 2) {
-        const uint32_t sg = it % FC1_NSLOT, su = (it + 1) % FC1_NSLOT;
+      for (int c = 0; c < nch; ++c, it += PAIR ? 1 : 2) {
+        // gate and up accumulators: two of the three slots, or the two halves
+        // of the pair's 256-column accumulator
+        const uint32_t sg = PAIR ? 0u : it % FC1_NSLOT, su = PAIR ? 0u : (it + 1) % FC1_NSLOT;
+        const uint32_t gcol = PAIR ? 0u : sg * BN, ucol = PAIR ? (uint32_t)BN : su * BN;
         const int n0 = c * BN + part * FC1_PART_COLS;  // first h column of this thread
         bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
-        if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (it / FC1_NSLOT) & 1u, abort_flag, args.status);
-        if (ok) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
-        // Two halves of 16 columns: load gate and up (one tensor-memory round
-        // trip), u = BF16(acc * (g_x * g_w)), h = BF16(silu(u_gate) * u_up),
-        // stage h; the accumulators are released after the second half.
+        if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (PAIR ? it : it / FC1_NSLOT) & 1u, abort_flag, args.status);
+        if (ok && !PAIR) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
+        // Drain: two halves of 16 columns, gate and up loaded together (one
+        // tensor-memory round trip each), u = BF16(acc * (g_x * g_w)) kept as
+        // packed pairs; then the accumulators are released, so the next MMAs
+        // do not wait for the SwiGLU, which runs from the registers:
+        // h = BF16(silu(u_gate) * u_up), staged, with the row amax.
+        uint32_t ugw[2][8], uuw[2][8];
         if (ok) {
           tc_fence_after();
-#pragma unroll 1
+#pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t Gv[16], Uv[16];
-            tmem_ld16(tmem + sg * BN + hh * 16, Gv);
-            tmem_ld16(tmem + su * BN + hh * 16, Uv);
+            tmem_ld16(tmem + gcol + hh * 16, Gv);
+            tmem_ld16(tmem + ucol + hh * 16, Uv);
             tmem_wait_ld();
             const int nh = n0 + hh * 16;
-            uint32_t hp[8], ugw[8], uuw[8];
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
               const float4 fg = *reinterpret_cast<const float4*>(gws + nh + i);
@@ -692,31 +934,50 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
                 const float yg1 = __fmul_rn(__uint_as_float(Gv[m + 1]), __fmul_rn(ga, gg[jj + 1]));
                 const float yu0 = __fmul_rn(__uint_as_float(Uv[m]), __fmul_rn(ga, uu[jj]));
                 const float yu1 = __fmul_rn(__uint_as_float(Uv[m + 1]), __fmul_rn(ga, uu[jj + 1]));
-                const uint32_t ugp = bf16x2_rn(yg0, yg1), uup = bf16x2_rn(yu0, yu1);
-                const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
-                const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
-                const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
-                const uint32_t h2 = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
-                amax2 = __vmaxu2(amax2, h2 & 0x7FFF7FFFu);
-                hp[m >> 1] = h2;
-                if (DBG && args.dbg_u) {
+                ugw[hh][m >> 1] = bf16x2_rn(yg0, yg1);
+                uuw[hh][m >> 1] = bf16x2_rn(yu0, yu1);
+                if (DBG && out && args.dbg_u) {
                   float* du = args.dbg_u + row * 2 * d_ff;
                   du[nh + m] = yg0; du[nh + m + 1] = yg1;
                   du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
                 }
-                ugw[m >> 1] = ugp;
-                uuw[m >> 1] = uup;
               }
             }
-            if (DBG && args.save_u) {  // 32-byte sectors: gate, then up
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) {
+            mbar_arrive_cluster(tempty0);
+          } else {
+            mbar_arrive(tempty0 + sg * 8u);
+            mbar_arrive(tempty0 + su * 8u);
+          }
+        }
+        if (ok) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int nh = n0 + hh * 16;
+            uint32_t hp[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              const uint32_t ugp = ugw[hh][w], uup = uuw[hh][w];
+              const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
+              const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
+              const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
+              hp[w] = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
+              amax2 = __vmaxu2(amax2, hp[w] & 0x7FFF7FFFu);
+            }
+            if (DBG && out && args.save_u) {  // 32-byte sectors: gate, then up
               uint4* sg4 = reinterpret_cast<uint4*>(args.save_u + row * 2 * d_ff + nh);
               uint4* su4 = reinterpret_cast<uint4*>(args.save_u + row * 2 * d_ff + d_ff + nh);
-              sg4[0] = make_uint4(ugw[0], ugw[1], ugw[2], ugw[3]);
-              sg4[1] = make_uint4(ugw[4], ugw[5], ugw[6], ugw[7]);
-              su4[0] = make_uint4(uuw[0], uuw[1], uuw[2], uuw[3]);
-              su4[1] = make_uint4(uuw[4], uuw[5], uuw[6], uuw[7]);
+              sg4[0] = make_uint4(ugw[hh][0], ugw[hh][1], ugw[hh][2], ugw[hh][3]);
+              sg4[1] = make_uint4(ugw[hh][4], ugw[hh][5], ugw[hh][6], ugw[hh][7]);
+              su4[0] = make_uint4(uuw[hh][0], uuw[hh][1], uuw[hh][2], uuw[hh][3]);
+              su4[1] = make_uint4(uuw[hh][4], uuw[hh][5], uuw[hh][6], uuw[hh][7]);
             }
-            if (DBG && args.dbg_h) {
+            if (DBG && out && args.dbg_h) {
               uint4* dh = reinterpret_cast<uint4*>(args.dbg_h + row * d_ff + nh);
               dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
               dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
@@ -725,13 +986,7 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
             scratch[(size_t)((c * FC1_PARTS + part) * 4 + 2 * hh + 1) * BM + rl] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&tl->tempty[sg]));
-          mbar_arrive(smem_u32(&tl->tempty[su]));
-        }
-        if (have_prev && !*abort_flag)
+        if (have_prev && !ghost_prev && !*abort_flag)
           requant_chunk(scr_prev, c, part, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf, d_ff);
       }
       // ---- outer scale of the unit's rows: amax over the full d_ff row ----
@@ -740,23 +995,24 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
       float a = tl->rowmax[0][rl];
 #pragma unroll
       for (int p2 = 1; p2 < FC1_PARTS; ++p2) a = fmaxf(a, tl->rowmax[p2][rl]);
-      if (have_prev && part == 0) args.h_g[row_prev] = g_prev;
-      if (!*abort_flag && !is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
+      if (have_prev && !ghost_prev && part == 0) args.h_g[row_prev] = g_prev;
+      if (out && !*abort_flag && !is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
       have_prev = true;
+      ghost_prev = !out;
       row_prev = row;
       g_prev = __fdiv_rn(a, 2688.0f);
       den_prev = __fmul_rn(6.0f, g_prev);
       scr_prev = scratch;
     }
     // the last unit
-    if (have_prev) {
+    if (have_prev && !ghost_prev) {
       if (!*abort_flag)
         for (int c = 0; c < nch; ++c)
           requant_chunk(scr_prev, c, part, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf, d_ff);
       if (part == 0) args.h_g[row_prev] = g_prev;
     }
   }
-  teardown<FC1_NE>(tl);
+  teardown<FC1_NE, PAIR>(tl);
 }
 
 // ---------------------------------------------------------------------------
@@ -776,6 +1032,14 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
   const int d = args.d, k = args.k;
   Geometry G;
   G.num_mt = __ldg(args.offsets + args.E) / BM;
+  G.pair = false;
+  G.rank = 0u;
+  G.cluster = 0;
+  G.nclusters = 1;
+  G.b_bytes = B_BYTES;
+  G.sfb_tiles = 1;
+  G.acc_cols = BN;
+  G.sf_cols = SF_COLS;
   G.items = d / BN;
   G.nk = (args.d_ff + 255) / 256;
   G.kgroups = args.d_ff / 64;
@@ -783,7 +1047,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
   G.log2_stages = args.nb == 2 ? 1 : 0;
   G.nslot = FC2_NSLOT;
   G.resident = args.resident != 0;
-  G.stage_bytes = G.resident ? B_STAGE : A_SLICE + B_STAGE;
+  G.stage_bytes = (G.resident ? 0 : A_SLICE) + G.b_bytes + 2 * SF_STAGE;
   const uint32_t a_base = smem_u32(smem);
   const size_t a_bytes = G.resident ? (size_t)G.nk * A_SLICE : 0;
   const size_t ring_bytes = (size_t)G.rings * (1 << G.log2_stages) * G.stage_bytes;
@@ -992,11 +1256,89 @@ static int fc_grid(int64_t m_cap) {
   return grid;
 }
 
+// CTA-pair plan: A resident, PAIR_RINGS rings of 2^PAIR_LOG2_STAGES stages
+// of PAIR_STAGE bytes, PAIR_SFBUF scale buffers after the accumulators.  The
+// a_empty reach rule is the single-CTA plan's.
+static bool plan_pair(int K, int items, int scale_floats, size_t* smem) {
+  const int nk = (K + 255) / 256;
+  const int stages = PAIR_RINGS << PAIR_LOG2_STAGES;
+  if (nk > MAX_A_SLOTS || (int64_t)(items + 1) * nk < stages) return false;
+  if (PAIR_ACC_COLS + PAIR_SFBUF * PAIR_SF_COLS > TMEM_COLS) return false;
+  const size_t need =
+      1024 + TAIL_BYTES + (size_t)2 * scale_floats * 4 + (size_t)nk * A_SLICE + (size_t)stages * PAIR_STAGE;
+  if (need > (size_t)SMEM_LIMIT) return false;
+  *smem = need;
+  return true;
+}
+
+// Clusters of two that can be resident at once with `smem` bytes per CTA.
+static int pair_clusters(void (*kern)(const Fc1Args), size_t smem) {
+  static void (*cached_kern)(const Fc1Args) = nullptr;
+  static size_t cached_smem = 0;
+  static int cached = 0;
+  if (kern == cached_kern && smem == cached_smem) return cached;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(Roles<FC1_NE>::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cached_kern = kern;
+  cached_smem = smem;
+  cached = n;
+  return n;
+}
+
+// FC1 runs on CTA pairs (clusters of two, cta_group::2 MMAs) when the pair
+// plan fits, A is not gathered and the device can hold clusters of two;
+// MOE_FC1_CTA_PAIRS=0 in the environment selects single CTAs throughout.
 int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
-  size_t smem;
-  if (!plan(a.d, 2 * (a.d_ff / BN), 2 * a.d_ff, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem)) return -1;
   const bool dbg = a.dbg_u != nullptr || a.dbg_h != nullptr || a.save_u != nullptr;
-  void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true> : fc1_swiglu_kernel<false>;
+  const char* env = std::getenv("MOE_FC1_CTA_PAIRS");
+  const bool allow_pairs = !(env && env[0] == '0');
+  size_t smem;
+  if (allow_pairs && a.a_rows == nullptr && plan_pair(a.d, a.d_ff / BN, 2 * a.d_ff, &smem)) {
+    void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true, true> : fc1_swiglu_kernel<false, true>;
+    if (set_smem((const void*)kern, smem) != 0) return -1;
+    int clusters = pair_clusters(kern, smem);
+    const int sms = gemm_num_ctas();
+    if (sms > 0 && clusters > sms / 2) clusters = sms / 2;
+    // every pair unit holds at least one of the m_cap / 128 tiles (the device
+    // walks the actual units)
+    const int64_t pair_units = m_cap / BM;
+    if (pair_units < clusters) clusters = (int)pair_units;
+    if (clusters >= 1) {
+      a.rings = PAIR_RINGS;
+      a.nb = 1 << PAIR_LOG2_STAGES;
+      a.resident = 1;
+      a.na = (a.d + 255) / 256;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(2 * clusters));
+      cfg.blockDim = dim3(Roles<FC1_NE>::THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? 0 : -1;
+    }
+  }
+  if (!plan(a.d, 2 * (a.d_ff / BN), 2 * a.d_ff, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem)) return -1;
+  void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true, false> : fc1_swiglu_kernel<false, false>;
   if (set_smem((const void*)kern, smem) != 0) return -1;
   const int grid = fc_grid(m_cap);
   if (grid <= 0) return -1;

@@ -102,6 +102,22 @@ def test_forward_against_oracle(orc, name):
     assert rel <= E2E_REL_L2 and mx <= E2E_MAX_ABS
 
 
+@pytest.mark.parametrize("name", ["small", "ragged"])
+def test_forward_cta_pairs_equal_single(orc, name, monkeypatch):
+    """The forward with FC1 on CTA pairs (the default at these shapes) and
+    with FC1 on single CTAs: identical h codes and output, bit for bit."""
+    lay = layer_of(name)
+    x, lg, W1, W2 = lay.x(), lay.logits(), lay.w1(), lay.w2()
+    r2, w1q, w2q = gpu_forward(lay, x, lg, W1, W2)
+    monkeypatch.setenv("MOE_FC1_CTA_PAIRS", "0")
+    r1, _, _ = gpu_forward(lay, x, lg, w1q=w1q, w2q=w2q)
+    assert r1["status"] == 0 and r2["status"] == 0
+    mp = int(r1["offsets"][-1])
+    assert np.array_equal(r2["h_codes"][:mp], r1["h_codes"][:mp])
+    assert np.array_equal(r2["h_g"][:mp].view(np.uint32), r1["h_g"][:mp].view(np.uint32))
+    assert np.array_equal(r2["out"], r1["out"])
+
+
 def test_forward_equals_modular_composition(orc):
     """moe_expert_forward = moe_permute_amax + nvfp4_quantize_rows +
     FC1 + FC2/unpermute, bit for bit."""

@@ -146,3 +146,24 @@ def test_fc2_parity(orc, name, T):
     slots_ref = orc.combine(y_full, c["perm"], c["w"], c["T"], lay.k, lay.d)
     assert np.array_equal(g["slots"], slots_ref)
     assert np.array_equal(g["out"], orc.reduce(g["slots"]))
+
+
+@pytest.mark.parametrize("name", ["small", "custom_skew"])
+def test_fc1_cta_pairs_equal_single(orc, name, monkeypatch):
+    """FC1 on CTA pairs (cta_group::2 MMAs over 256-row units, the default
+    where the pair plan fits) and on single CTAs produce the same bits: the
+    same K order per output element, only the tile's rows split over two
+    SMs.  custom_skew has empty experts and experts with an odd tile count,
+    whose last pair unit leaves rank 1 without a tile of its own."""
+    lay = layer_of(name)
+    c = make_case(orc, lay)
+    mp = c["perm"]["m_pad"]
+    g2 = run_fc1(lay, c)
+    monkeypatch.setenv("MOE_FC1_CTA_PAIRS", "0")
+    g1 = run_fc1(lay, c)
+    assert g1["status"] == 0 and g2["status"] == 0
+    assert np.array_equal(g2["u"][:mp].view(np.uint32), g1["u"][:mp].view(np.uint32))
+    assert np.array_equal(g2["h"][:mp], g1["h"][:mp])
+    assert np.array_equal(g2["h_codes"][:mp], g1["h_codes"][:mp])
+    assert np.array_equal(g2["h_g"][:mp].view(np.uint32), g1["h_g"][:mp].view(np.uint32))
+    assert np.array_equal(orc.unswizzle_sf(g2["h_sf"], mp, lay.d_ff), orc.unswizzle_sf(g1["h_sf"], mp, lay.d_ff))

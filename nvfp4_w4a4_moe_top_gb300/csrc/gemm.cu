@@ -64,7 +64,7 @@ constexpr int B_STAGE = B_BYTES + 2 * SF_STAGE;        // 20 KB: B, SFB, SFA
 // scale buffers in tensor memory form a ring of their own, decoupled from
 // the stages.
 constexpr int PAIR_STAGE = B_BYTES + 3 * SF_STAGE;     // 22 KB: B, SFB gate, SFB up, SFA
-constexpr int PAIR_RINGS = 3, PAIR_LOG2_STAGES = 0;    // 3 rings x 1 stage
+constexpr int PAIR_RINGS_MAX = 4;                      // rings of one stage (3 when 4 do not fit)
 constexpr int PAIR_SFBUF = 4;                          // tensor-memory scale buffers
 constexpr int PAIR_ACC_COLS = 2 * BN;                  // the 256-column accumulator
 constexpr int PAIR_SF_COLS = 64;                       // per buffer: [A scales 16 | B scales 32 | unused 16]
@@ -894,7 +894,9 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
       const bool out = !PAIR || !ghost;  // a ghost tile computes but writes nothing
       const float ga = args.a_g[row];
       uint4* scratch = scratch_cta + (size_t)(uc & 1) * (size_t)(d_ff / 8) * BM;
-      float* gws = gw_s + (uc & 1) * 2 * d_ff;
+      // one buffer: every read of the previous unit's scales precedes the
+      // end-of-unit barrier, which precedes this staging
+      float* gws = gw_s;
       stage_scales<FC1_NE>(gws, args.w_g + (int64_t)e * 2 * d_ff, 2 * d_ff, threadIdx.x);
       epi_barrier<FC1_NE>();
       uint32_t amax2 = 0;  // packed BF16 magnitudes
@@ -1203,7 +1205,7 @@ int gemm_num_ctas() {
 }
 
 // Pipeline plan for reduction length K, `items` accumulator tiles per unit,
-// `scale_floats` per-column scales per expert (staged twice) and `extra`
+// `scale_bytes` of per-column scales staged per unit and `extra`
 // bytes of epilogue staging.  The tensor memory after the accumulators holds
 // one scale buffer per stage; rings are 3 or 4, stages per ring 1 or 2, and
 // the plan takes the most stages that fit.  A is resident (loaded once per
@@ -1212,10 +1214,10 @@ int gemm_num_ctas() {
 // (items + 1) * nk >= rings*S keeps it from reaching the A slots of unit m
 // before the slots of unit m-2 are released, so the parity of every a_empty
 // wait is unambiguous.  Otherwise A streams through the stages with B.
-static bool plan(int K, int items, int scale_floats, int nslot, size_t extra, int* rings, int* na, int* nb,
+static bool plan(int K, int items, size_t scale_bytes, int nslot, size_t extra, int* rings, int* na, int* nb,
                  int* resident, size_t* smem) {
   const int nk = (K + 255) / 256;
-  const size_t fixed = 1024 /* alignment */ + TAIL_BYTES + (size_t)2 * scale_floats * 4 + extra;
+  const size_t fixed = 1024 /* alignment */ + TAIL_BYTES + scale_bytes + extra;
   if (fixed >= (size_t)SMEM_LIMIT) return false;
   const size_t avail = SMEM_LIMIT - fixed;
   static const int cand[4][2] = {{4, 2}, {3, 2}, {4, 1}, {3, 1}};  // (rings, stages per ring), most stages first
@@ -1256,19 +1258,21 @@ static int fc_grid(int64_t m_cap) {
   return grid;
 }
 
-// CTA-pair plan: A resident, PAIR_RINGS rings of 2^PAIR_LOG2_STAGES stages
-// of PAIR_STAGE bytes, PAIR_SFBUF scale buffers after the accumulators.  The
-// a_empty reach rule is the single-CTA plan's.
-static bool plan_pair(int K, int items, int scale_floats, size_t* smem) {
+// CTA-pair plan: A resident, PAIR_RINGS_MAX (or one fewer) rings of one
+// PAIR_STAGE stage each, PAIR_SFBUF scale buffers after the accumulator.
+// The a_empty reach rule is the single-CTA plan's.
+static bool plan_pair(int K, int items, size_t scale_bytes, int* rings, size_t* smem) {
   const int nk = (K + 255) / 256;
-  const int stages = PAIR_RINGS << PAIR_LOG2_STAGES;
-  if (nk > MAX_A_SLOTS || (int64_t)(items + 1) * nk < stages) return false;
   if (PAIR_ACC_COLS + PAIR_SFBUF * PAIR_SF_COLS > TMEM_COLS) return false;
-  const size_t need =
-      1024 + TAIL_BYTES + (size_t)2 * scale_floats * 4 + (size_t)nk * A_SLICE + (size_t)stages * PAIR_STAGE;
-  if (need > (size_t)SMEM_LIMIT) return false;
-  *smem = need;
-  return true;
+  for (int R = PAIR_RINGS_MAX; R >= PAIR_RINGS_MAX - 1; --R) {
+    if (nk > MAX_A_SLOTS || (int64_t)(items + 1) * nk < R) continue;
+    const size_t need = 1024 + TAIL_BYTES + scale_bytes + (size_t)nk * A_SLICE + (size_t)R * PAIR_STAGE;
+    if (need > (size_t)SMEM_LIMIT) continue;
+    *rings = R;
+    *smem = need;
+    return true;
+  }
+  return false;
 }
 
 // Clusters of two that can be resident at once with `smem` bytes per CTA.
@@ -1307,7 +1311,8 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
   const char* env = std::getenv("MOE_FC1_CTA_PAIRS");
   const bool allow_pairs = !(env && env[0] == '0');
   size_t smem;
-  if (allow_pairs && a.a_rows == nullptr && plan_pair(a.d, a.d_ff / BN, 2 * a.d_ff, &smem)) {
+  int pair_rings = 0;
+  if (allow_pairs && a.a_rows == nullptr && plan_pair(a.d, a.d_ff / BN, (size_t)2 * a.d_ff * 4, &pair_rings, &smem)) {
     void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true, true> : fc1_swiglu_kernel<false, true>;
     if (set_smem((const void*)kern, smem) != 0) return -1;
     int clusters = pair_clusters(kern, smem);
@@ -1318,8 +1323,8 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
     const int64_t pair_units = m_cap / BM;
     if (pair_units < clusters) clusters = (int)pair_units;
     if (clusters >= 1) {
-      a.rings = PAIR_RINGS;
-      a.nb = 1 << PAIR_LOG2_STAGES;
+      a.rings = pair_rings;
+      a.nb = 1;
       a.resident = 1;
       a.na = (a.d + 255) / 256;
       cudaLaunchConfig_t cfg = {};
@@ -1337,7 +1342,8 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
       return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? 0 : -1;
     }
   }
-  if (!plan(a.d, 2 * (a.d_ff / BN), 2 * a.d_ff, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem)) return -1;
+  if (!plan(a.d, 2 * (a.d_ff / BN), (size_t)2 * a.d_ff * 4, FC1_NSLOT, 0, &a.rings, &a.na, &a.nb, &a.resident, &smem))
+    return -1;
   void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true, false> : fc1_swiglu_kernel<false, false>;
   if (set_smem((const void*)kern, smem) != 0) return -1;
   const int grid = fc_grid(m_cap);
@@ -1348,7 +1354,8 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
 
 int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream) {
   size_t smem;
-  if (!plan(a.d_ff, a.d / BN, a.d, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident, &smem))
+  if (!plan(a.d_ff, a.d / BN, (size_t)2 * a.d * 4, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident,
+            &smem))
     return -1;
   void (*kern)(const Fc2Args) = a.dw != nullptr      ? fc2_scatter_kernel<2>
                                  : a.dbg_y != nullptr ? fc2_scatter_kernel<1>

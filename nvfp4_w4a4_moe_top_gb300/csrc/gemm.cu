@@ -297,9 +297,14 @@ struct Geometry {
   // first TMEM column of the scale buffers (after the accumulators; one per
   // stage, or a ring of PAIR_SFBUF in a pair)
   __device__ uint32_t sf_col() const { return (uint32_t)(nslot * acc_cols); }
+  // CTA pairs keep a separate ring of scale buffers (released by sf_empty)
+  // unless the stage ring has as many stages as there are buffers: then
+  // buffer and stage coincide, and a stage's refill (after the commit of its
+  // previous MMAs) already says the buffer is free.
+  __device__ bool sf_ring() const { return pair && (rings << log2_stages) != PAIR_SFBUF; }
   // scale buffer of CTA-local k-step kc (stage slot `slot`) and its use count
   __device__ void sfbuf_of(uint32_t kc, uint32_t slot, uint32_t use, uint32_t& buf, uint32_t& buse) const {
-    if (pair) {
+    if (sf_ring()) {
       buf = kc & (PAIR_SFBUF - 1);
       buse = kc / PAIR_SFBUF;
     } else {
@@ -496,9 +501,10 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
 //     scale bytes of row 32*qd + l in A-scale tile i (bytes 16*l + 4*qd).
 // Single CTAs: the stage's buffer is rewritten only after its next use has
 // landed, which the producer issues only after the MMAs of the previous use
-// completed.  CTA pairs: the buffers form a ring of their own, and a buffer
-// is rewritten once the commit of its previous MMAs (sf_empty, arriving in
-// both CTAs) says they completed.
+// completed.  CTA pairs with as many stages as scale buffers: the same.
+// Otherwise the buffers form a ring of their own, and a buffer is rewritten
+// once the commit of its previous MMAs (sf_empty, arriving in both CTAs)
+// says they completed.
 // The writers also wait for the resident A slice of the k-step (first item of
 // a unit), so the MMA thread waits on sf_full alone: its completion implies
 // that the stage's operands and the A slice have landed (in a pair, in both
@@ -522,7 +528,7 @@ __device__ void sf_writer_loop(int qd, const Geometry& G, const int32_t* off, in
         G.sfbuf_of(kc, slot, use, buf, buse);
         bool ok = warp_wait(smem_u32(&tl->b_full[slot]), use & 1u, abort_flag, status);
         if (ok && G.resident && q == 0) ok = warp_wait(smem_u32(&tl->a_full[ks]), unit_use & 1u, abort_flag, status);
-        if (ok && G.pair) ok = warp_wait(smem_u32(&tl->sf_empty[buf]), (buse & 1u) ^ 1u, abort_flag, status);
+        if (ok && G.sf_ring()) ok = warp_wait(smem_u32(&tl->sf_empty[buf]), (buse & 1u) ^ 1u, abort_flag, status);
         if (!ok) { aborted = true; break; }
         tc_fence_after();
         const int nsf = min(4, G.kgroups - 4 * ks);
@@ -606,7 +612,7 @@ __device__ void mma_loop(const Geometry& G, const int32_t* off, int E, uint32_t 
           for (int i = 0; i < nmma; ++i)
             tc_mma_pair(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 8 * i, (ks | i) != 0 ? 1u : 0u);
           tc_commit_pair(smem_u32(&tl->b_empty[slot]));
-          tc_commit_pair(smem_u32(&tl->sf_empty[buf]));
+          if (G.sf_ring()) tc_commit_pair(smem_u32(&tl->sf_empty[buf]));
           if (G.resident && q == G.items - 1) tc_commit_pair(smem_u32(&tl->a_empty[ks]));
         } else {
           if (nmma == 4) {

@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch of the dominant kernel, from one ncu capture of the
 # source whose hash is recorded (profiles/fc1_dram_traffic_qwen64k.md); the
 # bench reports null once the kernel source differs.
-NCU_TRAFFIC = {"fc1": {"src_sha": "b314e5fe42510a09", "bytes_per_launch": 1270033408 + 954439936,
+NCU_TRAFFIC = {"fc1": {"src_sha": "f05d8fb202485f11", "bytes_per_launch": 1428445184 + 1050287616,
                        "workload": "qwen64k"}}
 
 

@@ -389,7 +389,10 @@ def native(args):
     fc1_tflops = alg["fc1_flops"] / t_fc1 / 1e12
     sha = src_sha("gemm.cu", "common.cuh")
     tr = NCU_TRAFFIC.get("fc1")
-    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == sha else None
+    # ncu's DRAM bytes of one launch, valid only for the kernel source and the
+    # workload they were captured on
+    traffic = (tr["bytes_per_launch"] if tr and tr.get("src_sha") == sha and tr.get("workload") == args.workload
+               else None)
     roofline = {"kernel": "fc1_swiglu_kernel", "bound": "tensor", "achieved": round(fc1_tflops, 1),
                 "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(fc1_tflops / fp4_peak, 4),
                 "traffic": traffic, "ms_per_launch": round(t_fc1 * 1e3, 4),

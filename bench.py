@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -42,15 +43,21 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch of the dominant kernel, from one ncu capture of the
 # source whose hash is recorded (profiles/fc1_dram_traffic_qwen64k.md); the
 # bench reports null once the kernel source differs.
-NCU_TRAFFIC = {"fc1": {"src_sha": "f05d8fb202485f11", "bytes_per_launch": 1428445184 + 1050287616,
+NCU_TRAFFIC = {"fc1": {"src_sha": "5426b71a6129df7a", "bytes_per_launch": 1428445184 + 1050287616,
                        "workload": "qwen64k"}}
 
 
 def src_sha(*names):
+    """Hash of the sources' code: // comments, trailing blanks and blank lines
+    are left out, so a comment edit keeps a capture valid and any code
+    change invalidates it."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "nvfp4_w4a4_moe_top_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "nvfp4_w4a4_moe_top_gb300", "csrc", n), encoding="utf-8") as f:
+            for line in f:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -40,6 +40,15 @@
 //   FC2: the items of a unit are the d/128 output tiles; the epilogue forms
 //        y2 = acc * (g_h * g_w2), z = BF16(w_{t,e} * y2) and writes slot (t, j).
 //
+// FC1 on CTA pairs (where its plan fits): clusters of two CTAs, a unit being
+// two 128-row tiles of one expert.  Rank 0's MMA thread issues
+// tcgen05.mma.cta_group::2 of M = 256 (each CTA's 128 rows from its own
+// resident A) and N = 256 (a chunk's gate from rank 0's B tile, its up from
+// rank 1's), K = 64, into one 256-column accumulator per CTA; every commit
+// arrives in both CTAs.  Both CTAs' scale writers and epilogue warps arrive
+// on rank 0's sf_full / tempty barriers.  Each CTA runs the epilogue of its
+// own rows, and releases the accumulator once u is formed, before the SwiGLU.
+//
 // Every wait is bounded (a few seconds of wall clock); on expiry the kernel
 // raises MOE_STATUS_TIMEOUT, drains its own copies and MMAs, frees tensor
 // memory and returns.

@@ -69,6 +69,11 @@ def layer_of(name):
         # K = 128 in both GEMMs: one k-step per item, hundreds of units per
         # launch, so the producers run many units ahead of the MMAs
         return synth.custom(T=6000, d=128, E=4, k=2, d_ff=128, seed=6)
+    if name == "custom_pair_skew":
+        # d and d_ff multiples of 256, empty experts and experts with an odd
+        # tile count (the last CTA-pair unit of such an expert has one tile)
+        return synth.custom(T=900, d=512, E=10, k=3, d_ff=512, seed=9, logits="bias", bias_std=2.5,
+                            n_forced_empty=3)
     if name == "custom_skew":
         return synth.custom(T=700, d=384, E=16, k=3, d_ff=384, seed=5, logits="bias", bias_std=3.0,
                             n_forced_empty=5)
@@ -148,7 +153,7 @@ def test_fc2_parity(orc, name, T):
     assert np.array_equal(g["out"], orc.reduce(g["slots"]))
 
 
-@pytest.mark.parametrize("name", ["small", "custom_skew"])
+@pytest.mark.parametrize("name", ["small", "custom_skew", "custom_pair_skew"])
 def test_fc1_cta_pairs_equal_single(orc, name, monkeypatch):
     """FC1 on CTA pairs (cta_group::2 MMAs over 256-row units, the default
     where the pair plan fits) and on single CTAs produce the same bits: the

@@ -1319,7 +1319,8 @@ static int pair_clusters(void (*kern)(const Fc1Args), size_t smem) {
 }
 
 // FC1 runs on CTA pairs (clusters of two, cta_group::2 MMAs) when the pair
-// plan fits, A is not gathered and the device can hold clusters of two;
+// plan fits and the device can hold clusters of two (A rows loaded as boxes
+// or gathered alike: each CTA loads its own tile's rows);
 // MOE_FC1_CTA_PAIRS=0 in the environment selects single CTAs throughout.
 int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
   const bool dbg = a.dbg_u != nullptr || a.dbg_h != nullptr || a.save_u != nullptr;
@@ -1327,7 +1328,7 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
   const bool allow_pairs = !(env && env[0] == '0');
   size_t smem;
   int pair_rings = 0;
-  if (allow_pairs && a.a_rows == nullptr && plan_pair(a.d, a.d_ff / BN, (size_t)2 * a.d_ff * 4, &pair_rings, &smem)) {
+  if (allow_pairs && plan_pair(a.d, a.d_ff / BN, (size_t)2 * a.d_ff * 4, &pair_rings, &smem)) {
     void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true, true> : fc1_swiglu_kernel<false, true>;
     if (set_smem((const void*)kern, smem) != 0) return -1;
     int clusters = pair_clusters(kern, smem);

@@ -924,39 +924,37 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
         bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (PAIR ? it : it / FC1_NSLOT) & 1u, abort_flag, args.status);
         if (ok && !PAIR) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
-        // Drain: two halves of 16 columns, gate and up loaded together (one
-        // tensor-memory round trip each), u = BF16(acc * (g_x * g_w)) kept as
-        // packed pairs; then the accumulators are released, so the next MMAs
-        // do not wait for the SwiGLU, which runs from the registers:
-        // h = BF16(silu(u_gate) * u_up), staged, with the row amax.
+        // Drain: two halves of 16 columns, gate then up (one tensor-memory
+        // round trip each, which keeps fewer values live than loading both
+        // together), u = BF16(acc * (g_x * g_w)) kept as packed pairs; then
+        // the accumulators are released, so the next MMAs do not wait for the
+        // SwiGLU, which runs from the registers: h = BF16(silu(u_gate) *
+        // u_up), staged, with the row amax.
         uint32_t ugw[2][8], uuw[2][8];
         if (ok) {
           tc_fence_after();
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t Gv[16], Uv[16];
-            tmem_ld16(tmem + gcol + hh * 16, Gv);
-            tmem_ld16(tmem + ucol + hh * 16, Uv);
-            tmem_wait_ld();
             const int nh = n0 + hh * 16;
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              const float4 fg = *reinterpret_cast<const float4*>(gws + nh + i);
-              const float4 fu = *reinterpret_cast<const float4*>(gws + d_ff + nh + i);
-              const float gg[4] = {fg.x, fg.y, fg.z, fg.w}, uu[4] = {fu.x, fu.y, fu.z, fu.w};
+            for (int gu = 0; gu < 2; ++gu) {
+              uint32_t V[16];
+              tmem_ld16(tmem + (gu ? ucol : gcol) + hh * 16, V);
+              tmem_wait_ld();
 #pragma unroll
-              for (int jj = 0; jj < 4; jj += 2) {
-                const int m = i + jj;
-                const float yg0 = __fmul_rn(__uint_as_float(Gv[m]), __fmul_rn(ga, gg[jj]));
-                const float yg1 = __fmul_rn(__uint_as_float(Gv[m + 1]), __fmul_rn(ga, gg[jj + 1]));
-                const float yu0 = __fmul_rn(__uint_as_float(Uv[m]), __fmul_rn(ga, uu[jj]));
-                const float yu1 = __fmul_rn(__uint_as_float(Uv[m + 1]), __fmul_rn(ga, uu[jj + 1]));
-                ugw[hh][m >> 1] = bf16x2_rn(yg0, yg1);
-                uuw[hh][m >> 1] = bf16x2_rn(yu0, yu1);
-                if (DBG && out && args.dbg_u) {
-                  float* du = args.dbg_u + row * 2 * d_ff;
-                  du[nh + m] = yg0; du[nh + m + 1] = yg1;
-                  du[d_ff + nh + m] = yu0; du[d_ff + nh + m + 1] = yu1;
+              for (int i = 0; i < 16; i += 4) {
+                const float4 fs = *reinterpret_cast<const float4*>(gws + gu * d_ff + nh + i);
+                const float ss[4] = {fs.x, fs.y, fs.z, fs.w};
+#pragma unroll
+                for (int jj = 0; jj < 4; jj += 2) {
+                  const int m = i + jj;
+                  const float y0 = __fmul_rn(__uint_as_float(V[m]), __fmul_rn(ga, ss[jj]));
+                  const float y1 = __fmul_rn(__uint_as_float(V[m + 1]), __fmul_rn(ga, ss[jj + 1]));
+                  if (gu) uuw[hh][m >> 1] = bf16x2_rn(y0, y1); else ugw[hh][m >> 1] = bf16x2_rn(y0, y1);
+                  if (DBG && out && args.dbg_u) {
+                    float* du = args.dbg_u + row * 2 * d_ff + gu * d_ff;
+                    du[nh + m] = y0; du[nh + m + 1] = y1;
+                  }
                 }
               }
             }

@@ -246,7 +246,13 @@ int nvfp4_quantize_rows(const uint16_t* src, int src_rows, int K,
  *                     offsets[E] untouched)
  *   dbg_u_f32  f32 [M_cap][2 d_ff] pre-cast FC1 outputs, or NULL
  *   dbg_h      bf16 [M_cap][d_ff] h before requantisation, or NULL
- *   ws         nvfp4_fc1_workspace_bytes(d_ff) bytes of device scratch */
+ *   ws         nvfp4_fc1_workspace_bytes(d_ff) bytes of device scratch
+ * Launch: where A fits resident beside the pipeline (d <= 2048), the kernel
+ * runs on pairs of CTAs (clusters of two, cta_group::2 MMAs covering two
+ * 128-row tiles and a chunk's gate and up columns); elsewhere on single
+ * CTAs.  Both give the same bits.  The environment variable
+ * MOE_FC1_CTA_PAIRS=0, read at each launch, selects single CTAs throughout
+ * (this entry point and the forwards). */
 int nvfp4_grouped_gemm_fc1_swiglu(
     const uint8_t* a_codes, const uint8_t* a_sf, const float* a_g,
     const int32_t* offsets, int E, int64_t M_cap, int d, int d_ff,

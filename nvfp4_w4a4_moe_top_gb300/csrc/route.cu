@@ -43,7 +43,18 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float NEG_INF = __uint_as_float(0xFF800000u);
-  for (int tl = warp; tl < kChunk; tl += blockDim.x / 32) {
+  const int tstep = blockDim.x / 32;
+  // the warp's next token's logits are loaded while it routes the current one
+  float nxt[NPL];
+  auto load_logits = [&](int t) {
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      nxt[i] = e < E ? __ldg(logits + (int64_t)t * E + e) : NEG_INF;
+    }
+  };
+  if (logits && t0 + warp < T) load_logits(t0 + warp);
+  for (int tl = warp; tl < kChunk; tl += tstep) {
     const int t = t0 + tl;
     if (t >= T) break;
     int my_id = 0x7FFFFFFF;
@@ -53,13 +64,13 @@ __global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ l
       bool fin = true;
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {
-        const int e = i * 32 + lane;
+        const float x = nxt[i];
         v[i] = NEG_INF;
-        if (e < E) {
-          const float x = __ldg(logits + (int64_t)t * E + e);
+        if (i * 32 + lane < E) {
           if (is_finite_f32(x)) v[i] = x; else fin = false;
         }
       }
+      if (tl + tstep < kChunk && t + tstep < T) load_logits(t + tstep);
       if (!__all_sync(0xFFFFFFFFu, fin) && lane == 0) set_status(status, MOE_STATUS_NONFINITE_LOGITS);
       // k rounds: the lane's best untaken logit (its ids ascend with i, so
       // the first of equal keys has the smaller id), then the warp's largest

@@ -74,6 +74,11 @@ def layer_of(name):
         # tile count (the last CTA-pair unit of such an expert has one tile)
         return synth.custom(T=900, d=512, E=10, k=3, d_ff=512, seed=9, logits="bias", bias_std=2.5,
                             n_forced_empty=3)
+    if name == "custom_pair_3stage":
+        # d = 2048 with d_ff = 1024: four 22 KB pair stages no longer fit beside
+        # the resident A and the weight scales, so the pair plan takes three
+        # (scale buffers then released by their own barrier)
+        return synth.custom(T=320, d=2048, E=4, k=2, d_ff=1024, seed=12)
     if name == "custom_skew":
         return synth.custom(T=700, d=384, E=16, k=3, d_ff=384, seed=5, logits="bias", bias_std=3.0,
                             n_forced_empty=5)
@@ -153,7 +158,7 @@ def test_fc2_parity(orc, name, T):
     assert np.array_equal(g["out"], orc.reduce(g["slots"]))
 
 
-@pytest.mark.parametrize("name", ["small", "custom_skew", "custom_pair_skew"])
+@pytest.mark.parametrize("name", ["small", "custom_skew", "custom_pair_skew", "custom_pair_3stage"])
 def test_fc1_cta_pairs_equal_single(orc, name, monkeypatch):
     """FC1 on CTA pairs (cta_group::2 MMAs over 256-row units, the default
     where the pair plan fits) and on single CTAs produce the same bits: the

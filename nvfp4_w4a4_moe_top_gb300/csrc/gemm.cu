@@ -4,29 +4,30 @@
 // AI summary methodology: outer factors applied in FP32 after the native
 // block-scaled multiply, no decoded BF16 operand).
 //
-// Design (one persistent CTA per SM, 16 warps):
-//   warps 12-14  TMA producers.  A work unit is one 128-row tile of the
-//            routed rows (one expert).  Its A operand (128 rows x K FP4,
+// Design (one persistent CTA per SM; NE epilogue warps, NE = 16 in FC1 and 8
+// in FC2, then 4 scale writers, 3 producers and the MMA issuer):
+//   warps NE+4 .. NE+6  TMA producers.  A work unit is one 128-row tile of
+//            the routed rows (one expert).  Its A operand (128 rows x K FP4,
 //            128-byte swizzle) is loaded once into resident shared memory, one
 //            slice per 256 elements of K; the B operand (128 weight rows x 256
 //            elements of K) and the block-scale tiles of both operands stream
-//            through four rings of one or two stages, the k-steps dealt
-//            round-robin over the rings; producer warp p feeds the rings r
-//            with r % 3 == p, each ring from one warp in order.  When K does not fit,
-//            A streams through the stages too.
-//   warps 8-11  block-scale writers, one per tensor-memory lane quadrant.
-//            For each stage they move the scale tiles from shared to tensor
-//            memory with tcgen05.st: the B scales replicated in every
-//            quadrant (each quadrant of the tensor core reads all of them),
-//            the A scales only on the diagonal (row r is read from lane r,
-//            column base + r/32), and signal the stage's scales as ready.
-//   warp 15  MMA issuer: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X
+//            through three or four rings of one or two stages, the k-steps
+//            dealt round-robin over the rings; producer warp p feeds the rings
+//            r with r % 3 == p, each ring from one warp in order.  When K does
+//            not fit, A streams through the stages too.
+//   warps NE .. NE+3  block-scale writers, one per tensor-memory lane
+//            quadrant.  For each stage they move the scale tiles from shared
+//            to tensor memory with tcgen05.st: the B scales replicated in
+//            every quadrant (each quadrant of the tensor core reads all of
+//            them), the A scales only on the diagonal (row r is read from lane
+//            r, column base + r/32), and signal the stage's scales as ready.
+//   warp NE+7  MMA issuer: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X
 //            (M=128, N=128, K=64, UE4M3 scale per 16 elements) into one of
 //            the 128-column FP32 accumulators (three for FC1, two for FC2);
 //            nothing else goes through the tensor pipe.  Tensor memory after
 //            the accumulators holds one 32-column scale buffer per stage.
-//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and
-//            half (w/4) of the accumulator's columns, releases the
+//   warps 0 .. NE-1  epilogue: warp w reads TMEM lanes 32*(w%4).. (its 32
+//            rows) and part w/4 of the accumulator's columns, releases the
 //            accumulator, then does the FP32 epilogue from registers.  The
 //            expert's per-column outer scales are staged in shared memory per
 //            unit.

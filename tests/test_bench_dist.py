@@ -79,3 +79,22 @@ def test_aggregate_and_seeds():
     seeds = {bench.shard_seed(7, r) for r in range(8)}
     assert len(seeds) == 8 and bench.shard_seed(7, 0) == 7
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_source_hash_ignores_comments(tmp_path, monkeypatch):
+    """The kernel-source hash that keys bench.py's recorded ncu traffic: the
+    same for code that differs only in // comments and blank lines, different
+    for a changed statement."""
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "nvfp4_w4a4_moe_top_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+
+    def sha_of(text):
+        (csrc / "k.cu").write_text(text)
+        return bench.src_sha("k.cu")
+
+    base = sha_of("int f(int x) {\n  return x + 1;\n}\n")
+    assert sha_of("// a comment\nint f(int x) {  // trailing\n\n  return x + 1;   \n}\n") == base
+    assert sha_of("int f(int x) {\n  return x + 2;\n}\n") != base

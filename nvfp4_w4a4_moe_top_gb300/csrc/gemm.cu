@@ -1289,12 +1289,16 @@ static bool plan_pair(int K, int items, size_t scale_bytes, int* rings, size_t* 
   return false;
 }
 
-// Clusters of two that can be resident at once with `smem` bytes per CTA.
+// Clusters of two that can be resident at once with `smem` bytes per CTA
+// (the occupancy query is cached per host thread, keyed by device, kernel
+// and shared-memory size).
 static int pair_clusters(void (*kern)(const Fc1Args), size_t smem) {
-  static void (*cached_kern)(const Fc1Args) = nullptr;
-  static size_t cached_smem = 0;
-  static int cached = 0;
-  if (kern == cached_kern && smem == cached_smem) return cached;
+  thread_local void (*cached_kern)(const Fc1Args) = nullptr;
+  thread_local size_t cached_smem = 0;
+  thread_local int cached_dev = -1, cached = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (kern == cached_kern && smem == cached_smem && dev == cached_dev) return cached;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
   cfg.blockDim = dim3(Roles<FC1_NE>::THREADS);
@@ -1313,6 +1317,7 @@ static int pair_clusters(void (*kern)(const Fc1Args), size_t smem) {
   }
   cached_kern = kern;
   cached_smem = smem;
+  cached_dev = dev;
   cached = n;
   return n;
 }

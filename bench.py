@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per launch of the dominant kernel, from one ncu capture of the
 # source whose hash is recorded (profiles/fc1_dram_traffic_qwen64k.md); the
 # bench reports null once the kernel source differs.
-NCU_TRAFFIC = {"fc1": {"src_sha": "a0319916ec49b7d9", "bytes_per_launch": 1420742400 + 1044603648,
+NCU_TRAFFIC = {"fc1": {"src_sha": "f87f4f635117fde7", "bytes_per_launch": 1420742400 + 1044603648,
                        "workload": "qwen64k"}}
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe_nvfp4.so")
 SOURCES = ["abi.cu", "quant.cu", "route.cu", "gemm.cu", "bwd.cu", "noalloc.cu", "pipeline.cu"]
-HEADERS = ["common.cuh", "kernels.cuh", os.path.join("..", "..", "include", "moe_nvfp4.h")]
+HEADERS = ["common.cuh", "kernels.cuh", "swiglu.cuh", "exp_table.cuh", os.path.join("..", "..", "include", "moe_nvfp4.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -57,6 +57,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "swiglu.cuh"
 
 namespace moe {
 
@@ -725,18 +726,6 @@ __device__ __forceinline__ void teardown(Tail* tl) {
   }
 }
 
-// ---- approximate transcendentals for SiLU ----
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Two FP32 -> BF16x2 (lo = first argument), round to nearest even.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t r;
@@ -896,7 +885,6 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
     // one chunk after each chunk of unit i (the thread reads back only what
     // it wrote, so program order is the only ordering needed).
     uint4* scratch_cta = reinterpret_cast<uint4*>(args.scratch) + (size_t)blockIdx.x * 2 * (size_t)(d_ff / 8) * BM;
-    const float NLOG2E = -1.4426950408889634f;
     bool have_prev = false, ghost_prev = false;
     int64_t row_prev = 0;
     float g_prev = 0.0f, den_prev = 0.0f;
@@ -975,15 +963,14 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int nh = n0 + hh * 16;
+            // h = BF16(silu(u_gate) * u_up), rounded once; a row with g_x = 0
+            // (all-zero activations, pad rows) has u = +0 and so h = +0
             uint32_t hp[8];
+            if (ga != 0.0f) {
+              amax2 = __vmaxu2(amax2, swiglu16(ugw[hh], uuw[hh], hp));
+            } else {
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-              const uint32_t ugp = ugw[hh][w], uup = uuw[hh][w];
-              const float ug0 = bf16_lo(ugp), ug1 = bf16_hi(ugp);
-              const float s0 = ug0 * rcp_approx(1.0f + ex2_approx(ug0 * NLOG2E));
-              const float s1 = ug1 * rcp_approx(1.0f + ex2_approx(ug1 * NLOG2E));
-              hp[w] = bf16x2_rn(s0 * bf16_lo(uup), s1 * bf16_hi(uup));
-              amax2 = __vmaxu2(amax2, hp[w] & 0x7FFF7FFFu);
+              for (int w = 0; w < 8; ++w) hp[w] = 0u;
             }
             if (DBG && out && args.save_u) {  // 32-byte sectors: gate, then up
               uint4* sg4 = reinterpret_cast<uint4*>(args.save_u + row * 2 * d_ff + nh);

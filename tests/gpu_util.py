@@ -44,7 +44,9 @@ def build_test_so(name):
     out_dir = os.path.join(root, "_build")
     os.makedirs(out_dir, exist_ok=True)
     so = os.path.join(out_dir, "lib%s.so" % name)
-    if not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(src):
+    csrc = os.path.join(os.path.dirname(root), "nvfp4_w4a4_moe_top_gb300", "csrc")
+    deps = [src] + [os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith(".cuh")]
+    if not os.path.exists(so) or os.path.getmtime(so) < max(os.path.getmtime(d) for d in deps):
         subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
                         "-Xcompiler", "-fPIC", "-shared", src, "-o", so], check=True)
     return so

@@ -11,11 +11,13 @@
 //
 // The array is a file-scope device variable of MOE_PERMUTE_NOALLOC_SCRATCH_BYTES
 // (1 MiB): every GPU on which the library is loaded keeps it until the process
-// exits.  Host code cannot use the array's name as a device address, so the
-// first call on each device (with that device current) looks the address up
-// with cudaGetSymbolAddress, once, and every later call on that device reuses
-// it.  That first call may load the library's device code on the device, so
-// make it before any stream capture begins.
+// exits.  Host code cannot use the array's name as a device address, so every
+// call looks the address up on the current device with cudaGetSymbolAddress
+// (a table lookup once the device code is loaded).  The address is not kept
+// between calls: after a cudaDeviceReset the device code is loaded again and
+// the array may sit elsewhere, and a kept address would then point at freed
+// memory.  The first call on a device may load the library's device code on
+// that device, so make it before any stream capture begins.
 //
 // Every call shares the one array.  Calls whose work overlaps on the GPU (two
 // streams, or two host threads, at the same time) race on it and produce
@@ -32,30 +34,33 @@ static __device__ __align__(256) int32_t g_permute_noalloc_hist[MOE_PERMUTE_NOAL
 namespace {
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64];  // device address of the array, per device ordinal
+int g_noalloc_dev_ok[64];  // per device ordinal: 0 unknown, 1 compute capability 10.3, -1 other
 
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).
+// Device address of the scratch array on the current device.  The device
+// check is cached per ordinal (a reset does not change it); the address is
+// looked up on every call.
 int noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    int maj = 0, min = 0;
-    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    if (maj != 10 || min != 3) return MOE_ERR_DEVICE;
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_noalloc_hist);
-    if (e != cudaSuccess || p == nullptr) {
-      (void)cudaGetLastError();
-      return MOE_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_dev_ok[dev] == 0) {
+      int maj = 0, min = 0;
+      if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      g_noalloc_dev_ok[dev] = (maj == 10 && min == 3) ? 1 : -1;
     }
-    g_noalloc_addr[dev] = p;
+    if (g_noalloc_dev_ok[dev] < 0) return MOE_ERR_DEVICE;
   }
-  *out = g_noalloc_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_noalloc_hist);
+  if (e != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  *out = p;
   return MOE_OK;
 }
 

@@ -4,7 +4,11 @@ One step = one moe_expert_forward call (route, permute + amax + quantise,
 FC1 + SwiGLU + requantise, FC2 + router-weighted scatter, unpermute reduce)
 over the Qwen3-30B-A3B-shaped layer (T = 65536 tokens = 16 x 4096, d = 2048,
 E = 128, top-8, d_ff = 768, uniform router logits), inputs resident in HBM.
-Prints one JSON line.
+The timed steps are replays of one CUDA-graph capture of the forward.
+Prints one JSON line: the headline, each kernel against its roofline (CUDA
+events around each launch), the other Qwen-shaped and small workloads, the
+built next rows, end-to-end throughput with host buffers, and the CPU
+oracle.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...    # the CPU oracle as the reference arm
@@ -16,6 +20,7 @@ data path; timing is the max over ranks (weak scaling).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -23,6 +28,7 @@ import re
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -35,26 +41,31 @@ UNIT = "tokens/s"
 # cuBLAS peak times the nominal fp4:bf16 ratio (13.5 / 2.25 = 6).
 FP4_PER_BF16 = 6.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The seven launches of the forward, in order.
+KERNELS = ["route_kernel", "scan_kernel", "pad_rows_kernel", "permute_quant_kernel", "fc1_swiglu_kernel",
+           "fc2_scatter_kernel", "unpermute_reduce_kernel"]
 
-# DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed to the kernel source it was taken on; it is
-# reported only while that source is unchanged.  Filled from
-# profiles/*.md summaries.
-# DRAM bytes per launch of the dominant kernel, from one ncu capture of the
-# source whose hash is recorded (profiles/fc1_dram_traffic_qwen64k.md); the
-# bench reports null once the kernel source differs.
-NCU_TRAFFIC = {"fc1": {"src_sha": "f87f4f635117fde7", "bytes_per_launch": 1420742400 + 1044603648,
-                       "workload": "qwen64k"}}
+# DRAM traffic per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture), keyed to the hash of the
+# device code it was captured on and to the workload; reported as null once
+# either differs.
+NCU_TRAFFIC = {"fc1": {"src_sha": None, "bytes_per_launch": None, "workload": "qwen64k"}}
+# Host code follows this line in a source file; it is left out of the hash,
+# so a launcher edit keeps a capture of unchanged device code valid.
+HOST_MARKER = "// host launchers"
 
 
 def src_sha(*names):
-    """Hash of the sources' code: // comments, trailing blanks and blank lines
-    are left out, so a comment edit keeps a capture valid and any code
-    change invalidates it."""
+    """Hash of the sources' device code: everything up to a line holding
+    HOST_MARKER, with // comments, trailing blanks and blank lines left out,
+    so comment and host-code edits keep a capture valid and any change of
+    device code invalidates it."""
     h = hashlib.sha256()
     for n in names:
         with open(os.path.join(ROOT, "nvfp4_w4a4_moe_top_gb300", "csrc", n), encoding="utf-8") as f:
             for line in f:
+                if HOST_MARKER in line:
+                    break
                 code = re.sub(r"//.*", "", line).rstrip()
                 if code:
                     h.update(code.encode() + b"\n")
@@ -104,56 +115,115 @@ def aggregate(tokens_per_rank_step, steps, world, seconds_max):
 # --------------------------------------------------------------------------
 # clocks
 # --------------------------------------------------------------------------
+# NVML clock-event reason bits (nvml.h)
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
+    """SM clock and clock-event reasons of the GPU sampled during the timed
+    region: through NVML (read-only queries, every `period` seconds, in a
+    thread), else nvidia-smi at its fastest interval."""
+
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, index, uuid=None, period=0.002):
+        self.index, self.uuid, self.period = index, uuid, period
+        self.samples, self.max_mhz, self.source = [], None, None
         self.proc = None
-        self.path = os.path.join("/tmp", "moe_clocks_%d_%d.csv" % (os.getpid(), index))
+        self.stop = threading.Event()
+
+    def _nvml_open(self):
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = nv.nvmlDeviceGetHandleByUUID(("GPU-" + self.uuid).encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = nv.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) == 0
+        if not ok:
+            return None
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return nv, h
+
+    def _poll(self, nv, h):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and self.reason_fn(h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(self.period)
 
     def __enter__(self):
         try:
+            opened = self._nvml_open()
+        except OSError:
+            opened = None
+        if opened:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll, args=opened, daemon=True)
+            self.thread.start()
+            return self
+        self.path = os.path.join("/tmp", "moe_clocks_%d_%d.csv" % (os.getpid(), self.index))
+        try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *a):
-        if self.proc is not None:
+        if self.source == "nvml":
+            self.stop.set()
+            self.thread.join(timeout=5)
+        elif self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.f.close()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            bits = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+                    "sw_power_cap": 0x4}
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm = float(parts[1])
+                        self.max_mhz = float(parts[2])
+                    except ValueError:
+                        continue
+                    r = 0
+                    for n, v in zip(names, parts[5:9]):
+                        if v.lower().startswith("active"):
+                            r |= bits[n]
+                    self.samples.append((sm, r))
+            os.unlink(self.path)
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx = float(parts[2])
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no clock samples"], "samples": 0,
+                    "source": self.source}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in NVML_REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": self.source}
 
 
 # --------------------------------------------------------------------------
@@ -165,23 +235,115 @@ def make_inputs(lay, seed_rank):
     return rank_lay.x(), rank_lay.logits()
 
 
-def algorithmic(lay):
-    """Algorithmic work of one forward: routed rows only (no pad rows), the
-    method's own dataflow (x read once, codes written k times)."""
-    T, d, E, k, F = lay.T, lay.d, lay.E, lay.k, lay.d_ff
+def algorithmic(T, d, E, k, F):
+    """Algorithmic work of one forward per kernel: routed rows only (no pad
+    rows), the method's own dataflow (x read once, codes written k times)."""
     R = T * k
-    fc1_flops = 2.0 * R * d * 2 * F
-    fc2_flops = 2.0 * R * F * d
     fp4 = lambda rows, K: rows * (K / 2 + K / 16)            # codes + block scales
     w1 = fp4(E * 2 * F, d) + E * 2 * F * 4
     w2 = fp4(E * d, F) + E * d * 4
-    bytes_fc1 = fp4(R, d) + R * 4 + w1 + fp4(R, F) + R * 4       # A in, W1 in, h out
-    bytes_fc2 = fp4(R, F) + R * 4 + w2 + R * d * 2               # h in, W2 in, slots out
-    bytes_reduce = R * d * 2 + T * d * 2
-    bytes_quant = T * d * 2 + fp4(R, d) + R * 4                  # x in once, k copies out
-    bytes_route = T * E * 4 + R * 12
-    return dict(fc1_flops=fc1_flops, fc2_flops=fc2_flops, bytes_fc1=bytes_fc1, bytes_fc2=bytes_fc2,
-                bytes_reduce=bytes_reduce, bytes_quant=bytes_quant, bytes_route=bytes_route)
+    return dict(
+        fc1_flops=2.0 * R * d * 2 * F,
+        fc2_flops=2.0 * R * F * d,
+        bytes_route=T * E * 4 + R * 12,                          # logits in; ids, weights, ranks out
+        bytes_quant=T * d * 2 + fp4(R, d) + R * 4,               # x in once, k copies of codes, scales, g out
+        bytes_fc1=fp4(R, d) + R * 4 + w1 + fp4(R, F) + R * 4,    # A in, W1 in, h out
+        bytes_fc2=fp4(R, F) + R * 4 + w2 + R * d * 2,            # h in, W2 in, slots out
+        bytes_reduce=R * d * 2 + T * d * 2)                      # slots in, out
+
+
+class Forward:
+    """One workload's device buffers and its forward (eager, timed with
+    per-launch events, or captured once in a CUDA graph)."""
+
+    def __init__(self, M, dev, x, lg, T, E, k, d, F, w1q, w2q, stream):
+        import torch
+        self.M, self.dev, self.x, self.lg = M, dev, x, lg
+        self.T, self.E, self.k, self.d, self.F = T, E, k, d, F
+        self.w1q, self.w2q, self.stream = w1q, w2q, stream
+        self.out = torch.empty((T, d), dtype=torch.int16, device=dev)
+        self.ws = M.forward_workspace(T, E, k, d, F, dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    def args(self):
+        return (self.x, self.lg, self.T, self.E, self.k, self.d, self.F, self.w1q["codes"], self.w1q["sf"],
+                self.w1q["g"], self.w2q["codes"], self.w2q["sf"], self.w2q["g"], self.out, self.ws)
+
+    def eager(self):
+        self.M.moe_expert_forward(*self.args(), self.status, self.stream)
+
+    def timed(self, events):
+        self.M.moe_expert_forward_timed(*self.args(), self.status, self.stream, events)
+
+    def capture(self):
+        import torch
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self.eager()
+        self.graph = g
+
+    def replay(self):
+        self.graph.replay()
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        if int(self.status.item()) != 0:
+            raise RuntimeError("device status %#x" % int(self.status.item()))
+
+
+def graph_median_ms(fwd, reps):
+    """Median over `reps` graph replays, each between its own pair of
+    events on the launching stream."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(fwd.stream):
+        for a, b in ev:
+            a.record(fwd.stream)
+            fwd.replay()
+            b.record(fwd.stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def per_kernel_ms(fwd, reps):
+    """Mean device time of each of the forward's seven launches: events
+    recorded by the library before the first launch and after each one."""
+    import torch
+    sets = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(reps)]
+    for evs in sets:
+        fwd.timed(evs)
+    torch.cuda.synchronize()
+    return [statistics.fmean(evs[i].elapsed_time(evs[i + 1]) for evs in sets) for i in range(7)]
+
+
+def kernel_rooflines(ms, alg, peaks, fp4_peak):
+    """Each launch against the roofline that bounds it (achieved from the
+    algorithmic bytes or FLOPs of one launch over its mean duration)."""
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    for name, t in zip(KERNELS, ms):
+        out[name] = {"ms": round(t, 4)}
+    def mem(name, nbytes):
+        gbs = nbytes / (out[name]["ms"] * 1e-3) / 1e9
+        out[name].update(bound="hbm", achieved_gbs=round(gbs, 1), frac_hbm=round(gbs / hbm, 4),
+                         algorithmic_bytes=int(nbytes))
+    def flops(name, f):
+        tf = f / (out[name]["ms"] * 1e-3) / 1e12
+        out[name].update(achieved_tflops=round(tf, 1), frac_fp4_peak=round(tf / fp4_peak, 4),
+                         algorithmic_flops=int(f))
+    mem("route_kernel", alg["bytes_route"])
+    out["scan_kernel"]["bound"] = "latency"
+    out["pad_rows_kernel"]["bound"] = "latency"
+    mem("permute_quant_kernel", alg["bytes_quant"])
+    flops("fc1_swiglu_kernel", alg["fc1_flops"])
+    out["fc1_swiglu_kernel"]["bound"] = "tensor"
+    mem("fc2_scatter_kernel", alg["bytes_fc2"])
+    flops("fc2_scatter_kernel", alg["fc2_flops"])
+    mem("unpermute_reduce_kernel", alg["bytes_reduce"])
+    return out
 
 
 def tiny_latency(dev, reps=200):
@@ -201,14 +363,8 @@ def tiny_latency(dev, reps=200):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
 
     w1q, w2q = M.quantize_weights(to_dev(lay.w1())), M.quantize_weights(to_dev(lay.w2()))
-    x, lg = to_dev(lay.x()), to_dev(lay.logits())
-    out = torch.empty((T, d), dtype=torch.int16, device=dev)
-    ws = M.forward_workspace(T, E, k, d, F, dev)
     s = torch.cuda.Stream(dev)
-
-    def fwd():
-        M.moe_expert_forward(x, lg, T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"], w2q["sf"],
-                             w2q["g"], out, ws, None, s)
+    fwd = Forward(M, dev, to_dev(lay.x()), to_dev(lay.logits()), T, E, k, d, F, w1q, w2q, s)
 
     def per_call(fn):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -222,15 +378,51 @@ def tiny_latency(dev, reps=200):
         return e0.elapsed_time(e1) * 1e3 / reps
 
     with torch.cuda.stream(s):
-        fwd()
+        fwd.eager()
     torch.cuda.synchronize()
-    eager = per_call(fwd)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        fwd()
+    eager = per_call(fwd.eager)
+    fwd.capture()
     with torch.cuda.stream(s):  # replay() launches on the current stream
-        graph = per_call(g.replay)
+        graph = per_call(fwd.replay)
+    fwd.check()
     return {"workload": "tiny", "eager_us": round(eager, 2), "graph_us": round(graph, 2), "launches": 7}
+
+
+def other_config(M, dev, name, seed, rank, reps, w1q=None, w2q=None):
+    """Tokens/s of another workload (median of `reps` graph replays) with
+    its per-kernel times; Qwen-shaped workloads reuse the headline's
+    quantised weights (the same seeded weights)."""
+    import numpy as np
+    import torch
+
+    import synth
+    lay = synth.layer(name, seed=seed)
+    T, E, k, d, F = lay.T, lay.E, lay.k, lay.d, lay.d_ff
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    if w1q is None:
+        w1q = M.quantize_weights(to_dev(lay.w1()))
+        w2q = M.quantize_weights(to_dev(lay.w2()))
+    x_np, lg_np = make_inputs(lay, shard_seed(seed, rank))
+    s = torch.cuda.current_stream(dev)
+    fwd = Forward(M, dev, to_dev(x_np), to_dev(lg_np), T, E, k, d, F, w1q, w2q, s)
+    for _ in range(3):
+        fwd.eager()
+    fwd.check()
+    fwd.capture()
+    med = graph_median_ms(fwd, reps)
+    ms = per_kernel_ms(fwd, max(5, reps // 5))
+    fwd.check()
+    counts = M.forward_views(fwd.ws, T, E, k, d, F)["counts"].cpu().numpy()
+    alg = algorithmic(T, d, E, k, F)
+    return {"workload": name, "T": T, "d": d, "E": E, "k": k, "d_ff": F,
+            "value": round(T / (med * 1e-3), 1), "unit": UNIT, "ms_median_graph": round(med, 4),
+            "forward_tflops": round((alg["fc1_flops"] + alg["fc2_flops"]) / (med * 1e-3) / 1e12, 1),
+            "kernel_ms": {n: round(t, 4) for n, t in zip(KERNELS, ms)},
+            "empty_experts": int((counts == 0).sum()), "max_group_rows": int(counts.max())}
 
 
 def native(args):
@@ -247,6 +439,8 @@ def native(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    # one non-default stream for all the work (graph capture needs one)
+    torch.cuda.set_stream(torch.cuda.Stream(dev))
     B.build()
     lay = synth.layer(args.workload, seed=args.seed)
     T, E, k, d, F = lay.T, lay.E, lay.k, lay.d, lay.d_ff
@@ -263,30 +457,32 @@ def native(args):
     w1e, w2e = M.quantize_weights_per_expert(W1), M.quantize_weights_per_expert(W2)
     x_np, lg_np = make_inputs(lay, shard_seed(args.seed, rank))
     x, lg = to_dev(x_np), to_dev(lg_np)
-    out = torch.empty((T, d), dtype=torch.int16, device=dev)
-    ws = M.forward_workspace(T, E, k, d, F, dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        M.moe_expert_forward(x, lg, T, E, k, d, F, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"], w2q["sf"],
-                             w2q["g"], out, ws, status, stream)
+    fwd = Forward(M, dev, x, lg, T, E, k, d, F, w1q, w2q, stream)
+    out, ws, status = fwd.out, fwd.ws, fwd.status
 
     for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError("device status %#x" % int(status.item()))
+        fwd.eager()
+    fwd.check()
+    fwd.capture()
+    for _ in range(3):
+        fwd.replay()
+    fwd.check()
 
-    # ---- headline: K forwards on resident inputs, device-timed ----
+    # ---- headline: K graph replays of the forward on resident inputs,
+    # device-timed on the launching stream ----
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        uuid = None
+    with ClockSampler(local, uuid) as clk:
         ev0.record(stream)
         for _ in range(args.steps):
-            step()
+            fwd.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -295,13 +491,46 @@ def native(args):
     sec_max = max_over_ranks(sec, world, dev)
     value = aggregate(T, args.steps, world, sec_max)
     clocks = clk.summary()
+    fwd.check()
+    median_ms = graph_median_ms(fwd, max(50, min(args.steps, 200)))
 
-    # ---- per-kernel durations of the dominant kernels (same stream, same
-    # inputs, events around the one launch each entry point makes) ----
-    v = M.forward_views(ws, T, E, k, d, F)
-    mc = v["m_cap"]
-    f1ws = ws[M.forward_workspace_layout(T, E, k, d, F)["fc1_staging"]:]
-    hq = M.empty_quantized(mc, F, dev)
+    # ---- each launch of the forward against its roofline ----
+    peaks, peak_kind = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
+    alg = algorithmic(T, d, E, k, F)
+    kms = per_kernel_ms(fwd, max(10, min(args.steps, 50)))
+    fwd.check()
+    kernels = kernel_rooflines(kms, alg, peaks, fp4_peak)
+    t_fc1 = kms[KERNELS.index("fc1_swiglu_kernel")] * 1e-3
+    fc1_tflops = alg["fc1_flops"] / t_fc1 / 1e12
+    sha = src_sha("gemm.cu", "common.cuh", "swiglu.cuh")
+    tr = NCU_TRAFFIC.get("fc1")
+    # ncu's DRAM bytes of one launch, valid only for the device code and the
+    # workload they were captured on
+    traffic = (tr["bytes_per_launch"] if tr and tr.get("src_sha") == sha and tr.get("workload") == args.workload
+               else None)
+    roofline = {"kernel": "fc1_swiglu_kernel", "bound": "tensor", "achieved": round(fc1_tflops, 1),
+                "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(fc1_tflops / fp4_peak, 4),
+                "traffic": traffic, "ms_per_launch": round(t_fc1 * 1e3, 4), "src_sha": sha,
+                "algorithmic_bytes": int(alg["bytes_fc1"]),
+                "peak_source": "%s bf16 burst x %g (nominal fp4:bf16)" % (peak_kind, FP4_PER_BF16)}
+    fwd_sec = sec_max / args.steps
+    forward = {"tflops": round((alg["fc1_flops"] + alg["fc2_flops"]) / fwd_sec / 1e12, 1),
+               "frac_fp4_peak": round((alg["fc1_flops"] + alg["fc2_flops"]) / fwd_sec / 1e12 / fp4_peak, 4),
+               "algorithmic_gb": round(sum(alg[n] for n in ["bytes_route", "bytes_quant", "bytes_fc1", "bytes_fc2",
+                                                           "bytes_reduce"]) / 1e9, 3),
+               "hbm_gbs_of_algorithmic_bytes": round(sum(alg[n] for n in ["bytes_route", "bytes_quant", "bytes_fc1",
+                                                                        "bytes_fc2", "bytes_reduce"])
+                                                    / fwd_sec / 1e9, 1)}
+
+    # ---- the other workloads of the layer ----
+    configs = {}
+    if args.workload == "qwen64k":
+        configs["qwen16k"] = other_config(M, dev, "qwen16k", args.seed, rank, 50, w1q, w2q)
+    configs["small"] = other_config(M, dev, "small", args.seed, rank, 50)
+
+    # ---- weight quantisation (once per optimizer step, outside the forward):
+    # the per-row recipe and the per-expert recipe, W1 and W2 each call ----
     reps = max(5, min(args.steps, 50))
 
     def timed(fn):
@@ -315,18 +544,6 @@ def native(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3 / reps
 
-    t_fc1 = timed(lambda: M.nvfp4_grouped_gemm_fc1_swiglu(
-        v["x_codes"], v["x_sf"], v["x_g"], v["offsets"], E, mc, d, F, w1q["codes"], w1q["sf"], w1q["g"],
-        hq["codes"], hq["sf"], hq["g"], None, None, f1ws, status, stream))
-    slots2 = v["slots"]
-    t_fc2r = timed(lambda: M.nvfp4_grouped_gemm_fc2_unpermute(
-        v["h_codes"], v["h_sf"], v["h_g"], v["offsets"], E, mc, F, d, w2q["codes"], w2q["sf"], w2q["g"],
-        v["row_to_token"], v["token_slot_row"], v["topk_w"], T, k, slots2, out, None, status, stream))
-
-    peaks, peak_kind = load_peaks()
-
-    # ---- weight quantisation (once per optimizer step, outside the forward):
-    # the per-row recipe and the per-expert recipe, W1 and W2 each call ----
     def quant_rows():
         M.moe_nvfp4_quantize_weights(W1, w1q["codes"], w1q["sf"], w1q["g"], status, stream)
         M.moe_nvfp4_quantize_weights(W2, w2q["codes"], w2q["sf"], w2q["g"], status, stream)
@@ -370,8 +587,7 @@ def native(args):
     t_ftrain = timed(fwd_train)
     t_bwd = timed(bwd)
     t_fb = timed(lambda: (fwd_train(), bwd()))
-    alg0 = algorithmic(lay)
-    bwd_flops = 2.0 * (alg0["fc1_flops"] + alg0["fc2_flops"])  # dgrad + wgrad of both GEMMs
+    bwd_flops = 2.0 * (alg["fc1_flops"] + alg["fc2_flops"])  # dgrad + wgrad of both GEMMs
     del W1, W2, su, sh, bws, gW1, gW2
     latency = tiny_latency(dev)
     fb = {"value": round(T / t_fb, 1), "unit": UNIT, "ms_per_step": round(t_fb * 1e3, 4),
@@ -391,24 +607,6 @@ def native(args):
                                             "ms_per_step": round(t_fwd_gather * 1e3, 4),
                                             "note": "codes quantised once per token, FC1 A rows by tile::gather4"},
                  "algorithmic_bytes_weight_quant": int(wq_bytes), "forward_backward": fb}
-    alg = algorithmic(lay)
-    fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
-    fc1_tflops = alg["fc1_flops"] / t_fc1 / 1e12
-    sha = src_sha("gemm.cu", "common.cuh")
-    tr = NCU_TRAFFIC.get("fc1")
-    # ncu's DRAM bytes of one launch, valid only for the kernel source and the
-    # workload they were captured on
-    traffic = (tr["bytes_per_launch"] if tr and tr.get("src_sha") == sha and tr.get("workload") == args.workload
-               else None)
-    roofline = {"kernel": "fc1_swiglu_kernel", "bound": "tensor", "achieved": round(fc1_tflops, 1),
-                "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(fc1_tflops / fp4_peak, 4),
-                "traffic": traffic, "ms_per_launch": round(t_fc1 * 1e3, 4),
-                "peak_source": "%s bf16 burst x %g (nominal fp4:bf16)" % (peak_kind, FP4_PER_BF16)}
-    fc2_gbs = (alg["bytes_fc2"] + alg["bytes_reduce"]) / t_fc2r / 1e9
-    roofline_hbm = {"kernel": "fc2_scatter_kernel + unpermute_reduce_kernel", "bound": "hbm",
-                    "achieved": round(fc2_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(fc2_gbs / peaks["hbm_gbs"], 4), "ms_per_launch": round(t_fc2r * 1e3, 4),
-                    "peak_source": peak_kind}
 
     # ---- end to end through the public call with host buffers ----
     xh = torch.from_numpy(x_np.view(np.int16)).pin_memory()
@@ -419,7 +617,7 @@ def native(args):
     def e2e_step():
         x.copy_(xh, non_blocking=True)
         lg.copy_(lgh, non_blocking=True)
-        step()
+        fwd.eager()
         outh.copy_(out, non_blocking=True)
 
     e2e_step()
@@ -449,23 +647,28 @@ def native(args):
            "api": "moe_pipeline_submit (copy-in, forward, copy-out on three streams, depth 2)",
            "serial_value": round(aggregate(T, e2e_steps, world, max_over_ranks(e2e_serial_sec, world, dev)), 1),
            "h2d_bytes_per_step": int(xh.numel() * 2 + lgh.numel() * 4), "d2h_bytes_per_step": int(outh.numel() * 2)}
-    if int(status.item()) != 0:
-        raise RuntimeError("device status %#x" % int(status.item()))
+    fwd.check()
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(sec_max / args.steps * 1e3, 4), "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": round(sec_max / args.steps * 1e3, 4),
+            "ms_median_graph": round(median_ms, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate, bf16 out)",
             "data": "synthetic (seeded; shapes and distributions of the Qwen3-30B-A3B expert layer)",
-            "config": {"workload": args.workload, "T": T, "d": d, "E": E, "k": k, "d_ff": F,
-                       "parallelism": "token data parallel x%d" % world, "l2": "inputs larger than L2 (no flush)"},
-            "gpu_launches": 7 * args.steps, "roofline": roofline, "roofline_hbm": roofline_hbm,
-            "clocks": clocks, "e2e": e2e, "next_rows": next_rows, "latency_tiny": latency}
+            "config": config_of(args.workload, lay, world),
+            "gpu_launches": 7 * args.steps, "roofline": roofline, "kernels": kernels, "forward": forward,
+            "clocks": clocks, "e2e": e2e, "configs": configs, "next_rows": next_rows, "latency_tiny": latency}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(lay, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def config_of(workload, lay, world):
+    return {"workload": workload, "T": lay.T, "d": lay.d, "E": lay.E, "k": lay.k, "d_ff": lay.d_ff,
+            "parallelism": "token data parallel x%d" % world,
+            "l2": "inputs larger than L2 (no flush)", "timing": "CUDA-graph replays, CUDA events"}
 
 
 # --------------------------------------------------------------------------
@@ -497,7 +700,9 @@ def cpu_baseline(lay, args, tokens=None):
 
 def reference(args):
     """The oracle as the reference arm: W untimed + K timed steps, each step a
-    bounded sample (args.ref_tokens consecutive tokens) of the same workload."""
+    bounded sample (n consecutive tokens) of the same workload.  n is the
+    cpu_baseline's 1024 tokens unless the whole run would then pass about
+    three minutes, in which case it shrinks to fit (not below 256)."""
     import oracle
     import synth
     rank, world, _ = dist_env()
@@ -505,27 +710,32 @@ def reference(args):
         return
     lay = synth.layer(args.workload, seed=args.seed)
     w1q, w2q = oracle_weights(lay)
-    n = args.ref_tokens
 
-    def step(i):
+    def step(i, n):
         t0 = (i * n) % lay.T
         toks = [(t0 + j) % lay.T for j in range(n)]
         oracle.moe_forward(lay.x_rows(toks), lay.logits_rows(toks), w1q, w2q, lay.k, lay.d_ff)
 
+    n = args.ref_tokens
+    if n is None:
+        t0 = time.perf_counter()
+        step(0, 256)
+        per_tok = (time.perf_counter() - t0) / 256
+        n = int(max(256, min(1024, 180.0 / max(per_tok, 1e-9) / (args.steps + args.warmup))))
+        n = min(n, lay.T)
     for i in range(args.warmup):
-        step(i)
+        step(i, n)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        step(args.warmup + i)
+        step(args.warmup + i, n)
     sec = time.perf_counter() - t0
     value = n * args.steps / sec
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (oracle)",
-            "data": "synthetic (seeded)",
-            "config": {"workload": args.workload, "T": lay.T, "d": lay.d, "E": lay.E, "k": lay.k, "d_ff": lay.d_ff},
+            "data": "synthetic (seeded)", "config": config_of(args.workload, lay, world),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
-                             "kind": "oracle", "sample": "%d tokens per step" % n},
+                             "kind": "oracle", "sample": "%d consecutive tokens per step" % n},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -539,7 +749,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen64k")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-tokens", type=int, default=1024)
-    ap.add_argument("--ref-tokens", type=int, default=4)
+    ap.add_argument("--ref-tokens", type=int, default=None,
+                    help="tokens per reference step (default: 1024, fewer if the run would be long)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -34,8 +34,9 @@
  *     nibble; sign of a zero code = sign of the quotient.
  *   FC1: y = acc*(g_x*g_w) in FP32, u = BF16(y); gate = columns [0,d_ff),
  *     up = [d_ff, 2 d_ff); h = BF16(silu(gate)*up); h requantised per row.
- *   FC2: y2 = acc*(g_h*g_w2) in FP32; z = BF16(w_{t,e}*y2) stored at slot
- *     (t, j); out[t] = BF16(sum_j FP32(z_j)) in ascending j.
+ *   FC2: y2 = acc*(g_h*g_w2) in FP32; z = BF16(w_{t,e}*y2) stored as slot
+ *     (t, j), which lives at row token_slot_row[t][j] of the z rows;
+ *     out[t] = BF16(sum_j FP32(z_j)) in ascending j.
  *
  * Conventions for every entry point:
  *   - Tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned
@@ -121,8 +122,9 @@ size_t moe_expert_backward_workspace_bytes(int T, int E, int k, int d, int d_ff)
  * 1 topk_w f32[T][k], 2 token_slot_row i32[T][k], 3 counts i32[E],
  * 4 offsets i32[E+1], 5 row_to_token i32[M_cap], 6 amax_tok f32[T],
  * 7 x_codes u8[M_cap][d/2], 8 x_sf, 9 x_g f32[M_cap], 10 h_codes
- * u8[M_cap][d_ff/2], 11 h_sf, 12 h_g f32[M_cap], 13 slots bf16[T][k][d],
- * 14 chunk histograms, 15 FC1 staging).  Writes 16 entries; returns 0. */
+ * u8[M_cap][d_ff/2], 11 h_sf, 12 h_g f32[M_cap], 13 z rows bf16[M_cap][d]
+ * (slot (t, j) at row token_slot_row[t][j]), 14 chunk histograms, 15 FC1
+ * staging).  Writes 16 entries; returns 0. */
 int moe_expert_forward_workspace_layout(int T, int E, int k, int d, int d_ff,
                                         size_t offsets_out[16]);
 
@@ -205,12 +207,14 @@ int moe_permute_amax(const float* logits, const int32_t* ext_ids,
  * MOE_ERR_WORKSPACE before any CUDA call (with 1 MiB: T up to 524288 tokens
  * at E = 128, 65536 at E = 1024).
  *
- * The first call on a device, with that device current, looks up the
- * array's device address (cudaGetSymbolAddress, once per device); make that
- * first call before any stream capture.  All calls share the one array, so
- * calls whose GPU work overlaps (other streams or host threads at the same
- * time) race and give wrong results: serialise them.  The array needs no
- * clearing between calls. */
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress); no address is kept between calls, so a
+ * cudaDeviceReset in the process, after which the array may sit elsewhere,
+ * does not leave a stale pointer.  The first call on a device may load the
+ * library's device code there: make it before any stream capture.  All
+ * calls share the one array, so calls whose GPU work overlaps (other streams
+ * or host threads at the same time) race and give wrong results: serialise
+ * them.  The array needs no clearing between calls. */
 #define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1 << 20)
 int moe_permute_amax_noalloc(const float* logits, const int32_t* ext_ids,
                              const float* ext_w, const uint16_t* x, int T,
@@ -260,14 +264,18 @@ int nvfp4_grouped_gemm_fc1_swiglu(
     uint8_t* h_codes, uint8_t* h_sf, float* h_g, float* dbg_u_f32,
     uint16_t* dbg_h, void* ws, size_t ws_bytes, int* status, void* stream);
 
-/* Grouped FC2 with the router-weighted scatter epilogue, then the unpermute
- * reduce (two launches).  z = BF16(topk_w[t][j] * (acc * (g_h * g_w2))) goes
- * to slots[t][j][:], then out[t] = BF16(sum_j FP32(slots[t][j])) in ascending
- * j (= ascending expert id).
+/* Grouped FC2 with the router-weighted epilogue, then the unpermute reduce
+ * (two launches).  z = BF16(topk_w[t][j] * (acc * (g_h * g_w2))) of routed
+ * row r = token_slot_row[t][j] goes to row r of `slots` (the slot (t, j) of
+ * the combine, kept in routed-row order so that each 128-row tile leaves
+ * the GEMM with whole-tile tensor stores), then out[t] = BF16(sum_j
+ * FP32(slots[token_slot_row[t][j]])) in ascending j (= ascending expert
+ * id).
  *   h_codes/h_sf/h_g  M_cap rows of K = d_ff
  *   w2_codes/w2_sf/w2_g from moe_nvfp4_quantize_weights(W2, E, d, d_ff)
  *   row_to_token, token_slot_row, topk_w from moe_permute_amax
- *   slots      bf16 [T][k][d] (workspace, also an output)
+ *   slots      bf16 [M_cap][d] (workspace, also an output): z by routed
+ *              row; pad rows are written as zeros
  *   out        bf16 [T][d] (out)
  *   dbg_y_f32  f32 [M_cap][d] pre-weighting expert outputs y2, or NULL */
 int nvfp4_grouped_gemm_fc2_unpermute(
@@ -280,8 +288,9 @@ int nvfp4_grouped_gemm_fc2_unpermute(
 
 /* The whole expert forward: route, permute + amax + quantise (x read once),
  * FC1 + SwiGLU + requantise, FC2 + router-weighted scatter, unpermute
- * reduce.  Six launches on `stream`, no host synchronisation (capturable in
- * a CUDA graph).
+ * reduce.  Seven launches on `stream` (route, chunk scan, pad rows, permute +
+ * quantise, FC1, FC2, reduce), no host synchronisation (capturable in a CUDA
+ * graph).
  *   x       bf16 [T][d];  logits f32 [T][E]
  *   w1_*, w2_* quantised weights as above
  *   out     bf16 [T][d] (out)
@@ -293,6 +302,22 @@ int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E,
                        const uint8_t* w2_codes, const uint8_t* w2_sf,
                        const float* w2_g, uint16_t* out, void* ws,
                        size_t ws_bytes, int* status, void* stream);
+
+/* moe_expert_forward that also records eight caller-owned CUDA events on
+ * `stream` (cudaEvent_t handles passed as void*, created by the caller with
+ * timing enabled): events[0] before the first launch and events[i] after the
+ * i-th of the seven launches (route, chunk scan, pad rows, permute +
+ * quantise, FC1, FC2, reduce), so that the caller can time each kernel on the
+ * launching stream.  Same kernels, arguments, workspace and results as
+ * moe_expert_forward (the pages have no counterpart: it serves measurement).
+ * MOE_ERR_POINTER if events or one of its eight entries is NULL. */
+int moe_expert_forward_timed(const uint16_t* x, const float* logits, int T,
+                             int E, int k, int d, int d_ff,
+                             const uint8_t* w1_codes, const uint8_t* w1_sf,
+                             const float* w1_g, const uint8_t* w2_codes,
+                             const uint8_t* w2_sf, const float* w2_g,
+                             uint16_t* out, void* ws, size_t ws_bytes,
+                             int* status, void* stream, void* const* events);
 
 /* moe_expert_forward with gather-on-load FC1, a step toward the single-pass
  * fusion the pages name as future work (AI summary, "Future Directions":

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_pipeline_submit": (I32, [P, P, P, P, P, P, P, P, P, P, P]),
     "moe_pipeline_synchronize": (I32, [P]),
     "moe_pipeline_destroy": (I32, [P]),
+    "moe_expert_forward_timed": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P, P]),
     "moe_expert_forward_gather": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P]),
     "moe_expert_forward_train": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, SZ, P, P, P, P]),
     "moe_expert_backward_workspace_bytes": (SZ, [I32, I32, I32, I32, I32]),
@@ -193,6 +194,10 @@ def nvfp4_grouped_gemm_fc1_swiglu(a_codes, a_sf, a_g, offsets, E, M_cap, d, d_ff
 def nvfp4_grouped_gemm_fc2_unpermute(h_codes, h_sf, h_g, offsets, E, M_cap, d_ff, d, w2_codes, w2_sf, w2_g,
                                      row_to_token, token_slot_row, topk_w, T, k, slots, out, dbg_y_f32,
                                      status=None, stream=None):
+    """slots: the z rows, bf16 [M_cap][d] (the kernel stores whole 128-row
+    tiles there)."""
+    if T > 0 and slots.numel() * slots.element_size() < M_cap * d * 2:
+        raise ValueError("slots must hold M_cap x d bf16 values")
     _check("nvfp4_grouped_gemm_fc2_unpermute", lib().nvfp4_grouped_gemm_fc2_unpermute(
         _p(h_codes), _p(h_sf), _p(h_g), _p(offsets), E, M_cap, d_ff, d, _p(w2_codes), _p(w2_sf), _p(w2_g),
         _p(row_to_token), _p(token_slot_row), _p(topk_w), T, k, _p(slots), _p(out), _p(dbg_y_f32),
@@ -205,6 +210,24 @@ def moe_expert_forward(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_co
         _p(x), _p(logits), T, E, k, d, d_ff, _p(w1_codes), _p(w1_sf), _p(w1_g), _p(w2_codes), _p(w2_sf),
         _p(w2_g), _p(out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
         _s(stream)))
+
+
+def moe_expert_forward_timed(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws,
+                             status=None, stream=None, events=None):
+    """moe_expert_forward recording the eight torch.cuda.Event objects in
+    `events` (timing enabled) around its seven launches on the stream."""
+    import torch
+    if events is None or len(events) != 8:
+        raise ValueError("events: eight torch.cuda.Event objects")
+    s = torch.cuda.current_stream() if stream is None else stream
+    for e in events:  # the handle exists once the event has been recorded
+        if e.cuda_event == 0:
+            e.record(s)
+    arr = (ctypes.c_void_p * 8)(*[e.cuda_event for e in events])
+    _check("moe_expert_forward_timed", lib().moe_expert_forward_timed(
+        _p(x), _p(logits), T, E, k, d, d_ff, _p(w1_codes), _p(w1_sf), _p(w1_g), _p(w2_codes), _p(w2_sf),
+        _p(w2_g), _p(out), _p(ws), 0 if ws is None else ws.numel() * ws.element_size(), _p(status),
+        _s(stream), ctypes.cast(arr, P)))
 
 
 def moe_expert_forward_gather(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws,
@@ -333,4 +356,4 @@ def forward_views(ws, T, E, k, d, d_ff):
         amax_tok=v("amax_tok", torch.float32, (T,)), x_codes=v("x_codes", torch.uint8, (mc, d // 2)),
         x_sf=v("x_sf", torch.uint8, (sf_bytes(mc, d),)), x_g=v("x_g", torch.float32, (mc,)),
         h_codes=v("h_codes", torch.uint8, (mc, d_ff // 2)), h_sf=v("h_sf", torch.uint8, (sf_bytes(mc, d_ff),)),
-        h_g=v("h_g", torch.float32, (mc,)), slots=v("slots", torch.int16, (T, k, d)), m_cap=mc)
+        h_g=v("h_g", torch.float32, (mc,)), slots=v("slots", torch.int16, (mc, d)), m_cap=mc)

@@ -135,8 +135,8 @@ FwdLayout fwd_layout(int T, int E, int k, int d, int d_ff) {
   const size_t sizes[16] = {
       (size_t)T * k * 4, (size_t)T * k * 4, (size_t)T * k * 4, (size_t)E * 4, (size_t)(E + 1) * 4, (size_t)mc * 4,
       (size_t)T * 4,     (size_t)mc * (d / 2), sf_bytes_of(mc, d), (size_t)mc * 4, (size_t)mc * (d_ff / 2),
-      sf_bytes_of(mc, d_ff), (size_t)mc * 4, (size_t)T * k * d * 2, (size_t)C * E * 4,
-      (size_t)moe::kMaxGemmCtas * 2 * 128 * d_ff * 2};
+      sf_bytes_of(mc, d_ff), (size_t)mc * 4, (size_t)mc * d * 2, (size_t)C * E * 4,
+      moe::fc1_workspace_bytes(d_ff)};
   FwdLayout L;
   size_t o = 0;
   for (int i = 0; i < 16; ++i) {
@@ -170,7 +170,8 @@ BwdLayout bwd_layout(int T, int E, int k, int d, int d_ff) {
 int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
                  const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g, const uint8_t* w2_codes,
                  const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, uint16_t* save_u,
-                 uint16_t* save_h, float* save_y2, bool gather, int* status, void* stream);
+                 uint16_t* save_h, float* save_y2, bool gather, int* status, void* stream,
+                 void* const* events = nullptr);
 
 }  // namespace
 
@@ -207,7 +208,7 @@ size_t moe_permute_workspace_bytes(int T, int E) {
 
 size_t nvfp4_fc1_workspace_bytes(int d_ff) {
   if (d_ff < 128 || d_ff % 128 != 0) return 0;
-  return (size_t)moe::kMaxGemmCtas * 2 * 128 * d_ff * 2;
+  return moe::fc1_workspace_bytes(d_ff);
 }
 
 size_t moe_expert_forward_workspace_bytes(int T, int E, int k, int d, int d_ff) {
@@ -348,10 +349,11 @@ int nvfp4_grouped_gemm_fc2_unpermute(const uint8_t* h_codes, const uint8_t* h_sf
   a.a_sf = h_sf; a.a_g = h_g; a.w_sf = w2_sf; a.w_g = w2_g; a.offsets = offsets;
   a.E = E; a.d_ff = d_ff; a.d = d; a.k = k;
   a.row_to_token = row_to_token; a.token_slot_row = token_slot_row; a.topk_w = topk_w;
-  a.slots = slots; a.dbg_y = dbg_y_f32; a.status = status;
+  a.dbg_y = dbg_y_f32; a.status = status;
+  if (encode_bf16(&a.tmap_out, slots, M_cap, d, 32) != MOE_OK) return MOE_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   if (moe::launch_fc2(a, M_cap, s) != 0) return MOE_ERR_CUDA;
-  moe::launch_unpermute_reduce(slots, T, k, d, out, s);
+  moe::launch_unpermute_reduce(slots, token_slot_row, T, k, d, out, s);
   return finish();
 }
 
@@ -361,6 +363,17 @@ int moe_expert_forward(const uint16_t* x, const float* logits, int T, int E, int
                        void* stream) {
   return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
                       nullptr, nullptr, nullptr, false, status, stream);
+}
+
+int moe_expert_forward_timed(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
+                             const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g,
+                             const uint8_t* w2_codes, const uint8_t* w2_sf, const float* w2_g, uint16_t* out,
+                             void* ws, size_t ws_bytes, int* status, void* stream, void* const* events) {
+  if (events == nullptr) return MOE_ERR_POINTER;
+  for (int i = 0; i < 8; ++i)
+    if (events[i] == nullptr) return MOE_ERR_POINTER;
+  return forward_impl(x, logits, T, E, k, d, d_ff, w1_codes, w1_sf, w1_g, w2_codes, w2_sf, w2_g, out, ws, ws_bytes,
+                      nullptr, nullptr, nullptr, false, status, stream, events);
 }
 
 int moe_expert_forward_gather(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
@@ -430,7 +443,8 @@ int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int
   a2.a_sf = h_sf; a2.a_g = h_g; a2.w_sf = w2_sf; a2.w_g = w2_g; a2.offsets = offsets;
   a2.E = E; a2.d_ff = F; a2.d = d; a2.k = k;
   a2.row_to_token = row_to_token; a2.token_slot_row = token_slot_row; a2.topk_w = topk_w;
-  a2.dY = dY; a2.dy2 = dy2; a2.dw = dw; a2.status = status;
+  a2.dY = dY; a2.dw = dw; a2.status = status;
+  if (encode_bf16(&a2.tmap_out, dy2, mc, d, 32) != MOE_OK) return MOE_ERR_CUDA;
   if (moe::launch_fc2(a2, mc, s) != 0) return MOE_ERR_CUDA;
   moe::launch_bwd_xrows(x, row_to_token, offsets, E, T, d, mc, xp, s);
   if (dlogits) moe::launch_bwd_logits(dw, topk_w, topk_ids, T, E, k, dlogits, s);
@@ -478,7 +492,7 @@ namespace {
 int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, int d, int d_ff,
                  const uint8_t* w1_codes, const uint8_t* w1_sf, const float* w1_g, const uint8_t* w2_codes,
                  const uint8_t* w2_sf, const float* w2_g, uint16_t* out, void* ws, size_t ws_bytes, uint16_t* save_u,
-                 uint16_t* save_h, float* save_y2, bool gather, int* status, void* stream) {
+                 uint16_t* save_h, float* save_y2, bool gather, int* status, void* stream, void* const* events) {
   if (!ok_model_shape(T, E, k, d, d_ff)) return MOE_ERR_SHAPE;
   if (!ok_ptr(w1_codes) || !ok_ptr(w1_sf) || !ok_ptr(w1_g) || !ok_ptr(w2_codes) || !ok_ptr(w2_sf) || !ok_ptr(w2_g) ||
       !ok_opt(status))
@@ -509,15 +523,24 @@ int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, in
   uint16_t* scratch = reinterpret_cast<uint16_t*>(w + L.off[15]);
   const int64_t mc = m_cap_of(T, E, k);
   const int C = (T + kRouteChunk - 1) / kRouteChunk;
+  // caller-owned events recorded before the first launch and after each
+  auto mark = [&](int i) {
+    if (events) (void)cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s);
+  };
 
+  mark(0);
   moe::launch_route(logits, nullptr, nullptr, T, E, k, topk_ids, topk_w, tsr, hist, status, s);
+  mark(1);
   moe::launch_scan(hist, C, E, counts, offsets, s);
+  mark(2);
   // gather: x_codes holds the codes once per token (rows 0..T-1) and a zero
   // row T, which the pad rows gather; otherwise one copy per routed row
   moe::launch_pad_rows(offsets, counts, E, mc, r2t, nullptr, gather ? nullptr : x_codes, d, x_sf, x_g, s);
+  mark(3);
   if (moe::launch_permute_quant(topk_ids, tsr, hist, offsets, T, E, k, x, d, r2t, amax_tok, gather ? nullptr : x_codes,
                                 gather ? x_codes : nullptr, x_sf, x_g, status, s) != 0)
     return MOE_ERR_CUDA;
+  mark(4);
 
   moe::Fc1Args a1;
   std::memset(&a1, 0, sizeof(a1));
@@ -534,6 +557,7 @@ int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, in
   a1.h_codes = h_codes; a1.h_sf = h_sf; a1.h_g = h_g; a1.scratch = scratch; a1.status = status;
   a1.save_u = save_u; a1.dbg_h = save_h;
   if (moe::launch_fc1(a1, mc, s) != 0) return MOE_ERR_CUDA;
+  mark(5);
 
   moe::Fc2Args a2;
   std::memset(&a2, 0, sizeof(a2));
@@ -541,10 +565,13 @@ int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, in
   if (encode_operand(&a2.tmap_b, w2_codes, (int64_t)E * d, d_ff / 2) != MOE_OK) return MOE_ERR_CUDA;
   a2.a_sf = h_sf; a2.a_g = h_g; a2.w_sf = w2_sf; a2.w_g = w2_g; a2.offsets = offsets;
   a2.E = E; a2.d_ff = d_ff; a2.d = d; a2.k = k;
-  a2.row_to_token = r2t; a2.token_slot_row = tsr; a2.topk_w = topk_w; a2.slots = slots; a2.status = status;
+  a2.row_to_token = r2t; a2.token_slot_row = tsr; a2.topk_w = topk_w; a2.status = status;
   a2.dbg_y = save_y2;
+  if (encode_bf16(&a2.tmap_out, slots, mc, d, 32) != MOE_OK) return MOE_ERR_CUDA;
   if (moe::launch_fc2(a2, mc, s) != 0) return MOE_ERR_CUDA;
-  moe::launch_unpermute_reduce(slots, T, k, d, out, s);
+  mark(6);
+  moe::launch_unpermute_reduce(slots, tsr, T, k, d, out, s);
+  mark(7);
   return finish();
 }
 

@@ -39,7 +39,11 @@
 //        running amax; after the last chunk it requantises the row
 //        (g_h = amax/2688, E4M3 block scales, E2M1 codes).
 //   FC2: the items of a unit are the d/128 output tiles; the epilogue forms
-//        y2 = acc * (g_h * g_w2), z = BF16(w_{t,e} * y2) and writes slot (t, j).
+//        y2 = acc * (g_h * g_w2), z = BF16(w_{t,e} * y2) and writes it to the
+//        row's own row of the z rows (slot (t, j) of the combine lives at row
+//        token_slot_row[t][j]): each warp stages its 32 x 64 tile, swizzled
+//        like the destination's tensor map, and sends it with one TMA tensor
+//        store.
 //
 // FC1 on CTA pairs (where its plan fits): clusters of two CTAs, a unit being
 // two 128-row tiles of one expert.  Rank 0's MMA thread issues
@@ -913,23 +917,37 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
         bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (PAIR ? it : it / FC1_NSLOT) & 1u, abort_flag, args.status);
         if (ok && !PAIR) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
-        // Drain: two halves of 16 columns, gate then up (one tensor-memory
-        // round trip each, which keeps fewer values live than loading both
-        // together), u = BF16(acc * (g_x * g_w)) kept as packed pairs; then
-        // the accumulators are released, so the next MMAs do not wait for the
-        // SwiGLU, which runs from the registers: h = BF16(silu(u_gate) *
-        // u_up), staged, with the row amax.
+        // Drain: two halves of 16 columns, gate and up of a half in one
+        // tensor-memory round trip; the accumulators are released as soon as
+        // the second round trip has landed (before its scaling), so the next
+        // MMAs wait for two round trips only.  u = BF16(acc * (g_x * g_w)) is
+        // kept as packed pairs; the SwiGLU then runs from the registers: h =
+        // BF16(silu(u_gate) * u_up), staged, with the row amax.
         uint32_t ugw[2][8], uuw[2][8];
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (PAIR) {
+              mbar_arrive_cluster(tempty0);
+            } else {
+              mbar_arrive(tempty0 + sg * 8u);
+              mbar_arrive(tempty0 + su * 8u);
+            }
+          }
+        };
         if (ok) {
           tc_fence_after();
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int nh = n0 + hh * 16;
+            uint32_t V[2][16];
+            tmem_ld16(tmem + gcol + hh * 16, V[0]);
+            tmem_ld16(tmem + ucol + hh * 16, V[1]);
+            tmem_wait_ld();
+            if (hh == 1) release();
 #pragma unroll
             for (int gu = 0; gu < 2; ++gu) {
-              uint32_t V[16];
-              tmem_ld16(tmem + (gu ? ucol : gcol) + hh * 16, V);
-              tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 16; i += 4) {
                 const float4 fs = *reinterpret_cast<const float4*>(gws + gu * d_ff + nh + i);
@@ -937,8 +955,8 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
 #pragma unroll
                 for (int jj = 0; jj < 4; jj += 2) {
                   const int m = i + jj;
-                  const float y0 = __fmul_rn(__uint_as_float(V[m]), __fmul_rn(ga, ss[jj]));
-                  const float y1 = __fmul_rn(__uint_as_float(V[m + 1]), __fmul_rn(ga, ss[jj + 1]));
+                  const float y0 = __fmul_rn(__uint_as_float(V[gu][m]), __fmul_rn(ga, ss[jj]));
+                  const float y1 = __fmul_rn(__uint_as_float(V[gu][m + 1]), __fmul_rn(ga, ss[jj + 1]));
                   if (gu) uuw[hh][m >> 1] = bf16x2_rn(y0, y1); else ugw[hh][m >> 1] = bf16x2_rn(y0, y1);
                   if (DBG && out && args.dbg_u) {
                     float* du = args.dbg_u + row * 2 * d_ff + gu * d_ff;
@@ -948,16 +966,8 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
               }
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (PAIR) {
-            mbar_arrive_cluster(tempty0);
-          } else {
-            mbar_arrive(tempty0 + sg * 8u);
-            mbar_arrive(tempty0 + su * 8u);
-          }
+        } else {
+          release();
         }
         if (ok) {
 #pragma unroll
@@ -1021,12 +1031,13 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
 // ---------------------------------------------------------------------------
 // FC2 + router-weighted scatter
 // ---------------------------------------------------------------------------
-// MODE 0: the forward (z to the slots).  MODE 1: also the debug output
-// (pre-weighting FP32 y2).  MODE 2: the straight-through backward's
-// recomputation of the same y2 (same code, same results) against the output
-// gradient: dw[t][j] = sum_n dY[t][n] y2[row][n] (FP32) and the BF16 dgrad
-// operand dy2[row] = BF16(w_tj dY[t]) written in place of the slots (zero on
-// pad rows); no slots.
+// MODE 0: the forward (z rows).  MODE 1: also the debug output (pre-weighting
+// FP32 y2).  MODE 2: the straight-through backward's recomputation of the
+// same y2 (same code, same results) against the output gradient: dw[t][j] =
+// sum_n dY[t][n] y2[row][n] (FP32) and the BF16 dgrad operand dy2[row] =
+// BF16(w_tj dY[t]) written in place of the z rows (zero on pad rows).  The
+// output rows (z or dy2, [m_cap][d] BF16) leave through args.tmap_out; pad
+// rows come out as zeros (their h and router weight are zero).
 template <int MODE>
 __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(const __grid_constant__ Fc2Args args) {
   constexpr bool DBG = MODE == 1, DW = MODE == 2;
@@ -1070,6 +1081,8 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
     const int rl = q4 * 32 + lane;
     const uint32_t tmem = tl->tmem_base + ((uint32_t)(q4 * 32) << 16) + part * 64;
     uint32_t it = 0, uc = 0;
+    bool stores = false;  // lane 0: a tensor store of this warp may be in flight
+    if (lane == 0) prefetch_tmap(&args.tmap_out);
     for (int u = blockIdx.x; u < G.num_mt; u += gridDim.x, ++uc) {
       const int e = expert_of(args.offsets, args.E, u);
       const int64_t row = (int64_t)u * BM + rl;
@@ -1093,7 +1106,6 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
       float* gws = gw_s + (uc & 1) * d;
       stage_scales<FC2_NE>(gws, args.w_g + (int64_t)e * d, d, threadIdx.x);
       epi_barrier<FC2_NE>();
-      uint16_t* dst_row = DW ? args.dy2 + row * d : args.slots + ((int64_t)(t < 0 ? 0 : t) * k + j) * d;
       const uint16_t* dy_row = DW ? args.dY + (int64_t)(t < 0 ? 0 : t) * d : nullptr;
       float dot = 0.0f;
       for (int nt = 0; nt < G.items; ++nt, ++it) {
@@ -1113,6 +1125,9 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[slot]));
         if (ok) {
+          // the staging tile is free once the previous store has read it
+          if (lane == 0 && stores) bulk_wait_read0();
+          __syncwarp();
           if (DW) {
             // the warp's 32 output-gradient row segments (64 columns each)
             // into the staging tile, 8 lanes per row, 4 rows per load
@@ -1129,9 +1144,9 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
             }
             __syncwarp();
           }
-          // scale and weight into the staging tile, then write each row's 64
-          // columns as one 128-byte segment (8 lanes per row, 4 rows per
-          // instruction); pad rows (t < 0) are not stored
+          // scale and weight into the staging tile (the 128-byte-swizzled
+          // layout of the destination tensor map), then one TMA store of the
+          // warp's 32 rows x 64 columns
 #pragma unroll
           for (int hf = 0; hf < 4; ++hf) {
             const int n0 = nt * BN + part * 64 + hf * 16;
@@ -1171,18 +1186,12 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
             sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf) ^ (lane & 7)), zp[0], zp[1], zp[2], zp[3]);
             sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf + 1) ^ (lane & 7)), zp[4], zp[5], zp[6], zp[7]);
           }
+          fence_proxy_async();
           __syncwarp();
-          const unsigned long long my_dst =
-              (DW || t >= 0) ? reinterpret_cast<unsigned long long>(dst_row + nt * BN + part * 64) : 0ull;
-          const int sub = lane >> 3, ch = lane & 7;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = i * 4 + sub;
-            const unsigned long long dp = __shfl_sync(0xFFFFFFFFu, my_dst, rr);
-            const uint4 v = lds128(stg + rr * FC2_STAGE_ROW + 16 * (ch ^ (rr & 7)));
-            if (dp) reinterpret_cast<uint4*>(dp)[ch] = v;
+          if (lane == 0) {
+            tma_store_2d(&args.tmap_out, stg, nt * BN + part * 64, u * BM + q4 * 32);
+            stores = true;
           }
-          __syncwarp();
         }
       }
       if (DW) {  // dw of the row: the two column parts' sums, part 0 + part 1
@@ -1191,6 +1200,8 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
         if (part == 0 && t >= 0) args.dw[(int64_t)t * k + j] = dot + tl->rowmax[1][rl];
       }
     }
+    if (lane == 0 && stores) bulk_wait0();  // the stores complete before the CTA exits
+    __syncwarp();
   }
   teardown<FC2_NE>(tl);
 }

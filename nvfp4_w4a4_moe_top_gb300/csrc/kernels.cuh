@@ -46,7 +46,9 @@ int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const
                          int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
                          uint8_t* codes, uint8_t* tok_codes, uint8_t* sf, float* g, int* status, cudaStream_t stream);
 
-int launch_unpermute_reduce(const uint16_t* slots, int T, int k, int d, uint16_t* out, cudaStream_t stream);
+// out[t] = BF16(sum_j FP32(z[token_slot_row[t][j]])), j ascending.
+int launch_unpermute_reduce(const uint16_t* z, const int32_t* token_slot_row, int T, int k, int d, uint16_t* out,
+                            cudaStream_t stream);
 
 struct Fc1Args {
   CUtensorMap tmap_a, tmap_b;
@@ -71,8 +73,12 @@ struct Fc1Args {
   int* status;
   int rings, na, nb, resident;  // pipeline plan, set by launch_fc1
 };
+constexpr int kMaxGemmCtas = 256;
+// FC1 workspace: h staging, two 128 x d_ff BF16 buffers per CTA.
+inline size_t fc1_workspace_bytes(int d_ff) { return (size_t)kMaxGemmCtas * 2 * 128 * d_ff * 2; }
 struct Fc2Args {
   CUtensorMap tmap_a, tmap_b;
+  CUtensorMap tmap_out;  // output rows [m_cap][d] BF16 (z, or dy2 in MODE 2): boxes 64 x 32, 128-byte swizzle
   const uint8_t* a_sf;
   const float* a_g;
   const uint8_t* w_sf;
@@ -82,12 +88,10 @@ struct Fc2Args {
   const int32_t* row_to_token;
   const int32_t* token_slot_row;
   const float* topk_w;
-  uint16_t* slots;
   float* dbg_y;
-  // backward recomputation (dw set): dY bf16 [T][d] in, dy2 bf16 [rows][d]
-  // and dw f32 [T][k] out, no slots
+  // backward recomputation (dw set): dY bf16 [T][d] in, dw f32 [T][k] out,
+  // and tmap_out maps dy2 bf16 [m_cap][d] instead of the z rows
   const uint16_t* dY;
-  uint16_t* dy2;
   float* dw;
   int* status;
   int rings, na, nb, resident;  // pipeline plan, set by launch_fc2
@@ -121,6 +125,5 @@ int launch_bwd_dx(const float* dxr, const int32_t* token_slot_row, int T, int k,
 int gemm_num_ctas();  // persistent grid size on the current device
 int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream);
 int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream);
-constexpr int kMaxGemmCtas = 256;
 
 }  // namespace moe

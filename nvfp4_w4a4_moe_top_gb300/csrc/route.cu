@@ -423,21 +423,23 @@ int launch_permute_quant(const int32_t* topk_ids, int32_t* token_slot_row, const
   return 0;
 }
 
-// out[t] = BF16(sum_j FP32(slots[t][j])), j ascending; 8 columns per thread.
-// KMAX >= k: all k slot loads are issued before the ordered sum.
+// out[t] = BF16(sum_j FP32(z[token_slot_row[t][j]])), j ascending (the
+// ascending expert ids of the token's slots); 8 columns per thread.
+// KMAX >= k: all k row loads are issued before the ordered sum.
 template <int KMAX>
-__global__ void __launch_bounds__(256) unpermute_reduce_kernel(const uint16_t* __restrict__ slots, int T, int k,
-                                                               int d, uint16_t* __restrict__ out) {
+__global__ void __launch_bounds__(256) unpermute_reduce_kernel(const uint16_t* __restrict__ z,
+                                                               const int32_t* __restrict__ token_slot_row, int T,
+                                                               int k, int d, uint16_t* __restrict__ out) {
   const int c8n = d / 8;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)T * c8n) return;
   const int64_t t = idx / c8n;
   const int c8 = (int)(idx - t * c8n);
-  const uint4* base = reinterpret_cast<const uint4*>(slots + t * k * (int64_t)d) + c8;
+  const int32_t* ts = token_slot_row + t * k;
   uint4 v[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j)
-    if (j < k) v[j] = __ldg(base + (int64_t)j * c8n);
+    if (j < k) v[j] = __ldg(reinterpret_cast<const uint4*>(z + (int64_t)__ldg(ts + j) * d) + c8);
   float s[8];
   {
     const uint32_t w[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
@@ -463,14 +465,15 @@ __global__ void __launch_bounds__(256) unpermute_reduce_kernel(const uint16_t* _
   reinterpret_cast<uint4*>(out + t * (int64_t)d)[c8] = o;
 }
 
-int launch_unpermute_reduce(const uint16_t* slots, int T, int k, int d, uint16_t* out, cudaStream_t stream) {
+int launch_unpermute_reduce(const uint16_t* z, const int32_t* token_slot_row, int T, int k, int d, uint16_t* out,
+                            cudaStream_t stream) {
   const int64_t n = (int64_t)T * (d / 8);
   if (n == 0) return 0;
   const unsigned grid = (unsigned)((n + 255) / 256);
-  if (k <= 4) unpermute_reduce_kernel<4><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
-  else if (k <= 8) unpermute_reduce_kernel<8><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
-  else if (k <= 16) unpermute_reduce_kernel<16><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
-  else unpermute_reduce_kernel<32><<<grid, 256, 0, stream>>>(slots, T, k, d, out);
+  if (k <= 4) unpermute_reduce_kernel<4><<<grid, 256, 0, stream>>>(z, token_slot_row, T, k, d, out);
+  else if (k <= 8) unpermute_reduce_kernel<8><<<grid, 256, 0, stream>>>(z, token_slot_row, T, k, d, out);
+  else if (k <= 16) unpermute_reduce_kernel<16><<<grid, 256, 0, stream>>>(z, token_slot_row, T, k, d, out);
+  else unpermute_reduce_kernel<32><<<grid, 256, 0, stream>>>(z, token_slot_row, T, k, d, out);
   return 0;
 }
 

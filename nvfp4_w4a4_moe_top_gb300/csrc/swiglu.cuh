@@ -192,18 +192,28 @@ __device__ __forceinline__ uint32_t swiglu_pair_fix(uint32_t gw, uint32_t uw) {
   return r0 | (r1 << 16);
 }
 
-// The rare path of swiglu16, out of line: v holds the 8 gate words, the 8
-// up words and the 8 result words; the pairs whose bit is set in `mask` are
-// recomputed exactly.
-__device__ __noinline__ void swiglu16_fix(uint32_t* v, uint32_t mask) {
-#pragma unroll 1
+// The 16 inputs of a group and its 8 result words, passed by value so that
+// the rare path below takes its arguments in registers.
+struct Swiglu16In {
+  uint32_t g[8], u[8];
+};
+struct Swiglu16Out {
+  uint32_t h[8];
+};
+
+// Rare path of swiglu16, out of line (its code and register needs stay out
+// of the caller's loop): the pairs whose bit is set in `mask` are recomputed
+// exactly.
+__device__ __noinline__ Swiglu16Out swiglu16_rare(const Swiglu16In in, Swiglu16Out out, uint32_t mask) {
+#pragma unroll
   for (int w = 0; w < 8; ++w)
-    if (mask & (1u << w)) v[16 + w] = swiglu_pair_fix(v[w], v[8 + w]);
+    if (mask & (1u << w)) out.h[w] = swiglu_pair_fix(in.g[w], in.u[w]);
+  return out;
 }
 
 // h of 16 elements (8 packed gate words, 8 packed up words) into 8 packed
-// BF16 words; returns the largest |h| of the 16 as packed magnitude bits
-// (the larger of its two halves is the maximum).
+// BF16 words, exact; returns the largest |h| of the 16 as packed magnitude
+// bits (the larger of its two halves is the maximum).
 __device__ __forceinline__ uint32_t swiglu16(const uint32_t (&gw)[8], const uint32_t (&uw)[8], uint32_t (&h)[8]) {
   uint32_t mask = 0, gmax = 0, hmax = 0, hmin = 0x7FFF7FFFu;
 #pragma unroll
@@ -219,18 +229,19 @@ __device__ __forceinline__ uint32_t swiglu16(const uint32_t (&gw)[8], const uint
   if (max(gmax & 0xFFFFu, gmax >> 16) > kSwigluNegGmaxBits || min(hmin & 0xFFFFu, hmin >> 16) < kSwigluTinyBits)
     mask = 0xFFu;
   if (mask) {
-    uint32_t v[24];
+    Swiglu16In in;
+    Swiglu16Out o;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      v[w] = gw[w];
-      v[8 + w] = uw[w];
-      v[16 + w] = h[w];
+      in.g[w] = gw[w];
+      in.u[w] = uw[w];
+      o.h[w] = h[w];
     }
-    swiglu16_fix(v, mask);
+    o = swiglu16_rare(in, o, mask);
     hmax = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      h[w] = v[16 + w];
+      h[w] = o.h[w];
       hmax = __vmaxu2(hmax, h[w] & 0x7FFF7FFFu);
     }
   }

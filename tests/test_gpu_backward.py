@@ -60,7 +60,7 @@ def gpu_train_step(lay, x, lg, W1, W2, dY):
     sy = torch.full((mc, d), float("nan"), dtype=torch.float32, device="cuda")
     M.nvfp4_grouped_gemm_fc2_unpermute(v["h_codes"], v["h_sf"], v["h_g"], v["offsets"], E, mc, F, d, w2q["codes"],
                                        w2q["sf"], w2q["g"], v["row_to_token"], v["token_slot_row"], v["topk_w"], T,
-                                       k, torch.empty((T, k, d), dtype=torch.int16, device="cuda"),
+                                       k, torch.empty((mc, d), dtype=torch.int16, device="cuda"),
                                        torch.empty((T, d), dtype=torch.int16, device="cuda"), sy)
     dx = torch.full((T, d), float("nan"), dtype=torch.float32, device="cuda")
     dW1 = torch.full((E, 2 * F, d), float("nan"), dtype=torch.float32, device="cuda")

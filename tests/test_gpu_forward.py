@@ -17,13 +17,18 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
-# Independent end-to-end tolerance on the BF16 output (rel-L2 over the
-# checked tokens, and max-abs).  FP32 accumulation order differs between the
-# tensor cores and the sequential oracle (~1e-7 relative); a rare one-ulp
-# BF16 flip of u or h can move one FP4 code of h, which moves an output by
-# about |w| * |W2| * S_b ~ 1e-3.
-E2E_REL_L2 = 2e-3
-E2E_MAX_ABS = 2e-2
+# Independent end-to-end tolerance on the BF16 output.  The FP32 sums of the
+# GEMMs run in the tensor cores' order, not the oracle's sequential order
+# (about 1e-7 relative); with h rounded exactly on both sides, what reaches
+# the output is a rare flip of a BF16 rounding: of u (which can move an h
+# code), of z, or of out itself.  Measured on GB300 over the configurations
+# below: rel-L2 at most 1.1e-5, no element off by more than one BF16 ulp of
+# the oracle's value (e.g. 7.8e-3 at |out| ~ 1.5 in the small layer, 1.2e-4
+# in the tiny one), and no h-code row different.  The bounds are those
+# figures with a margin: rel-L2 <= 2e-5, every element within one BF16 ulp
+# (so max-abs <= 2e-3 wherever |out| < 0.5), h-code rows differing <= 1e-3.
+E2E_REL_L2 = 2e-5
+H_ROWS_DIFFERING = 1e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,9 +59,12 @@ def gpu_forward(lay, x, lg, W1=None, W2=None, w1q=None, w2q=None, status=True):
 
 
 def e2e_errors(got_bf16, exp_bf16):
+    """rel-L2, max-abs, and the largest difference in BF16 ulps of the
+    expected value (the spacing of BF16 values at |expected|)."""
     from gpu_util import f32_of_bf16, rel_l2
     g, e = f32_of_bf16(got_bf16), f32_of_bf16(exp_bf16)
-    return rel_l2(g, e), float(np.abs(g - e).max())
+    ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(e), 2.0 ** -126))[1] - 8)
+    return rel_l2(g, e), float(np.abs(g - e).max()), float((np.abs(g - e) / ulp).max())
 
 
 def layer_of(name):
@@ -96,10 +104,11 @@ def test_forward_against_oracle(orc, name):
     assert np.array_equal(orc.unswizzle_sf(r["x_sf"], mp, lay.d), orc.unswizzle_sf(ref["x_sf"], mp, lay.d))
     # h codes: identical except rows touched by a rare accumulation-order flip
     row_diff = np.any(r["h_codes"][:mp] != ref["h_codes"][:mp], axis=1)
-    assert row_diff.mean() <= 0.02, row_diff.mean()
-    rel, mx = e2e_errors(r["out"], ref["out"])
-    print("%s: e2e rel-L2 %.3e max-abs %.3e, h-code rows differing %.4f" % (name, rel, mx, row_diff.mean()))
-    assert rel <= E2E_REL_L2 and mx <= E2E_MAX_ABS
+    rel, mx, ulps = e2e_errors(r["out"], ref["out"])
+    print("%s: e2e rel-L2 %.3e max-abs %.3e (%.2f BF16 ulps), h-code rows differing %.5f"
+          % (name, rel, mx, ulps, row_diff.mean()))
+    assert row_diff.mean() <= H_ROWS_DIFFERING, row_diff.mean()
+    assert rel <= E2E_REL_L2 and ulps <= 1.0
 
 
 @pytest.mark.parametrize("name", ["small", "ragged"])
@@ -146,7 +155,7 @@ def test_forward_equals_modular_composition(orc):
     f1ws = torch.empty(M.fc1_workspace_bytes(dff), dtype=torch.uint8, device="cuda")
     M.nvfp4_grouped_gemm_fc1_swiglu(xq["codes"], xq["sf"], xq["g"], offs, E, mc, d, dff, w1q["codes"],
                                     w1q["sf"], w1q["g"], hq["codes"], hq["sf"], hq["g"], None, None, f1ws)
-    slots = torch.zeros((T, k, d), dtype=torch.int16, device="cuda")
+    slots = torch.zeros((mc, d), dtype=torch.int16, device="cuda")
     out = torch.zeros((T, d), dtype=torch.int16, device="cuda")
     M.nvfp4_grouped_gemm_fc2_unpermute(hq["codes"], hq["sf"], hq["g"], offs, E, mc, dff, d, w2q["codes"],
                                        w2q["sf"], w2q["g"], r2t, tsr, w, T, k, slots, out, None)
@@ -162,12 +171,12 @@ def test_forward_deterministic(orc):
     x, lg, W1, W2 = lay.x(), lay.logits(), lay.w1(), lay.w2()
     r1, w1q, w2q = gpu_forward(lay, x, lg, W1, W2)
     r2, _, _ = gpu_forward(lay, x, lg, w1q=w1q, w2q=w2q)
-    for key in ["out", "slots", "row_to_token", "token_slot_row"]:
+    for key in ["out", "row_to_token", "token_slot_row"]:
         assert np.array_equal(r1[key], r2[key]), key
     # the per-row buffers are written below offsets[E] only; the rest of the
     # workspace is whatever the allocation held
     mp = int(r1["offsets"][-1])
-    for key in ["h_codes", "x_codes", "h_g", "x_g"]:
+    for key in ["h_codes", "x_codes", "h_g", "x_g", "slots"]:
         assert np.array_equal(r1[key][:mp], r2[key][:mp]), key
 
 
@@ -234,6 +243,32 @@ def test_full_size_sampled_tokens(orc, name):
             assert r["x_g"][row] == o["x_g"]
         got.append(r["out"][t])
         exp.append(o["out"])
-    rel, mx = e2e_errors(np.stack(got), np.stack(exp))
-    print("%s sampled %d tokens: rel-L2 %.3e max-abs %.3e" % (name, len(sample), rel, mx))
-    assert rel <= E2E_REL_L2 and mx <= E2E_MAX_ABS
+    rel, mx, ulps = e2e_errors(np.stack(got), np.stack(exp))
+    print("%s sampled %d tokens: rel-L2 %.3e max-abs %.3e (%.2f BF16 ulps)" % (name, len(sample), rel, mx, ulps))
+    assert rel <= E2E_REL_L2 and ulps <= 1.0
+
+
+def test_forward_timed_equals_forward(orc):
+    """moe_expert_forward_timed runs the same seven launches as
+    moe_expert_forward (same output, bit for bit) and records the caller's
+    eight events around them, in order."""
+    import torch
+    from gpu_util import dev, host
+    lay = synth.layer("small")
+    x, lg, W1, W2 = lay.x(), lay.logits(), lay.w1(), lay.w2()
+    T, E, k, d, dff = lay.T, lay.E, lay.k, lay.d, lay.d_ff
+    r, w1q, w2q = gpu_forward(lay, x, lg, W1, W2)
+    out = torch.full((T, d), 0x5A5A, dtype=torch.int16, device="cuda")
+    ws = M.forward_workspace(T, E, k, d, dff)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    M.moe_expert_forward_timed(dev(x), dev(lg), T, E, k, d, dff, w1q["codes"], w1q["sf"], w1q["g"], w2q["codes"],
+                               w2q["sf"], w2q["g"], out, ws, st, None, ev)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(host(out, np.uint16), r["out"])
+    times = [ev[0].elapsed_time(e) for e in ev]
+    assert all(b >= a for a, b in zip(times, times[1:])) and times[-1] > 0
+    # no events: refused before anything is enqueued
+    assert M.lib().moe_expert_forward_timed(None, None, T, E, k, d, dff, None, None, None, None, None, None, None,
+                                            None, 0, None, None, None) == M.MOE_ERR_POINTER

@@ -7,9 +7,9 @@ weights).  Checks, per the specification's tolerance rules:
        of the GPU's u; h codes / scales / g bit-exact with the oracle's
        quantisation of the GPU's h.
   FC2: pre-weighting expert outputs y2 (dbg_y) within rel-L2 1e-5 and BF16
-       max-abs 2e-3 of the oracle; slots bit-exact with the oracle's
-       weighting of the GPU's y2; out bit-exact with the oracle's reduce of
-       the GPU's slots.
+       max-abs 2e-3 of the oracle; the slots (z rows, slot (t, j) at row
+       token_slot_row[t][j]) bit-exact with the oracle's weighting of the
+       GPU's y2; out bit-exact with the oracle's reduce of the GPU's slots.
 The debug outputs select a separate instantiation of each GEMM kernel; the
 production instantiation (no debug pointers, the one the forward runs) is
 tied to it bit for bit on the same inputs, including a 2048-token slice of
@@ -137,7 +137,7 @@ def run_fc2(lay, c, hq, debug=True):
     import torch
     from gpu_util import dev, host
     mc, d, dff, E, T, k = c["mc"], lay.d, lay.d_ff, lay.E, c["T"], lay.k
-    slots = torch.zeros((T, k, d), dtype=torch.int16, device="cuda")
+    slots = torch.zeros((mc, d), dtype=torch.int16, device="cuda")
     out = torch.zeros((T, d), dtype=torch.int16, device="cuda")
     dbg_y = torch.full((mc, d), float("nan"), dtype=torch.float32, device="cuda") if debug else None
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -175,8 +175,11 @@ def test_fc2_parity(orc, name, T):
     y_full = np.zeros_like(y2)
     y_full[:mp] = g["y"][:mp]
     slots_ref = orc.combine(y_full, c["perm"], c["w"], c["T"], lay.k, lay.d)
-    assert np.array_equal(g["slots"], slots_ref)
-    assert np.array_equal(g["out"], orc.reduce(g["slots"]))
+    slots = g["slots"][c["perm"]["token_slot_row"]]  # [T][k][d]
+    assert np.array_equal(slots, slots_ref)
+    assert np.array_equal(g["out"], orc.reduce(slots))
+    # pad rows of the z rows are written as zeros
+    assert not g["slots"][:mp][~real].any()
 
 
 @pytest.mark.parametrize("name", ["small", "custom_skew", "custom_pair_skew", "custom_pair_3stage"])

@@ -106,7 +106,9 @@ size_t moe_permute_workspace_bytes(int T, int E);
 
 /* Workspace of nvfp4_grouped_gemm_fc1_swiglu: h staging, two 128 x d_ff
  * BF16 buffers per CTA (a unit is staged while the previous one is
- * requantised). */
+ * requantised), then sixteen 16-byte slots per epilogue thread (512 per
+ * CTA) for the SwiGLU pairs whose exact evaluation is deferred to the end of
+ * the unit. */
 size_t nvfp4_fc1_workspace_bytes(int d_ff);
 
 /* Workspace of moe_expert_forward (all intermediates of one forward). */
@@ -124,7 +126,7 @@ size_t moe_expert_backward_workspace_bytes(int T, int E, int k, int d, int d_ff)
  * 7 x_codes u8[M_cap][d/2], 8 x_sf, 9 x_g f32[M_cap], 10 h_codes
  * u8[M_cap][d_ff/2], 11 h_sf, 12 h_g f32[M_cap], 13 z rows bf16[M_cap][d]
  * (slot (t, j) at row token_slot_row[t][j]), 14 chunk histograms, 15 FC1
- * staging).  Writes 16 entries; returns 0. */
+ * workspace: h staging and deferred SwiGLU slots).  Writes 16 entries; returns 0. */
 int moe_expert_forward_workspace_layout(int T, int E, int k, int d, int d_ff,
                                         size_t offsets_out[16]);
 

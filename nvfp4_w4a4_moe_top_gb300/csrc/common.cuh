@@ -179,18 +179,30 @@ __device__ __forceinline__ uint32_t e2m1x8_pairs(const uint64_t (&p)[4]) {
 // from the correctly rounded division.  Quotients far below 0.25 encode to
 // zero on both sides, so subnormal products do not break the argument.  The
 // bracket products go two at a time through the packed f32x2 multiply.
-__device__ __forceinline__ uint32_t e2m1_codes8(const uint32_t (&w)[4], float S) {
-  if (S >= 7.52316384526264e-37f) {  // 2^-120: R and the products stay finite
-    const float R = __frcp_rn(S);
-    const float Rl = __fmul_rn(R, 0.99999952316284180f);  // 1 - 2^-21
-    const float Rh = __fmul_rn(R, 1.00000047683715820f);  // 1 + 2^-21
-    const uint64_t rl = f32x2_pack(Rl, Rl), rh = f32x2_pack(Rh, Rh);
+// The two bracket factors depend on S only: a 16-element block computes
+// them once for both of its halves.
+struct E2m1Bracket {
+  uint64_t rl, rh;  // RN(R(1 - 2^-21)), RN(R(1 + 2^-21)), each in both halves
+  bool ok;          // S >= 2^-120: R and the products stay finite
+};
+__device__ __forceinline__ E2m1Bracket e2m1_bracket(float S) {
+  E2m1Bracket b;
+  b.ok = S >= 7.52316384526264e-37f;  // 2^-120
+  const float R = b.ok ? __frcp_rn(S) : 0.0f;
+  const float Rl = __fmul_rn(R, 0.99999952316284180f);  // 1 - 2^-21
+  const float Rh = __fmul_rn(R, 1.00000047683715820f);  // 1 + 2^-21
+  b.rl = f32x2_pack(Rl, Rl);
+  b.rh = f32x2_pack(Rh, Rh);
+  return b;
+}
+__device__ __forceinline__ uint32_t e2m1_codes8(const uint32_t (&w)[4], float S, const E2m1Bracket& br) {
+  if (br.ok) {
     uint64_t l[4], h[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint64_t x = f32x2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
-      l[i] = mul_f32x2(x, rl);
-      h[i] = mul_f32x2(x, rh);
+      l[i] = mul_f32x2(x, br.rl);
+      h[i] = mul_f32x2(x, br.rh);
     }
     const uint32_t cl = e2m1x8_pairs(l);
     if (cl == e2m1x8_pairs(h)) return cl;
@@ -202,6 +214,11 @@ __device__ __forceinline__ uint32_t e2m1_codes8(const uint32_t (&w)[4], float S)
     q[2 * i + 1] = __fdiv_rn(bf16_hi(w[i]), S);
   }
   return e2m1x8(q);
+}
+// Codes of the 16 BF16 values of one block (two groups of 4 packed words).
+__device__ __forceinline__ uint2 e2m1_codes16(const uint32_t (&w0)[4], const uint32_t (&w1)[4], float S) {
+  const E2m1Bracket br = e2m1_bracket(S);
+  return make_uint2(e2m1_codes8(w0, S, br), e2m1_codes8(w1, S, br));
 }
 
 // ---------------------------------------------------------------------------

@@ -95,7 +95,12 @@ constexpr int FC2_NSLOT = 2;                           // FC2: double buffering
 // columns each, 80 registers per thread); FC2's light epilogue keeps 8 warps
 // of 64 columns at 128 registers.
 constexpr int FC1_NE = 16, FC2_NE = 8;
-constexpr int FC1_PARTS = FC1_NE / 4, FC1_PART_COLS = BN / FC1_PARTS;  // 4 parts of 32 columns
+static_assert(FC1_NE * 32 <= kFc1EpiThreads, "FC1 epilogue threads");
+constexpr int FC1_PARTS = FC1_NE / 4, FC1_PART_COLS = BN / FC1_PARTS;  // column parts of a chunk, one per warp
+// h is staged and requantised in 32-column sub-parts (two 16-element blocks,
+// half of a scale word); a thread's part holds FC1_SUB of them and
+// FC1_HALVES 16-column halves.
+constexpr int FC1_VPARTS = 4, FC1_SUB = FC1_VPARTS / FC1_PARTS, FC1_HALVES = FC1_PART_COLS / 16;
 constexpr int FC2_PARTS = FC2_NE / 4, FC2_PART_COLS = BN / FC2_PARTS;  // 2 parts of 64 columns
 constexpr int FC2_STAGE_ROW = FC2_PART_COLS * 2;       // FC2 output staging: one part's BF16 columns per row
 constexpr int FC2_STAGING_BYTES = FC2_NE * 32 * FC2_STAGE_ROW;  // 32 rows per epilogue warp
@@ -596,57 +601,86 @@ __device__ void sf_writer_loop(int qd, const Geometry& G, const int32_t* off, in
 template <bool PAIR>
 __device__ void mma_loop(const Geometry& G, const int32_t* off, int E, uint32_t a_base, uint32_t ring_base, Tail* tl,
                          uint32_t tmem, volatile int* abort_flag, int* status) {
-  const uint32_t b_off = G.b_off();
-  uint32_t kc = 0, it = 0;
+  // The per-k-step work of this single thread is the latency the tensor
+  // pipe waits on, so everything that does not change per k-step is
+  // computed here, and the ring position advances by increments: k-step kc
+  // sits in ring r = kc % rings at position pos = kc / rings, in stage slot
+  // r * S + pos % S, used for the (pos / S)-th time.
+  const uint32_t R = (uint32_t)G.rings, lgS = (uint32_t)G.log2_stages, Smask = (1u << lgS) - 1u;
+  const bool sf_ring = G.sf_ring();
+  const uint32_t sf_full0 = smem_u32(&tl->sf_full[0]), b_empty0 = smem_u32(&tl->b_empty[0]);
+  const uint32_t a_empty0 = smem_u32(&tl->a_empty[0]), sf_empty0 = smem_u32(&tl->sf_empty[0]);
+  const uint32_t tempty0 = smem_u32(&tl->tempty[0]), tfull0 = smem_u32(&tl->tfull[0]);
+  const uint32_t stage_desc = (uint32_t)G.stage_bytes >> 4;  // descriptor units (16 B) per stage
+  const uint64_t bdesc0 = sdesc_k_sw128(ring_base + G.b_off());
+  const uint64_t adesc0 = sdesc_k_sw128(G.resident ? a_base : ring_base);
+  const uint32_t adesc_step = G.resident ? (uint32_t)(A_SLICE >> 4) : 0u;
+  const uint32_t sf0 = tmem + G.sf_col();
+  uint32_t kc = 0, it = 0, r = 0, pos = 0;
   bool aborted = false;
   UnitCursor cur;
   int u, e;
   bool ghost;
   for (int iu = 0; !aborted && unit_at(G, off, E, iu, cur, u, e, ghost); ++iu) {
     for (int q = 0; q < G.items && !aborted; ++q, ++it) {
-      const uint32_t acc_slot = it % (uint32_t)G.nslot, suse = it / (uint32_t)G.nslot;
-      if (!wait_bounded(smem_u32(&tl->tempty[acc_slot]), (suse & 1u) ^ 1u, abort_flag, status)) {
+      const uint32_t acc_slot = PAIR ? 0u : it % (uint32_t)G.nslot, suse = PAIR ? it : it / (uint32_t)G.nslot;
+      if (!wait_bounded(tempty0 + 8u * acc_slot, (suse & 1u) ^ 1u, abort_flag, status)) {
         aborted = true;
         break;
       }
       tc_fence_after();
       const uint32_t dacc = tmem + acc_slot * (uint32_t)G.acc_cols;
+      const bool last_item = G.resident && q == G.items - 1;
       for (int ks = 0; ks < G.nk; ++ks, ++kc) {
-        uint32_t slot, use, buf, buse;
-        G.slot_of(kc, slot, use);
-        G.sfbuf_of(kc, slot, use, buf, buse);
-        if (!wait_bounded(smem_u32(&tl->sf_full[buf]), buse & 1u, abort_flag, status)) { aborted = true; break; }
+        const uint32_t slot = (r << lgS) | (pos & Smask), use = pos >> lgS;
+        const uint32_t buf = sf_ring ? (kc & (PAIR_SFBUF - 1)) : slot;
+        const uint32_t buse = sf_ring ? kc / PAIR_SFBUF : use;
+        if (++r == R) {
+          r = 0;
+          ++pos;
+        }
+        if (!wait_bounded(sf_full0 + 8u * buf, buse & 1u, abort_flag, status)) { aborted = true; break; }
         tc_fence_after();
         const int nmma = min(4, G.kgroups - 4 * ks);
-        const uint32_t st = ring_base + slot * G.stage_bytes;
-        const uint32_t sf_a = tmem + G.sf_col() + buf * G.sf_cols;
-        const uint32_t sf_b = sf_a + 16;
-        const uint64_t adesc = sdesc_k_sw128(G.resident ? a_base + ks * A_SLICE : st);
-        const uint64_t bdesc = sdesc_k_sw128(st + b_off);
+        const uint32_t sf_a = sf0 + buf * (uint32_t)G.sf_cols;
+        const uint64_t bdesc = bdesc0 + slot * stage_desc;
+        const uint64_t adesc = adesc0 + (G.resident ? (uint32_t)ks * adesc_step : slot * stage_desc);
         if constexpr (PAIR) {
-          for (int i = 0; i < nmma; ++i)
-            tc_mma_pair(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 8 * i, (ks | i) != 0 ? 1u : 0u);
-          tc_commit_pair(smem_u32(&tl->b_empty[slot]));
-          if (G.sf_ring()) tc_commit_pair(smem_u32(&tl->sf_empty[buf]));
-          if (G.resident && q == G.items - 1) tc_commit_pair(smem_u32(&tl->a_empty[ks]));
-        } else {
+          const uint32_t sf_b = sf_a + 16;
           if (nmma == 4) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
+            const uint32_t acc0 = ks != 0 ? 1u : 0u;
+            tc_mma_pair(dacc, adesc, bdesc, sf_a, sf_b, acc0);
+            tc_mma_pair(dacc, adesc + 2, bdesc + 2, sf_a + 4, sf_b + 8, 1u);
+            tc_mma_pair(dacc, adesc + 4, bdesc + 4, sf_a + 8, sf_b + 16, 1u);
+            tc_mma_pair(dacc, adesc + 6, bdesc + 6, sf_a + 12, sf_b + 24, 1u);
+          } else {
+            for (int i = 0; i < nmma; ++i)
+              tc_mma_pair(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 8 * i, (ks | i) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair(b_empty0 + 8u * slot);
+          if (sf_ring) tc_commit_pair(sf_empty0 + 8u * buf);
+          if (last_item) tc_commit_pair(a_empty0 + 8u * (uint32_t)ks);
+        } else {
+          const uint32_t sf_b = sf_a + 16;
+          if (nmma == 4) {
+            const uint32_t acc0 = ks != 0 ? 1u : 0u;
+            tc_mma(dacc, adesc, bdesc, sf_a, sf_b, acc0);
+            tc_mma(dacc, adesc + 2, bdesc + 2, sf_a + 4, sf_b + 4, 1u);
+            tc_mma(dacc, adesc + 4, bdesc + 4, sf_a + 8, sf_b + 8, 1u);
+            tc_mma(dacc, adesc + 6, bdesc + 6, sf_a + 12, sf_b + 12, 1u);
           } else {
             for (int i = 0; i < nmma; ++i)
               tc_mma(dacc, adesc + 2 * i, bdesc + 2 * i, sf_a + 4 * i, sf_b + 4 * i, (ks | i) != 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&tl->b_empty[slot]));
-          if (G.resident && q == G.items - 1) tc_commit(smem_u32(&tl->a_empty[ks]));
+          tc_commit(b_empty0 + 8u * slot);
+          if (last_item) tc_commit(a_empty0 + 8u * (uint32_t)ks);
         }
       }
       if (!aborted) {
         if constexpr (PAIR)
-          tc_commit_pair(smem_u32(&tl->tfull[acc_slot]));
+          tc_commit_pair(tfull0 + 8u * acc_slot);
         else
-          tc_commit(smem_u32(&tl->tfull[acc_slot]));
+          tc_commit(tfull0 + 8u * acc_slot);
       }
     }
   }
@@ -740,7 +774,7 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 // Codes of 16 BF16 values (8 packed words) for block scale S > 0.
 __device__ __forceinline__ uint2 e2m1_block16(const uint32_t (&w)[8], float S) {
   const uint32_t w0[4] = {w[0], w[1], w[2], w[3]}, w1[4] = {w[4], w[5], w[6], w[7]};
-  return make_uint2(e2m1_codes8(w0, S), e2m1_codes8(w1, S));
+  return e2m1_codes16(w0, w1, S);
 }
 
 // Largest BF16 magnitude of 16 values (8 packed words), as a float.
@@ -759,16 +793,16 @@ __device__ __forceinline__ void stage_scales(float* dst, const float* src, int n
     reinterpret_cast<float4*>(dst)[i] = __ldg(reinterpret_cast<const float4*>(src) + i);
 }
 
-// FC1 requantisation of one thread's 32 columns (part `part` of chunk c,
+// FC1 requantisation of one thread's 32 columns (sub-part vp of chunk c,
 // two blocks of 16) of row `row`, read back from the scratch vectors this
 // thread staged: per block the E4M3 scale s_b = E4M3(a_b / (6 g)) and the
-// E2M1 codes of h / (g s_b).  The two scale bytes are bytes 2*(part % 2)
-// and +1 of scale word 2c + part/2.
-__device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int part, int rl, int64_t row, float g,
+// E2M1 codes of h / (g s_b).  The two scale bytes are bytes 2*(vp % 2)
+// and +1 of scale word 2c + vp/2.
+__device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int vp, int rl, int64_t row, float g,
                                               float den, uint8_t* h_codes, uint8_t* h_sf, int d_ff) {
   uint4 cur[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) cur[v] = scr[(size_t)((c * FC1_PARTS + part) * 4 + v) * BM + rl];
+  for (int v = 0; v < 4; ++v) cur[v] = scr[(size_t)((c * FC1_VPARTS + vp) * 4 + v) * BM + rl];
   uint32_t sb2 = 0;
   uint32_t cw[4];
 #pragma unroll
@@ -786,11 +820,10 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int part,
     cw[2 * b + 1] = p.y;
     sb2 |= sb << (8 * b);
   }
-  *reinterpret_cast<uint4*>(h_codes + row * (d_ff / 2) + (c * BN + part * FC1_PART_COLS) / 2) =
-      make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  *reinterpret_cast<uint4*>(h_codes + row * (d_ff / 2) + (c * BN + vp * 32) / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
   const int kgh = d_ff / 64;
-  *reinterpret_cast<uint16_t*>(h_sf + ((row >> 7) * kgh + 2 * c + (part >> 1)) * 512 + (row & 31) * 16 +
-                               ((row >> 5) & 3) * 4 + 2 * (part & 1)) = (uint16_t)sb2;
+  *reinterpret_cast<uint16_t*>(h_sf + ((row >> 7) * kgh + 2 * c + (vp >> 1)) * 512 + (row & 31) * 16 +
+                               ((row >> 5) & 3) * 4 + 2 * (vp & 1)) = (uint16_t)sb2;
 }
 
 // Shared roles of both GEMMs.  Returns true for the epilogue warps, which
@@ -889,6 +922,18 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
     // one chunk after each chunk of unit i (the thread reads back only what
     // it wrote, so program order is the only ordering needed).
     uint4* scratch_cta = reinterpret_cast<uint4*>(args.scratch) + (size_t)blockIdx.x * 2 * (size_t)(d_ff / 8) * BM;
+    // This thread's slots for SwiGLU pairs the bracket left open: their exact
+    // values are computed at the end of the unit, so that the rare slow path
+    // runs once per unit and not inside the item that met it (the next
+    // accumulator release would wait for it).  Each slot: gate word, up word,
+    // position (chunk << 5 | half << 3 | word).
+    // (The slot address is recomputed where it is used: it stays out of the
+    // registers of the hot loop.)
+    auto defer_slots = [&]() {
+      return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(args.scratch) + fc1_staging_bytes(d_ff)) +
+             ((size_t)blockIdx.x * kFc1EpiThreads + threadIdx.x) * kFc1DeferSlots;
+    };
+    int ndefer = 0;
     bool have_prev = false, ghost_prev = false;
     int64_t row_prev = 0;
     float g_prev = 0.0f, den_prev = 0.0f;
@@ -917,13 +962,13 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
         bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (PAIR ? it : it / FC1_NSLOT) & 1u, abort_flag, args.status);
         if (ok && !PAIR) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
-        // Drain: two halves of 16 columns, gate and up of a half in one
+        // Drain: halves of 16 columns, gate and up of a half in one
         // tensor-memory round trip; the accumulators are released as soon as
-        // the second round trip has landed (before its scaling), so the next
-        // MMAs wait for two round trips only.  u = BF16(acc * (g_x * g_w)) is
+        // the last round trip has landed (before its scaling), so the next
+        // MMAs wait for the round trips only.  u = BF16(acc * (g_x * g_w)) is
         // kept as packed pairs; the SwiGLU then runs from the registers: h =
         // BF16(silu(u_gate) * u_up), staged, with the row amax.
-        uint32_t ugw[2][8], uuw[2][8];
+        uint32_t ugw[FC1_HALVES][8], uuw[FC1_HALVES][8];
         auto release = [&]() {
           tc_fence_before();
           __syncwarp();
@@ -939,13 +984,13 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
         if (ok) {
           tc_fence_after();
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+          for (int hh = 0; hh < FC1_HALVES; ++hh) {
             const int nh = n0 + hh * 16;
             uint32_t V[2][16];
             tmem_ld16(tmem + gcol + hh * 16, V[0]);
             tmem_ld16(tmem + ucol + hh * 16, V[1]);
             tmem_wait_ld();
-            if (hh == 1) release();
+            if (hh == FC1_HALVES - 1) release();
 #pragma unroll
             for (int gu = 0; gu < 2; ++gu) {
 #pragma unroll
@@ -971,13 +1016,33 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
         }
         if (ok) {
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+          for (int hh = 0; hh < FC1_HALVES; ++hh) {
             const int nh = n0 + hh * 16;
             // h = BF16(silu(u_gate) * u_up), rounded once; a row with g_x = 0
             // (all-zero activations, pad rows) has u = +0 and so h = +0
             uint32_t hp[8];
             if (ga != 0.0f) {
-              amax2 = __vmaxu2(amax2, swiglu16(ugw[hh], uuw[hh], hp));
+              uint32_t hmax;
+              const uint32_t open = swiglu16_fast(ugw[hh], uuw[hh], hp, hmax);
+              if (open) {
+                // open pairs wait for the end of the unit in the slots (more
+                // than fit: computed here); where the whole group is open
+                // its bracket values may exceed the exact ones, so none of
+                // them enters the amax (the exact values do, later)
+                if (open & kSwigluAll) hmax = 0;
+                uint4* defer = defer_slots();
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                  if (open & (1u << w)) {
+                    if (ndefer < kFc1DeferSlots) {
+                      defer[ndefer++] = make_uint4(ugw[hh][w], uuw[hh][w], (uint32_t)(c << 5 | hh << 3 | w), 0u);
+                    } else {
+                      hp[w] = swiglu_pair_exact(ugw[hh][w], uuw[hh][w]);
+                      hmax = __vmaxu2(hmax, hp[w] & 0x7FFF7FFFu);
+                    }
+                  }
+              }
+              amax2 = __vmaxu2(amax2, hmax);
             } else {
 #pragma unroll
               for (int w = 0; w < 8; ++w) hp[w] = 0u;
@@ -995,13 +1060,30 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
               dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
               dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
             }
-            scratch[(size_t)((c * FC1_PARTS + part) * 4 + 2 * hh) * BM + rl] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-            scratch[(size_t)((c * FC1_PARTS + part) * 4 + 2 * hh + 1) * BM + rl] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+            const size_t sv = (size_t)((c * FC1_VPARTS + part * FC1_SUB) * 4 + 2 * hh) * BM + rl;
+            scratch[sv] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            scratch[sv + BM] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
           }
         }
         if (have_prev && !ghost_prev && !*abort_flag)
-          requant_chunk(scr_prev, c, part, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf, d_ff);
+#pragma unroll
+          for (int sp = 0; sp < FC1_SUB; ++sp)
+            requant_chunk(scr_prev, c, part * FC1_SUB + sp, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf,
+                          d_ff);
       }
+      // deferred pairs: exact values over the bracket's in the staged h (and
+      // the debug copy), and into the row amax
+      for (int i = 0; i < ndefer; ++i) {
+        const uint4 en = defer_slots()[i];
+        const uint32_t hw = swiglu_pair_exact(en.x, en.y);
+        const int c = (int)(en.z >> 5), hh = (int)(en.z >> 3) & 3, w = (int)en.z & 7;
+        reinterpret_cast<uint32_t*>(scratch + (size_t)((c * FC1_VPARTS + part * FC1_SUB) * 4 + 2 * hh + (w >> 2)) * BM +
+                                    rl)[w & 3] = hw;
+        amax2 = __vmaxu2(amax2, hw & 0x7FFF7FFFu);
+        if (DBG && out && args.dbg_h)
+          reinterpret_cast<uint32_t*>(args.dbg_h + row * d_ff + c * BN + part * FC1_PART_COLS + hh * 16)[w] = hw;
+      }
+      ndefer = 0;
       // ---- outer scale of the unit's rows: amax over the full d_ff row ----
       tl->rowmax[part][rl] = __uint_as_float(__vmaxu2(amax2, amax2 >> 16) << 16);
       epi_barrier<FC1_NE>();
@@ -1021,7 +1103,9 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
     if (have_prev && !ghost_prev) {
       if (!*abort_flag)
         for (int c = 0; c < nch; ++c)
-          requant_chunk(scr_prev, c, part, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf, d_ff);
+          for (int sp = 0; sp < FC1_SUB; ++sp)
+            requant_chunk(scr_prev, c, part * FC1_SUB + sp, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf,
+                          d_ff);
       if (part == 0) args.h_g[row_prev] = g_prev;
     }
   }

@@ -74,8 +74,15 @@ struct Fc1Args {
   int rings, na, nb, resident;  // pipeline plan, set by launch_fc1
 };
 constexpr int kMaxGemmCtas = 256;
-// FC1 workspace: h staging, two 128 x d_ff BF16 buffers per CTA.
-inline size_t fc1_workspace_bytes(int d_ff) { return (size_t)kMaxGemmCtas * 2 * 128 * d_ff * 2; }
+constexpr int kFc1EpiThreads = 512;  // FC1 epilogue threads per CTA
+constexpr int kFc1DeferSlots = 16;   // deferred exact-SwiGLU fixes per epilogue thread and unit
+// FC1 workspace: h staging, two 128 x d_ff BF16 buffers per CTA, then
+// kFc1DeferSlots 16-byte slots per epilogue thread for the SwiGLU pairs
+// whose exact evaluation waits until the end of the unit.
+__host__ __device__ inline size_t fc1_staging_bytes(int d_ff) { return (size_t)kMaxGemmCtas * 2 * 128 * d_ff * 2; }
+inline size_t fc1_workspace_bytes(int d_ff) {
+  return fc1_staging_bytes(d_ff) + (size_t)kMaxGemmCtas * kFc1EpiThreads * kFc1DeferSlots * 16;
+}
 struct Fc2Args {
   CUtensorMap tmap_a, tmap_b;
   CUtensorMap tmap_out;  // output rows [m_cap][d] BF16 (z, or dy2 in MODE 2): boxes 64 x 32, 128-byte swizzle

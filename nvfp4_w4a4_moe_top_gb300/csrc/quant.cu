@@ -18,38 +18,25 @@ namespace moe {
 // and the non-finite check at once.  A row holding a NaN takes its amax over
 // the other values, as fmaxf does; its codes are unspecified and the status
 // bit reports it.
+
+// The row (K BF16 values) into the warp's registers.
 template <int NG>
-__global__ void __launch_bounds__(256) quantize_rows_kernel(
-    const uint16_t* __restrict__ src, int64_t src_rows, int K, const int32_t* __restrict__ row_map,
-    const float* __restrict__ amax, int64_t amax_rows, int64_t dst_rows, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ sf, float* __restrict__ gout, int* status, int nonfinite_bit) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= dst_rows) return;
-  const int kg = K / 64;
-  const int n8 = K / 8;  // 8-column vectors of the row
-  int64_t s = row_map ? (int64_t)row_map[r] : r;
-  if (s >= src_rows) {  // invalid map entry: write a zero row and flag it
-    if (lane == 0) set_status(status, MOE_STATUS_BAD_ROUTING);
-    s = -1;
-  }
-  uint4* crow = reinterpret_cast<uint4*>(codes + r * (K / 2));
-  const int64_t sf_row = (r >> 7) * kg * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-  if (s < 0) {
-    for (int i = lane; i < K / 32; i += 32) crow[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int c4 = lane; c4 < kg; c4 += 32) *reinterpret_cast<uint32_t*>(sf + sf_row + c4 * 512) = 0u;
-    if (lane == 0) gout[r] = 0.0f;
-    return;
-  }
-  const uint4* srow = reinterpret_cast<const uint4*>(src + s * (int64_t)K);
-  uint4 v[NG][4];
+__device__ __forceinline__ void load_row(const uint16_t* __restrict__ src_row, int K, int lane, uint4 (&v)[NG][4]) {
+  const uint4* srow = reinterpret_cast<const uint4*>(src_row);
+  const int n8 = K / 8;
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int e8 = g * 128 + 4 * lane;
 #pragma unroll
     for (int q = 0; q < 4; ++q) v[g][q] = e8 < n8 ? __ldg(srow + e8 + q) : make_uint4(0u, 0u, 0u, 0u);
   }
-  uint32_t bm[NG][2];  // magnitude bits of each block's largest |x|
+}
+
+// Largest magnitude of the row as BF16 magnitude bits, NaNs left out (warp
+// reduction); sets `nonfinite_bit` in status when the row holds a NaN or Inf.
+template <int NG>
+__device__ __forceinline__ uint32_t row_amax_bits(const uint4 (&v)[NG][4], uint32_t (&bm)[NG][2], int lane, int* status,
+                                                  int nonfinite_bit) {
   uint32_t lm = 0;
 #pragma unroll
   for (int g = 0; g < NG; ++g)
@@ -60,11 +47,20 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
     }
   const uint32_t rm = __reduce_max_sync(0xFFFFFFFFu, lm);
   if (rm >= 0x7F80u && lane == 0) set_status(status, nonfinite_bit);
-  float a;
-  if (amax)
-    a = amax[s / amax_rows];
-  else  // a NaN in the row (warp-uniform, rare): the largest other magnitude
-    a = __uint_as_float((rm <= 0x7F80u ? rm : __reduce_max_sync(0xFFFFFFFFu, absmax_bits_no_nan(v))) << 16);
+  // a NaN in the row (warp-uniform, rare): the largest other magnitude
+  return rm <= 0x7F80u ? rm : __reduce_max_sync(0xFFFFFFFFu, absmax_bits_no_nan(v));
+}
+
+// Codes, block scales and g of destination row r from the row in registers
+// (bm: its blocks' magnitude maxima) and the outer amax a.
+template <int NG>
+__device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32_t (&bm)[NG][2], float a, int64_t r,
+                                           int K, int lane, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                           float* __restrict__ gout) {
+  const int kg = K / 64;
+  const int n8 = K / 8;
+  uint4* crow = reinterpret_cast<uint4*>(codes + r * (K / 2));
+  const int64_t sf_row = (r >> 7) * kg * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
   const float gs = __fdiv_rn(a, 2688.0f);
   const float den = __fmul_rn(6.0f, gs);
 #pragma unroll
@@ -80,8 +76,9 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
         const uint32_t sb = e4m3_encode(__fdiv_rn(__uint_as_float(bm[g][b] << 16), den));
         const float S = __fmul_rn(gs, e4m3_decode(sb));
         if (S != 0.0f) {
-          c[2 * b] = e2m1_codes8(w0, S);
-          c[2 * b + 1] = e2m1_codes8(w1, S);
+          const uint2 cc = e2m1_codes16(w0, w1, S);
+          c[2 * b] = cc.x;
+          c[2 * b + 1] = cc.y;
         }
         sb2 |= sb << (8 * b);
       }
@@ -93,6 +90,36 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
     }
   }
   if (lane == 0) gout[r] = gs;
+}
+
+template <int NG>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(
+    const uint16_t* __restrict__ src, int64_t src_rows, int K, const int32_t* __restrict__ row_map,
+    const float* __restrict__ amax, int64_t amax_rows, int64_t dst_rows, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ sf, float* __restrict__ gout, int* status, int nonfinite_bit) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= dst_rows) return;
+  const int kg = K / 64;
+  int64_t s = row_map ? (int64_t)row_map[r] : r;
+  if (s >= src_rows) {  // invalid map entry: write a zero row and flag it
+    if (lane == 0) set_status(status, MOE_STATUS_BAD_ROUTING);
+    s = -1;
+  }
+  if (s < 0) {
+    uint4* crow = reinterpret_cast<uint4*>(codes + r * (K / 2));
+    const int64_t sf_row = (r >> 7) * kg * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+    for (int i = lane; i < K / 32; i += 32) crow[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int c4 = lane; c4 < kg; c4 += 32) *reinterpret_cast<uint32_t*>(sf + sf_row + c4 * 512) = 0u;
+    if (lane == 0) gout[r] = 0.0f;
+    return;
+  }
+  uint4 v[NG][4];
+  load_row<NG>(src + s * (int64_t)K, K, lane, v);
+  uint32_t bm[NG][2];
+  const uint32_t ab = row_amax_bits<NG>(v, bm, lane, status, nonfinite_bit);
+  const float a = amax ? amax[s / amax_rows] : __uint_as_float(ab << 16);
+  encode_row<NG>(v, bm, a, r, K, lane, codes, sf, gout);
 }
 
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,

@@ -371,8 +371,9 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
         sb = e4m3_encode(__fdiv_rn(ab, den));
         const float S = __fmul_rn(gs, e4m3_decode(sb));
         if (S != 0.0f) {
-          c[2 * b] = e2m1_codes8(w0, S);
-          c[2 * b + 1] = e2m1_codes8(w1, S);
+          const uint2 cc = e2m1_codes16(w0, w1, S);
+          c[2 * b] = cc.x;
+          c[2 * b + 1] = cc.y;
         }
       }
       sb2 |= sb << (8 * b);

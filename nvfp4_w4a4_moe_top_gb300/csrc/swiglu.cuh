@@ -192,6 +192,9 @@ __device__ __forceinline__ uint32_t swiglu_pair_fix(uint32_t gw, uint32_t uw) {
   return r0 | (r1 << 16);
 }
 
+// The exact pair, out of line: for rare fixes made away from the hot loop.
+__device__ __noinline__ uint32_t swiglu_pair_exact(uint32_t gw, uint32_t uw) { return swiglu_pair_fix(gw, uw); }
+
 // The 16 inputs of a group and its 8 result words, passed by value so that
 // the rare path below takes its arguments in registers.
 struct Swiglu16In {
@@ -211,11 +214,18 @@ __device__ __noinline__ Swiglu16Out swiglu16_rare(const Swiglu16In in, Swiglu16O
   return out;
 }
 
-// h of 16 elements (8 packed gate words, 8 packed up words) into 8 packed
-// BF16 words, exact; returns the largest |h| of the 16 as packed magnitude
-// bits (the larger of its two halves is the maximum).
-__device__ __forceinline__ uint32_t swiglu16(const uint32_t (&gw)[8], const uint32_t (&uw)[8], uint32_t (&h)[8]) {
-  uint32_t mask = 0, gmax = 0, hmax = 0, hmin = 0x7FFF7FFFu;
+// Bit of the swiglu16_fast mask that sends every pair of the group to the
+// exact path (a g below -16 or a result below 2^-100 somewhere in it).
+constexpr uint32_t kSwigluAll = 0x100u;
+
+// Tier 1 of 16 elements (8 packed gate words, 8 packed up words): h[w] is
+// the bracket's BF16 pair, exact unless bit w of the returned mask is set
+// (kSwigluAll: no pair may be trusted); hmax gets the largest |h| as packed
+// magnitude bits.
+__device__ __forceinline__ uint32_t swiglu16_fast(const uint32_t (&gw)[8], const uint32_t (&uw)[8], uint32_t (&h)[8],
+                                                  uint32_t& hmax) {
+  uint32_t mask = 0, gmax = 0, hmin = 0x7FFF7FFFu;
+  hmax = 0;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     uint32_t open;
@@ -227,24 +237,37 @@ __device__ __forceinline__ uint32_t swiglu16(const uint32_t (&gw)[8], const uint
     hmin = __vminu2(hmin, m);
   }
   if (max(gmax & 0xFFFFu, gmax >> 16) > kSwigluNegGmaxBits || min(hmin & 0xFFFFu, hmin >> 16) < kSwigluTinyBits)
-    mask = 0xFFu;
-  if (mask) {
-    Swiglu16In in;
-    Swiglu16Out o;
+    mask = kSwigluAll | 0xFFu;
+  return mask;
+}
+
+// The pairs of `mask` (bits 0-7) recomputed exactly, and hmax updated.
+__device__ __forceinline__ void swiglu16_fix(const uint32_t (&gw)[8], const uint32_t (&uw)[8], uint32_t (&h)[8],
+                                             uint32_t mask, uint32_t& hmax) {
+  Swiglu16In in;
+  Swiglu16Out o;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      in.g[w] = gw[w];
-      in.u[w] = uw[w];
-      o.h[w] = h[w];
-    }
-    o = swiglu16_rare(in, o, mask);
-    hmax = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      h[w] = o.h[w];
-      hmax = __vmaxu2(hmax, h[w] & 0x7FFF7FFFu);
-    }
+  for (int w = 0; w < 8; ++w) {
+    in.g[w] = gw[w];
+    in.u[w] = uw[w];
+    o.h[w] = h[w];
   }
+  o = swiglu16_rare(in, o, mask & 0xFFu);
+  hmax = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    h[w] = o.h[w];
+    hmax = __vmaxu2(hmax, h[w] & 0x7FFF7FFFu);
+  }
+}
+
+// h of 16 elements into 8 packed BF16 words, exact; returns the largest |h|
+// of the 16 as packed magnitude bits (the larger of its two halves is the
+// maximum).
+__device__ __forceinline__ uint32_t swiglu16(const uint32_t (&gw)[8], const uint32_t (&uw)[8], uint32_t (&h)[8]) {
+  uint32_t hmax;
+  const uint32_t mask = swiglu16_fast(gw, uw, h, hmax);
+  if (mask) swiglu16_fix(gw, uw, h, mask, hmax);
   return hmax;
 }
 

@@ -37,7 +37,8 @@ def test_helpers_match_oracle(L, orc):
     assert M.sf_bytes(10, 48) == 0
     assert M.status_string(-3) == "workspace too small"
     # h staging: two 128 x d_ff BF16 buffers per CTA, 256 CTAs at most
-    assert M.fc1_workspace_bytes(768) == 256 * 2 * 128 * 768 * 2
+    # h staging (two 128 x d_ff BF16 buffers per CTA) + 16 deferred-SwiGLU slots of 16 B per epilogue thread
+    assert M.fc1_workspace_bytes(768) == 256 * 2 * 128 * 768 * 2 + 256 * 512 * 16 * 16
     mc = M.m_cap(65536, 128, 8)
     assert M.backward_workspace_bytes(65536, 128, 8, 2048, 768) == mc * 2048 * 2 * 2 + mc * 1536 * 2 + mc * 2048 * 4
     assert M.backward_workspace_bytes(10, 4, 2, 200, 128) == 0

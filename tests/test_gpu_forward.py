@@ -21,12 +21,14 @@ pytestmark = pytest.mark.gpu
 # GEMMs run in the tensor cores' order, not the oracle's sequential order
 # (about 1e-7 relative); with h rounded exactly on both sides, what reaches
 # the output is a rare flip of a BF16 rounding: of u (which can move an h
-# code), of z, or of out itself.  Measured on GB300 over the configurations
-# below: rel-L2 at most 1.1e-5, no element off by more than one BF16 ulp of
-# the oracle's value (e.g. 7.8e-3 at |out| ~ 1.5 in the small layer, 1.2e-4
-# in the tiny one), and no h-code row different.  The bounds are those
-# figures with a margin: rel-L2 <= 2e-5, every element within one BF16 ulp
-# (so max-abs <= 2e-3 wherever |out| < 0.5), h-code rows differing <= 1e-3.
+# code), of one of the token's k slot values z = BF16(w y2), or of out itself.
+# Per element, then, out may differ from the oracle's by at most one BF16 ulp
+# of out plus one BF16 ulp of each of the k slot values (the oracle's) that
+# were summed into it: where the slots cancel, that is several ulps of out.
+# Measured on GB300 over the configurations below: rel-L2 at most 1.1e-5,
+# at most 0.5 of that per-element bound, no h-code row different.  The
+# checks: rel-L2 <= 2e-5, every element within the bound, h-code rows
+# differing <= 1e-3.
 E2E_REL_L2 = 2e-5
 H_ROWS_DIFFERING = 1e-3
 
@@ -58,13 +60,19 @@ def gpu_forward(lay, x, lg, W1=None, W2=None, w1q=None, w2q=None, status=True):
     return r, w1q, w2q
 
 
-def e2e_errors(got_bf16, exp_bf16):
-    """rel-L2, max-abs, and the largest difference in BF16 ulps of the
-    expected value (the spacing of BF16 values at |expected|)."""
+def bf16_ulp(v):
+    """Spacing of BF16 values at |v| (v in FP32)."""
+    return np.ldexp(1.0, np.frexp(np.maximum(np.abs(v), 2.0 ** -126))[1] - 8)
+
+
+def e2e_errors(got_bf16, exp_bf16, slots_bf16):
+    """rel-L2, max-abs, and the largest ratio of |got - expected| to the
+    per-element bound ulp(expected) + sum_j ulp(z_j), z_j the oracle's k slot
+    values [T][k][d] behind each output element."""
     from gpu_util import f32_of_bf16, rel_l2
     g, e = f32_of_bf16(got_bf16), f32_of_bf16(exp_bf16)
-    ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(e), 2.0 ** -126))[1] - 8)
-    return rel_l2(g, e), float(np.abs(g - e).max()), float((np.abs(g - e) / ulp).max())
+    bound = bf16_ulp(e) + bf16_ulp(f32_of_bf16(slots_bf16)).sum(axis=1)
+    return rel_l2(g, e), float(np.abs(g - e).max()), float((np.abs(g - e) / bound).max())
 
 
 def layer_of(name):
@@ -104,11 +112,11 @@ def test_forward_against_oracle(orc, name):
     assert np.array_equal(orc.unswizzle_sf(r["x_sf"], mp, lay.d), orc.unswizzle_sf(ref["x_sf"], mp, lay.d))
     # h codes: identical except rows touched by a rare accumulation-order flip
     row_diff = np.any(r["h_codes"][:mp] != ref["h_codes"][:mp], axis=1)
-    rel, mx, ulps = e2e_errors(r["out"], ref["out"])
-    print("%s: e2e rel-L2 %.3e max-abs %.3e (%.2f BF16 ulps), h-code rows differing %.5f"
-          % (name, rel, mx, ulps, row_diff.mean()))
+    rel, mx, ratio = e2e_errors(r["out"], ref["out"], ref["slots"])
+    print("%s: e2e rel-L2 %.3e max-abs %.3e (%.2f of the flip bound), h-code rows differing %.5f"
+          % (name, rel, mx, ratio, row_diff.mean()))
     assert row_diff.mean() <= H_ROWS_DIFFERING, row_diff.mean()
-    assert rel <= E2E_REL_L2 and ulps <= 1.0
+    assert rel <= E2E_REL_L2 and ratio <= 1.0
 
 
 @pytest.mark.parametrize("name", ["small", "ragged"])
@@ -234,7 +242,7 @@ def test_full_size_sampled_tokens(orc, name):
     tok = orc.TokenOracle(W1, W2, lay.k)
     T = lay.T
     sample = sorted(set([0, 1, T // 3, T // 2, T - 2, T - 1] + list(np.random.default_rng(0).integers(0, T, 6))))
-    got, exp = [], []
+    got, exp, slots = [], [], []
     for t in sample:
         o = tok.token(x[t], lg[t])
         for j in range(lay.k):
@@ -243,9 +251,10 @@ def test_full_size_sampled_tokens(orc, name):
             assert r["x_g"][row] == o["x_g"]
         got.append(r["out"][t])
         exp.append(o["out"])
-    rel, mx, ulps = e2e_errors(np.stack(got), np.stack(exp))
-    print("%s sampled %d tokens: rel-L2 %.3e max-abs %.3e (%.2f BF16 ulps)" % (name, len(sample), rel, mx, ulps))
-    assert rel <= E2E_REL_L2 and ulps <= 1.0
+        slots.append(o["slots"])
+    rel, mx, ratio = e2e_errors(np.stack(got), np.stack(exp), np.stack(slots))
+    print("%s sampled %d tokens: rel-L2 %.3e max-abs %.3e (%.2f of the flip bound)" % (name, len(sample), rel, mx, ratio))
+    assert rel <= E2E_REL_L2 and ratio <= 1.0
 
 
 def test_forward_timed_equals_forward(orc):

@@ -137,9 +137,9 @@ def test_forward_with_per_expert_weights(orc, name):
     assert np.array_equal(host(v["x_codes"])[:mp], ref["x_codes"][:mp])
     row_diff = np.any(host(v["h_codes"])[:mp] != ref["h_codes"][:mp], axis=1)
     from test_gpu_forward import E2E_REL_L2, H_ROWS_DIFFERING, e2e_errors
-    rel, mx, ulps = e2e_errors(host(out, np.uint16), ref["out"])
-    print("%s per-expert weights: e2e rel-L2 %.3e max-abs %.3e (%.2f BF16 ulps), h-code rows differing %.5f"
-          % (name, rel, mx, ulps, row_diff.mean()))
+    rel, mx, ratio = e2e_errors(host(out, np.uint16), ref["out"], ref["slots"])
+    print("%s per-expert weights: e2e rel-L2 %.3e max-abs %.3e (%.2f of the flip bound), h-code rows differing %.5f"
+          % (name, rel, mx, ratio, row_diff.mean()))
     # the same end-to-end tolerance as the per-row forward
     assert row_diff.mean() <= H_ROWS_DIFFERING
-    assert rel <= E2E_REL_L2 and ulps <= 1.0
+    assert rel <= E2E_REL_L2 and ratio <= 1.0

@@ -145,9 +145,23 @@ struct Tail {
 
 constexpr size_t TAIL_BYTES = (sizeof(Tail) + 1023) / 1024 * 1024;
 
+// The CTA's abort flag (in shared memory), held as its 32-bit shared
+// address: a wait raises it on timeout, and every role checks it.
+struct AbortFlag {
+  uint32_t addr;
+  __device__ __forceinline__ bool raised() const {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v != 0u;
+  }
+  __device__ __forceinline__ void raise() const {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(1u) : "memory");
+  }
+};
+
 // Poll the barrier; the abort flag and the wall clock are consulted only
 // every 256 failed polls, so a short wait costs nothing but the polls.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, AbortFlag abort_flag, int* status) {
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -156,9 +170,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
+    if (abort_flag.raised()) return false;
     if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-      *abort_flag = 1;
+      abort_flag.raise();
       set_status(status, MOE_STATUS_TIMEOUT);
       return false;
     }
@@ -169,7 +183,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 // and then take their own (immediately satisfied) look at the completed
 // phase, so a waiting warp costs the barrier unit one poller, not 32.  All
 // 32 lanes call it; the result is the same in every lane.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, AbortFlag abort_flag, int* status) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, status);
   ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -419,7 +433,7 @@ __device__ __forceinline__ void load_a_slice(uint32_t dst, const CUtensorMap* tm
 // Barrier wait of a producer: the single producer lane polls alone; with
 // GATHER the whole warp takes part (lane 0 polls).
 template <bool GATHER>
-__device__ __forceinline__ bool producer_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+__device__ __forceinline__ bool producer_wait(uint32_t bar, uint32_t parity, AbortFlag abort_flag, int* status) {
   return GATHER ? warp_wait(bar, parity, abort_flag, status) : wait_bounded(bar, parity, abort_flag, status);
 }
 
@@ -436,7 +450,7 @@ __device__ __forceinline__ bool producer_wait(uint32_t bar, uint32_t parity, vol
 template <bool GATHER>
 __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMap* tmap_b, const uint8_t* a_sf,
                               const uint8_t* b_sf, const Geometry& G, const ItemRows& rows, const int32_t* off, int E,
-                              uint32_t a_base, uint32_t ring_base, Tail* tl, volatile int* abort_flag, int* status,
+                              uint32_t a_base, uint32_t ring_base, Tail* tl, AbortFlag abort_flag, int* status,
                               const int32_t* a_rows, int zero_row) {
   const uint32_t b_off = G.b_off();
   const int lane = threadIdx.x & 31;
@@ -530,7 +544,7 @@ __device__ void producer_loop(int r, const CUtensorMap* tmap_a, const CUtensorMa
 // that the stage's operands and the A slice have landed (in a pair, in both
 // CTAs: all eight writer warps arrive on rank 0's barrier).
 __device__ void sf_writer_loop(int qd, const Geometry& G, const int32_t* off, int E, uint32_t ring_base, Tail* tl,
-                               uint32_t tmem, volatile int* abort_flag, int* status) {
+                               uint32_t tmem, AbortFlag abort_flag, int* status) {
   const int lane = threadIdx.x & 31;
   const uint32_t b_off = G.b_off();
   const uint32_t tq = tmem + ((uint32_t)(qd * 32) << 16);
@@ -600,7 +614,7 @@ __device__ void sf_writer_loop(int qd, const Geometry& G, const int32_t* off, in
 // tempty) also count arrivals from the peer's threads.
 template <bool PAIR>
 __device__ void mma_loop(const Geometry& G, const int32_t* off, int E, uint32_t a_base, uint32_t ring_base, Tail* tl,
-                         uint32_t tmem, volatile int* abort_flag, int* status) {
+                         uint32_t tmem, AbortFlag abort_flag, int* status) {
   // The per-k-step work of this single thread is the latency the tensor
   // pipe waits on, so everything that does not change per k-step is
   // computed here, and the ring position advances by increments: k-step kc
@@ -834,7 +848,7 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
                                                    const ItemRows& rows, const int32_t* off, int E, uint32_t a_base,
                                                    uint32_t ring_base, Tail* tl, int* status,
                                                    const int32_t* a_rows = nullptr, int zero_row = 0) {
-  volatile int* abort_flag = &tl->abort_flag;
+  const AbortFlag abort_flag{smem_u32(&tl->abort_flag)};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   using RL = Roles<NE>;
   if (warp >= RL::PROD && warp < RL::MMA) {
@@ -905,7 +919,7 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
   const uint32_t ring_base = a_base + (uint32_t)a_bytes;
   Tail* tl = setup<FC1_NE, PAIR>(smem + a_bytes + ring_bytes);
   float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
-  volatile int* abort_flag = &tl->abort_flag;
+  const AbortFlag abort_flag{smem_u32(&tl->abort_flag)};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ItemRows rows{true, 2 * d_ff, d_ff};
   // the accumulator release goes to rank 0's barrier, which counts both CTAs
@@ -921,23 +935,24 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
     // thread requantises its own row half of unit i - 1 from the other,
     // one chunk after each chunk of unit i (the thread reads back only what
     // it wrote, so program order is the only ordering needed).
-    uint4* scratch_cta = reinterpret_cast<uint4*>(args.scratch) + (size_t)blockIdx.x * 2 * (size_t)(d_ff / 8) * BM;
+    // (Pointers that live across the unit loop are recomputed where they are
+    // used, from the kernel parameters: fewer registers held in the loop.)
+    auto scratch_buf = [&](uint32_t parity) {
+      return reinterpret_cast<uint4*>(args.scratch) + ((size_t)blockIdx.x * 2 + parity) * (size_t)(d_ff / 8) * BM;
+    };
     // This thread's slots for SwiGLU pairs the bracket left open: their exact
     // values are computed at the end of the unit, so that the rare slow path
     // runs once per unit and not inside the item that met it (the next
     // accumulator release would wait for it).  Each slot: gate word, up word,
     // position (chunk << 5 | half << 3 | word).
-    // (The slot address is recomputed where it is used: it stays out of the
-    // registers of the hot loop.)
     auto defer_slots = [&]() {
       return reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(args.scratch) + fc1_staging_bytes(d_ff)) +
              ((size_t)blockIdx.x * kFc1EpiThreads + threadIdx.x) * kFc1DeferSlots;
     };
     int ndefer = 0;
     bool have_prev = false, ghost_prev = false;
-    int64_t row_prev = 0;
-    float g_prev = 0.0f, den_prev = 0.0f;
-    const uint4* scr_prev = scratch_cta;
+    int u_prev = 0;  // the previous unit's tile, staged in scratch_buf((uc - 1) & 1)
+    float g_prev = 0.0f;  // its outer scale (the block-scale divisor is 6 g_prev)
     uint32_t it = 0, uc = 0;
     UnitCursor cur;
     int u, e;
@@ -946,7 +961,6 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
       const int64_t row = (int64_t)u * BM + rl;
       const bool out = !PAIR || !ghost;  // a ghost tile computes but writes nothing
       const float ga = args.a_g[row];
-      uint4* scratch = scratch_cta + (size_t)(uc & 1) * (size_t)(d_ff / 8) * BM;
       // one buffer: every read of the previous unit's scales precedes the
       // end-of-unit barrier, which precedes this staging
       float* gws = gw_s;
@@ -959,7 +973,7 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
         const uint32_t sg = PAIR ? 0u : it % FC1_NSLOT, su = PAIR ? 0u : (it + 1) % FC1_NSLOT;
         const uint32_t gcol = PAIR ? 0u : sg * BN, ucol = PAIR ? (uint32_t)BN : su * BN;
         const int n0 = c * BN + part * FC1_PART_COLS;  // first h column of this thread
-        bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
+        bool ok = __all_sync(0xFFFFFFFFu, !abort_flag.raised());
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[sg]), (PAIR ? it : it / FC1_NSLOT) & 1u, abort_flag, args.status);
         if (ok && !PAIR) ok = warp_wait(smem_u32(&tl->tfull[su]), ((it + 1) / FC1_NSLOT) & 1u, abort_flag, args.status);
         // Drain: halves of 16 columns, gate and up of a half in one
@@ -1060,16 +1074,16 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
               dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
               dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
             }
-            const size_t sv = (size_t)((c * FC1_VPARTS + part * FC1_SUB) * 4 + 2 * hh) * BM + rl;
-            scratch[sv] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-            scratch[sv + BM] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+            uint4* sv = scratch_buf(uc & 1) + (size_t)((c * FC1_VPARTS + part * FC1_SUB) * 4 + 2 * hh) * BM + rl;
+            sv[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            sv[BM] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
           }
         }
-        if (have_prev && !ghost_prev && !*abort_flag)
+        if (have_prev && !ghost_prev && !abort_flag.raised())
 #pragma unroll
           for (int sp = 0; sp < FC1_SUB; ++sp)
-            requant_chunk(scr_prev, c, part * FC1_SUB + sp, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf,
-                          d_ff);
+            requant_chunk(scratch_buf((uc - 1) & 1), c, part * FC1_SUB + sp, rl, (int64_t)u_prev * BM + rl, g_prev,
+                          __fmul_rn(6.0f, g_prev), args.h_codes, args.h_sf, d_ff);
       }
       // deferred pairs: exact values over the bracket's in the staged h (and
       // the debug copy), and into the row amax
@@ -1077,8 +1091,9 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
         const uint4 en = defer_slots()[i];
         const uint32_t hw = swiglu_pair_exact(en.x, en.y);
         const int c = (int)(en.z >> 5), hh = (int)(en.z >> 3) & 3, w = (int)en.z & 7;
-        reinterpret_cast<uint32_t*>(scratch + (size_t)((c * FC1_VPARTS + part * FC1_SUB) * 4 + 2 * hh + (w >> 2)) * BM +
-                                    rl)[w & 3] = hw;
+        reinterpret_cast<uint32_t*>(scratch_buf(uc & 1) +
+                                    (size_t)((c * FC1_VPARTS + part * FC1_SUB) * 4 + 2 * hh + (w >> 2)) * BM + rl)[w & 3] =
+            hw;
         amax2 = __vmaxu2(amax2, hw & 0x7FFF7FFFu);
         if (DBG && out && args.dbg_h)
           reinterpret_cast<uint32_t*>(args.dbg_h + row * d_ff + c * BN + part * FC1_PART_COLS + hh * 16)[w] = hw;
@@ -1090,23 +1105,21 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
       float a = tl->rowmax[0][rl];
 #pragma unroll
       for (int p2 = 1; p2 < FC1_PARTS; ++p2) a = fmaxf(a, tl->rowmax[p2][rl]);
-      if (have_prev && !ghost_prev && part == 0) args.h_g[row_prev] = g_prev;
-      if (out && !*abort_flag && !is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
+      if (have_prev && !ghost_prev && part == 0) args.h_g[(int64_t)u_prev * BM + rl] = g_prev;
+      if (out && !abort_flag.raised() && !is_finite_f32(a)) set_status(args.status, MOE_STATUS_NONFINITE_X);
       have_prev = true;
       ghost_prev = !out;
-      row_prev = row;
+      u_prev = u;
       g_prev = __fdiv_rn(a, 2688.0f);
-      den_prev = __fmul_rn(6.0f, g_prev);
-      scr_prev = scratch;
     }
     // the last unit
     if (have_prev && !ghost_prev) {
-      if (!*abort_flag)
+      if (!abort_flag.raised())
         for (int c = 0; c < nch; ++c)
           for (int sp = 0; sp < FC1_SUB; ++sp)
-            requant_chunk(scr_prev, c, part * FC1_SUB + sp, rl, row_prev, g_prev, den_prev, args.h_codes, args.h_sf,
-                          d_ff);
-      if (part == 0) args.h_g[row_prev] = g_prev;
+            requant_chunk(scratch_buf((uc - 1) & 1), c, part * FC1_SUB + sp, rl, (int64_t)u_prev * BM + rl, g_prev,
+                          __fmul_rn(6.0f, g_prev), args.h_codes, args.h_sf, d_ff);
+      if (part == 0) args.h_g[(int64_t)u_prev * BM + rl] = g_prev;
     }
   }
   teardown<FC1_NE, PAIR>(tl);
@@ -1152,7 +1165,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
   const uint32_t ring_base = a_base + (uint32_t)a_bytes;
   Tail* tl = setup<FC2_NE>(smem + a_bytes + ring_bytes);
   float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
-  volatile int* abort_flag = &tl->abort_flag;
+  const AbortFlag abort_flag{smem_u32(&tl->abort_flag)};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ItemRows rows{false, d, args.d_ff};
   // per epilogue warp: 32 rows x 64 BF16 columns, 16-byte chunks XOR-swizzled by row
@@ -1194,7 +1207,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
       float dot = 0.0f;
       for (int nt = 0; nt < G.items; ++nt, ++it) {
         const uint32_t slot = it % FC2_NSLOT;
-        bool ok = __all_sync(0xFFFFFFFFu, !*abort_flag);
+        bool ok = __all_sync(0xFFFFFFFFu, !abort_flag.raised());
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[slot]), (it / FC2_NSLOT) & 1u, abort_flag, args.status);
         // Drain the accumulator (this thread's 64 columns) into registers,
         // release it to the MMA warp, then scale, weight and store.

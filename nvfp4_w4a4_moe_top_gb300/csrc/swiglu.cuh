@@ -3,15 +3,20 @@
 // execution specification: u = BF16(FC1 output), h = BF16(SwiGLU), one
 // rounding).  Three tiers, each exact where it answers:
 //
-//   1. Bracket (every element).  p = RN(RN(g * rcp(1 + ex2(g * -log2 e))) *
-//      up) with the hardware approximations; for g >= -16 its relative
-//      error plus 2^-24 is below kSwigluEps (the hardware terms of the bound
-//      are measured exhaustively by the tests).  The BF16 roundings of
-//      p * (1 - eps) and p * (1 + eps) bracket RN_bf16 of the exact value:
-//      when they agree, that is the answer.  Results below 2^-100 in
-//      magnitude (where a subnormal product or a zero would escape the
-//      relative bound) and g < -16 go to the next tier; the caller handles
-//      all-zero rows (pad rows) itself, whose h is zero.
+//   1. Bracket (every element).  e^-g = 2^(g C1) * 2^(g C2), where C1 + C2 =
+//      -log2 e and C1 carries 16 significant bits, so that g C1 is exact
+//      for a BF16 g; 2^(g C1) comes from the hardware ex2 and the small
+//      second factor from its first-order term, 1 + g C2 ln 2.  Then
+//      p = RN(RN(g * rcp(1 + E)) * up) with the hardware reciprocal, in
+//      packed f32x2 arithmetic.  Wherever the intermediates stay normal, p
+//      has a relative error below kSwigluEps - 2^-24 (the hardware terms of
+//      the bound are measured exhaustively by the tests), so the BF16
+//      roundings of p * (1 - eps) and p * (1 + eps) bracket RN_bf16 of the
+//      exact value: when they agree, that is the answer.  Where E overflows
+//      or the reciprocal underflows (g < -87) p is zero; zero and results
+//      below 2^-100 in magnitude (where a subnormal product would escape the
+//      relative bound) go to the next tier; the caller handles all-zero
+//      rows (pad rows) itself, whose h is zero.
 //   2. Double-float (elements the bracket leaves open, about one in 2000).
 //      e^-g by Tang's table-driven method (P. T. P. Tang, ACM TOMS 15(2),
 //      1989: g = k ln2/64 + r, e^r by its Taylor polynomial, 2^(j/64) from a
@@ -23,14 +28,13 @@
 //      g / (1 + exp(-g)) * up in double, rounded to BF16 through
 //      round-to-odd single precision (which keeps the one rounding exact).
 //
-// Error bound of tier 1 (relative): the argument g * -log2 e is rounded once
-// and the constant carries 9.3e-9 relative error, which moves e^-g by
-// |g| * 6.9e-8 relative; that error reaches 1 + e^-g scaled by
-// e^-g / (1 + e^-g), so it stays below 0.28 * 6.9e-8 for g >= 0 and below
-// 16 * 6.9e-8 for -16 <= g < 0.  ex2 and rcp add their maxima (2^-22.7 and
-// 2^-23.3 measured over every input they see here), three roundings add
-// 3 * 2^-24, and the bracket products' own rounding 2^-24 more: 1.59e-6 in
-// all, under kSwigluEps = 1.67e-6.
+// Error bound of tier 1 (relative): ex2 of the exact argument (2^-22.7,
+// its maximum measured over every input it sees); the first-order factor
+// drops (g C2 ln 2)^2 / 2 <= 9.4e-8 (|g| <= 88.7, beyond which E is
+// infinite) and rounds once (2^-24); these errors reach 1 + E scaled by
+// E / (1 + E) <= 1.  The reciprocal adds 2^-23.3 (measured), the roundings
+// of 1 + E, of g * r and of p three times 2^-24, and the bracket products'
+// own rounding 2^-24: 6.35e-7 in all, under kSwigluEps = 7.15e-7.
 #pragma once
 
 #include "common.cuh"
@@ -38,13 +42,14 @@
 
 namespace moe {
 
-constexpr float kNegLog2e = -1.4426950408889634f;
-constexpr float kSwigluGmax = 16.0f;                  // the bracket serves g >= -kSwigluGmax
-constexpr uint32_t kSwigluNegGmaxBits = 0xC180u;      // BF16 pattern of -16.0: larger patterns are g < -16
+// -log2 e = kNegLog2eHi + C2 with kNegLog2eHi = -47274 / 2^15 (16
+// significant bits); kNegLog2eLoLn2 = RN(C2 ln 2)
+constexpr float kNegLog2eHi = -0x1.7154p+0f;
+constexpr float kNegLog2eLoLn2 = -0x1.480fb6p-18f;
 // tier-1 half-width of the bracket: the error bound of p (see above) plus
 // 2^-24 for the rounding of the bracket products, a multiple of 2^-23 so
 // that 1 -+ eps are exact floats
-constexpr float kSwigluEps = 0x1.Cp-20f;              // 14 * 2^-23 = 1.67e-6
+constexpr float kSwigluEps = 0x1.8p-21f;              // 6 * 2^-23 = 7.15e-7
 constexpr uint32_t kSwigluTinyBits = 0x0D80u;         // BF16 pattern of 2^-100
 
 __device__ __forceinline__ float ex2_ftz(float x) {
@@ -85,9 +90,12 @@ __device__ __forceinline__ uint32_t bf16x2_of(uint64_t v) {
 __device__ __forceinline__ uint32_t swiglu_pair_fast(uint32_t gw, uint32_t uw, uint32_t& open) {
   const uint64_t z = f32x2_bits(bf16_lo(gw), bf16_hi(gw));
   float t0, t1;
-  f32x2_unpack(mul_f32x2(z, f32x2_bits(kNegLog2e, kNegLog2e)), t0, t1);
+  f32x2_unpack(mul_f32x2(z, f32x2_bits(kNegLog2eHi, kNegLog2eHi)), t0, t1);  // exact
+  const uint64_t dl = mul_f32x2(z, f32x2_bits(kNegLog2eLoLn2, kNegLog2eLoLn2));
+  uint64_t E = f32x2_bits(ex2_ftz(t0), ex2_ftz(t1));
+  E = fma_f32x2(E, dl, E);  // E (1 + g C2 ln 2)
   float d0, d1;
-  f32x2_unpack(add_f32x2(f32x2_bits(ex2_ftz(t0), ex2_ftz(t1)), f32x2_bits(1.0f, 1.0f)), d0, d1);
+  f32x2_unpack(add_f32x2(E, f32x2_bits(1.0f, 1.0f)), d0, d1);
   const uint64_t s = mul_f32x2(z, f32x2_bits(rcp_ftz(d0), rcp_ftz(d1)));
   const uint64_t p = mul_f32x2(s, f32x2_bits(bf16_lo(uw), bf16_hi(uw)));
   const uint32_t lo = bf16x2_of(mul_f32x2(p, f32x2_bits(1.0f - kSwigluEps, 1.0f - kSwigluEps)));
@@ -174,11 +182,9 @@ __device__ __noinline__ uint32_t swiglu_bf16_exact(float g, float up) {
 }
 
 // True when the bracket cannot decide half `sh` (0 or 16) of a pair: open,
-// g < -16 (or a non-finite pattern above it), or a result below 2^-100 in
-// magnitude (zero included).
-__device__ __forceinline__ bool swiglu_half_open(uint32_t gw, uint32_t lo, uint32_t open, int sh) {
-  return ((open >> sh) & 0xFFFFu) != 0u || ((gw >> sh) & 0xFFFFu) > kSwigluNegGmaxBits ||
-         ((lo >> sh) & 0x7FFFu) < kSwigluTinyBits;
+// or a result below 2^-100 in magnitude (zero included).
+__device__ __forceinline__ bool swiglu_half_open(uint32_t lo, uint32_t open, int sh) {
+  return ((open >> sh) & 0xFFFFu) != 0u || ((lo >> sh) & 0x7FFFu) < kSwigluTinyBits;
 }
 
 // The exact pair: each half from the bracket where it decides, else from
@@ -187,8 +193,8 @@ __device__ __forceinline__ uint32_t swiglu_pair_fix(uint32_t gw, uint32_t uw) {
   uint32_t open;
   const uint32_t lo = swiglu_pair_fast(gw, uw, open);
   uint32_t r0 = lo & 0xFFFFu, r1 = lo >> 16;
-  if (swiglu_half_open(gw, lo, open, 0)) r0 = swiglu_bf16_exact(bf16_lo(gw), bf16_lo(uw));
-  if (swiglu_half_open(gw, lo, open, 16)) r1 = swiglu_bf16_exact(bf16_hi(gw), bf16_hi(uw));
+  if (swiglu_half_open(lo, open, 0)) r0 = swiglu_bf16_exact(bf16_lo(gw), bf16_lo(uw));
+  if (swiglu_half_open(lo, open, 16)) r1 = swiglu_bf16_exact(bf16_hi(gw), bf16_hi(uw));
   return r0 | (r1 << 16);
 }
 
@@ -215,7 +221,7 @@ __device__ __noinline__ Swiglu16Out swiglu16_rare(const Swiglu16In in, Swiglu16O
 }
 
 // Bit of the swiglu16_fast mask that sends every pair of the group to the
-// exact path (a g below -16 or a result below 2^-100 somewhere in it).
+// exact path (a result below 2^-100, or zero, somewhere in it).
 constexpr uint32_t kSwigluAll = 0x100u;
 
 // Tier 1 of 16 elements (8 packed gate words, 8 packed up words): h[w] is
@@ -224,20 +230,18 @@ constexpr uint32_t kSwigluAll = 0x100u;
 // magnitude bits.
 __device__ __forceinline__ uint32_t swiglu16_fast(const uint32_t (&gw)[8], const uint32_t (&uw)[8], uint32_t (&h)[8],
                                                   uint32_t& hmax) {
-  uint32_t mask = 0, gmax = 0, hmin = 0x7FFF7FFFu;
+  uint32_t mask = 0, hmin = 0x7FFF7FFFu;
   hmax = 0;
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     uint32_t open;
     h[w] = swiglu_pair_fast(gw[w], uw[w], open);
     mask |= (open != 0u ? 1u : 0u) << w;
-    gmax = __vmaxu2(gmax, gw[w]);
     const uint32_t m = h[w] & 0x7FFF7FFFu;
     hmax = __vmaxu2(hmax, m);
     hmin = __vminu2(hmin, m);
   }
-  if (max(gmax & 0xFFFFu, gmax >> 16) > kSwigluNegGmaxBits || min(hmin & 0xFFFFu, hmin >> 16) < kSwigluTinyBits)
-    mask = kSwigluAll | 0xFFu;
+  if (min(hmin & 0xFFFFu, hmin >> 16) < kSwigluTinyBits) mask = kSwigluAll | 0xFFu;
   return mask;
 }
 

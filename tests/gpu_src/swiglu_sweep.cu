@@ -8,19 +8,26 @@ namespace {
 __device__ __forceinline__ bool finite_bf16(uint32_t b) { return (b & 0x7F80u) != 0x7F80u; }
 
 // Largest relative error of ex2.approx.ftz over every float t with
-// 2^-30 <= |t| <= 24, and of rcp.approx.ftz over every float in [1, 2^25)
-// (float bits of the maxima: non-negative floats order like their bits).
+// 2^-30 <= |t| <= 128 and a normal result (below 2^-30 the result is 1 or
+// its neighbour, within 2^-30 of 2^t), and of rcp.approx.ftz over every float
+// in [1, 2^126) (float bits of the maxima: non-negative floats order like
+// their bits).  The bracket's exponent argument g * kNegLog2eHi of any
+// finite BF16 g, and its 1 + E, lie in these ranges wherever the result is
+// not flagged for the exact tiers.
 __global__ void hw_bounds(unsigned int* out) {
   const unsigned int stride = gridDim.x * blockDim.x;
   const unsigned int i0 = blockIdx.x * blockDim.x + threadIdx.x;
   float e_ex2 = 0.0f, e_rcp = 0.0f;
-  for (unsigned int b = 0x30800000u + i0; b <= 0x41C00000u; b += stride)
+  for (unsigned int b = 0x30800000u + i0; b <= 0x43000000u; b += stride)
     for (unsigned int s = 0; s < 2; ++s) {
       const float t = __uint_as_float(b | (s << 31));
+      if (t < -126.0f) continue;
+      const float y = moe::ex2_ftz(t);
+      if (isinf(y)) continue;  // an infinite E makes p zero, which the exact tiers take
       const double r = exp2((double)t);
-      e_ex2 = fmaxf(e_ex2, (float)(fabs((double)moe::ex2_ftz(t) - r) / r));
+      e_ex2 = fmaxf(e_ex2, (float)(fabs((double)y - r) / r));
     }
-  for (unsigned int b = 0x3F800000u + i0; b < 0x4C000000u; b += stride) {
+  for (unsigned int b = 0x3F800000u + i0; b < 0x7E800000u; b += stride) {
     const float D = __uint_as_float(b);
     const double r = 1.0 / (double)D;
     e_rcp = fmaxf(e_rcp, (float)(fabs((double)moe::rcp_ftz(D) - r) / r));
@@ -31,7 +38,7 @@ __global__ void hw_bounds(unsigned int* out) {
 
 // Every pair of finite BF16 values (g, up): h from swiglu16 (16 up values
 // per call, one g) against the FP64 tier; counts mismatches, and how many
-// halves the bracket left open (g >= -16 and |h| >= 2^-100 only).
+// halves the bracket left open (|h| >= 2^-100 only).
 __global__ void sweep_all(unsigned long long* out) {
   unsigned long long bad = 0, open_n = 0, tested = 0;
   const uint32_t gb = blockIdx.x;  // 65536 blocks: one g each
@@ -55,7 +62,7 @@ __global__ void sweep_all(unsigned long long* out) {
         ++tested;
         const uint32_t ref = moe::swiglu_bf16_f64(g, moe::bf16_bits_to_f32(ub));
         if (((h[w] >> (16 * hf)) & 0xFFFFu) != ref) ++bad;
-        if (((open >> (16 * hf)) & 0xFFFFu) && g >= -16.0f && ((lo >> (16 * hf)) & 0x7FFFu) >= 0x0D80u) ++open_n;
+        if (((open >> (16 * hf)) & 0xFFFFu) && ((lo >> (16 * hf)) & 0x7FFFu) >= 0x0D80u) ++open_n;
       }
     }
   }
@@ -99,7 +106,8 @@ __global__ void eval_pairs(const uint16_t* g, const uint16_t* up, uint16_t* h, i
 }  // namespace
 
 extern "C" float swiglu_eps() { return moe::kSwigluEps; }
-extern "C" float swiglu_gmax() { return moe::kSwigluGmax; }
+extern "C" float swiglu_c1() { return moe::kNegLog2eHi; }
+extern "C" float swiglu_c2ln2() { return moe::kNegLog2eLoLn2; }
 
 extern "C" int run_hw_bounds(float* e_ex2, float* e_rcp) {
   unsigned int* d;

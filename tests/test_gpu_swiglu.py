@@ -24,7 +24,8 @@ def _lib():
     from gpu_util import build_test_so
     L = ctypes.CDLL(build_test_so("swiglu_sweep"))
     L.swiglu_eps.restype = ctypes.c_float
-    L.swiglu_gmax.restype = ctypes.c_float
+    L.swiglu_c1.restype = ctypes.c_float
+    L.swiglu_c2ln2.restype = ctypes.c_float
     return L
 
 
@@ -32,11 +33,16 @@ def test_bracket_covers_hardware_error():
     L = _lib()
     e_ex2, e_rcp = ctypes.c_float(), ctypes.c_float()
     assert L.run_hw_bounds(ctypes.byref(e_ex2), ctypes.byref(e_rcp)) == 0
-    # relative error bound of the fast value p for g >= -gmax: the rounded
-    # argument (one rounding plus the constant's 9.3e-9) moves e^-g by
-    # |g| * 6.9e-8; ex2 and rcp; three roundings; plus 2^-24 for the
-    # rounding of the bracket products
-    bound = L.swiglu_gmax() * 6.9e-8 + e_ex2.value + e_rcp.value + 3 * 2.0 ** -24 + 2.0 ** -24
+    # relative error bound of the fast value p: ex2 of the exact argument
+    # g * C1; the first-order factor 1 + g C2 ln 2 drops (g C2 ln 2)^2 / 2
+    # for |g| up to 128 / |C1| (beyond, E overflows and p is flagged) and
+    # rounds once (fma); the reciprocal; the roundings of 1 + E, g * r and p;
+    # plus 2^-24 for the rounding of the bracket products
+    c1, c2 = abs(L.swiglu_c1()), abs(L.swiglu_c2ln2())
+    assert c1 * 2 ** 15 == int(c1 * 2 ** 15) and int(c1 * 2 ** 15) < 2 ** 16  # 16 significant bits
+    assert abs(c1 + c2 / np.log(2) - 1 / np.log(2)) < 1e-12  # C1 + C2 = log2 e
+    dmax = 128.0 / c1 * c2
+    bound = e_ex2.value + dmax ** 2 / 2 + 2.0 ** -24 + e_rcp.value + 3 * 2.0 ** -24 + 2.0 ** -24
     print("ex2.approx.ftz max rel %.3e, rcp.approx.ftz max rel %.3e, needed eps %.3e, eps %.3e"
           % (e_ex2.value, e_rcp.value, bound, L.swiglu_eps()))
     assert 0 < e_ex2.value < 1e-5 and 0 < e_rcp.value < 1e-5
@@ -52,9 +58,10 @@ def test_swiglu_all_bf16_pairs():
     print("all pairs: %d mismatches, tier 2 alone %d mismatches; bracket open on %.3e of the pairs"
           % (bad.value, bad2.value, open_n.value / tested.value))
     assert bad.value == 0 and bad2.value == 0
-    # over all pairs the bracket leaves about 0.5% open: besides straddles of
-    # a midpoint, for large g the product g * up of two 8-bit significands
-    # is often itself a BF16 midpoint, which p * (1 -+ eps) always straddles
+    # over all pairs the bracket leaves well under 1% open: besides
+    # straddles of a midpoint, for large g the product g * up of two 8-bit
+    # significands is often itself a BF16 midpoint, which p * (1 -+ eps)
+    # always straddles
     assert open_n.value / tested.value < 1e-2
 
 

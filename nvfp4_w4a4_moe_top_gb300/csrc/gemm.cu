@@ -95,6 +95,7 @@ constexpr int FC2_NSLOT = 2;                           // FC2: double buffering
 // columns each, 80 registers per thread); FC2's light epilogue keeps 8 warps
 // of 64 columns at 128 registers.
 constexpr int FC1_NE = 16, FC2_NE = 8;
+constexpr int FC2P_NE = 16;  // FC2 on CTA pairs: 4 column parts of 64 of the 256-column accumulator
 static_assert(FC1_NE * 32 <= kFc1EpiThreads, "FC1 epilogue threads");
 constexpr int FC1_PARTS = FC1_NE / 4, FC1_PART_COLS = BN / FC1_PARTS;  // column parts of a chunk, one per warp
 // h is staged and requantised in 32-column sub-parts (two 16-element blocks,
@@ -1303,6 +1304,159 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
   teardown<FC2_NE>(tl);
 }
 
+
+// FC2 on CTA pairs (the forward; MODE 0 and 1): clusters of two CTAs, a
+// unit being two 128-row tiles of one expert, walked as FC1's pair units
+// (ghost tile included).  An item is 256 output columns: rank 0's B tile
+// holds W2 rows nt*256 .. +127, rank 1's the next 128; one cta_group::2 MMA
+// of M = 256, N = 256, K = 64 per 64-deep K group into one 256-column
+// accumulator per CTA.  16 epilogue warps: warp w drains TMEM lane quadrant
+// w % 4 and accumulator columns 64 (w / 4) .., in two round trips of 32
+// columns; the accumulator is released (to rank 0's barrier) once the
+// second round trip has landed; z = BF16(w * acc * (g_h * g_w2)) goes
+// through the warp's swizzled 32 x 64 staging tile to one TMA tensor store,
+// as in the single-CTA kernel.  A ghost tile computes but stores nothing.
+template <bool DBG>
+__global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(const __grid_constant__ Fc2Args args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int d = args.d, k = args.k;
+  Geometry G;
+  G.num_mt = __ldg(args.offsets + args.E) / BM;
+  G.pair = true;
+  G.rank = cluster_rank();
+  G.cluster = (int)cluster_id_x();
+  G.nclusters = (int)cluster_count_x();
+  G.b_bytes = B_BYTES;
+  G.sfb_tiles = 2;
+  G.acc_cols = PAIR_ACC_COLS;
+  G.sf_cols = PAIR_SF_COLS;
+  G.items = d / (2 * BN);
+  G.nk = (args.d_ff + 255) / 256;
+  G.kgroups = args.d_ff / 64;
+  G.rings = args.rings;
+  G.log2_stages = 0;
+  G.nslot = 1;
+  G.resident = true;
+  G.stage_bytes = G.b_bytes + 3 * SF_STAGE;
+  const uint32_t a_base = smem_u32(smem);
+  const size_t a_bytes = (size_t)G.nk * A_SLICE;
+  const size_t ring_bytes = (size_t)G.rings * G.stage_bytes;
+  const uint32_t ring_base = a_base + (uint32_t)a_bytes;
+  Tail* tl = setup<FC2P_NE, true>(smem + a_bytes + ring_bytes);
+  float* gw_s = reinterpret_cast<float*>(smem + a_bytes + ring_bytes + TAIL_BYTES);
+  const AbortFlag abort_flag{smem_u32(&tl->abort_flag)};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ItemRows rows{false, d, args.d_ff};
+  const uint32_t stg = smem_u32(smem + a_bytes + ring_bytes + TAIL_BYTES + (size_t)2 * d * 4) +
+                       (uint32_t)(warp < FC2P_NE ? warp : 0) * 32 * FC2_STAGE_ROW;
+  const uint32_t tempty0 = map_to_rank(smem_u32(&tl->tempty[0]), 0);
+
+  if (run_pipeline_roles<FC2P_NE, true>(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets,
+                                        args.E, a_base, ring_base, tl, args.status)) {
+    const int q4 = warp & 3, part = warp >> 2;  // part: accumulator columns 64*part ..
+    const int rl = q4 * 32 + lane;
+    const uint32_t tmem = tl->tmem_base + ((uint32_t)(q4 * 32) << 16) + part * 64;
+    uint32_t it = 0, uc = 0;
+    bool stores = false;  // lane 0: a tensor store of this warp may be in flight
+    if (lane == 0) prefetch_tmap(&args.tmap_out);
+    UnitCursor cur;
+    int u, e;
+    bool ghost;
+    for (int iu = 0; unit_at(G, args.offsets, args.E, iu, cur, u, e, ghost); ++iu, ++uc) {
+      const int64_t row = (int64_t)u * BM + rl;
+      const int t = args.row_to_token[row];
+      float w = 0.0f;
+      if (t >= 0) {
+        // slot of this row among the token's k (loads issued eight at a time)
+        const int32_t* ts = args.token_slot_row + (int64_t)t * k;
+        int j = 0;
+        for (int j0 = 0; j0 < k; j0 += 8) {
+          int v8[8];
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) v8[q8] = j0 + q8 < k ? ts[j0 + q8] : -1;
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8)
+            if (v8[q8] == (int)row) j = j0 + q8;
+        }
+        w = args.topk_w[(int64_t)t * k + j];
+      }
+      const float gh = args.a_g[row];
+      float* gws = gw_s + (uc & 1) * d;
+      stage_scales<FC2P_NE>(gws, args.w_g + (int64_t)e * d, d, threadIdx.x);
+      epi_barrier<FC2P_NE>();
+      for (int nt = 0; nt < G.items; ++nt, ++it) {
+        bool ok = __all_sync(0xFFFFFFFFu, !abort_flag.raised());
+        if (ok) ok = warp_wait(smem_u32(&tl->tfull[0]), it & 1u, abort_flag, args.status);
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty0);
+        };
+        uint32_t zp[32];  // the row's 64 z values, packed pairs
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t R[2][16];
+            tmem_ld16(tmem + hh * 32, R[0]);
+            tmem_ld16(tmem + hh * 32 + 16, R[1]);
+            tmem_wait_ld();
+            if (hh == 1) release();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int c0 = hh * 32 + hf * 16;  // column within the warp's 64
+              const int n0 = nt * 2 * BN + part * 64 + c0;
+              float yv[16];
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                const float4 f4 = *reinterpret_cast<const float4*>(gws + n0 + i);
+                const float f[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+                for (int jj = 0; jj < 4; jj += 2) {
+                  const int m = i + jj;
+                  const float y0 = __fmul_rn(__uint_as_float(R[hf][m]), __fmul_rn(gh, f[jj]));
+                  const float y1 = __fmul_rn(__uint_as_float(R[hf][m + 1]), __fmul_rn(gh, f[jj + 1]));
+                  zp[(c0 + m) >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
+                  yv[m] = y0;
+                  yv[m + 1] = y1;
+                }
+              }
+              if (DBG && args.dbg_y && t >= 0 && !ghost) {
+                float4* y4 = reinterpret_cast<float4*>(args.dbg_y + row * d + n0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) y4[q] = make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
+              }
+            }
+          }
+        } else {
+          release();
+        }
+        if (ok && !ghost) {
+          // the staging tile is free once the previous store has read it
+          if (lane == 0 && stores) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            sts128(stg + lane * FC2_STAGE_ROW + 16 * (ch ^ (lane & 7)), zp[4 * ch], zp[4 * ch + 1], zp[4 * ch + 2],
+                   zp[4 * ch + 3]);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&args.tmap_out, stg, nt * 2 * BN + part * 64, u * BM + q4 * 32);
+            stores = true;
+          }
+        }
+      }
+      // every read of this unit's scale buffer precedes the barrier that
+      // precedes the staging of the unit after next into it
+    }
+    if (lane == 0 && stores) bulk_wait0();  // the stores complete before the CTA exits
+    __syncwarp();
+  }
+  teardown<FC2P_NE, true>(tl);
+}
+
 // ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
@@ -1370,12 +1524,12 @@ static int fc_grid(int64_t m_cap) {
 // CTA-pair plan: A resident, PAIR_RINGS_MAX (or one fewer) rings of one
 // PAIR_STAGE stage each, PAIR_SFBUF scale buffers after the accumulator.
 // The a_empty reach rule is the single-CTA plan's.
-static bool plan_pair(int K, int items, size_t scale_bytes, int* rings, size_t* smem) {
+static bool plan_pair(int K, int items, size_t scale_bytes, size_t extra, int* rings, size_t* smem) {
   const int nk = (K + 255) / 256;
   if (PAIR_ACC_COLS + PAIR_SFBUF * PAIR_SF_COLS > TMEM_COLS) return false;
   for (int R = PAIR_RINGS_MAX; R >= PAIR_RINGS_MAX - 1; --R) {
     if (nk > MAX_A_SLOTS || (int64_t)(items + 1) * nk < R) continue;
-    const size_t need = 1024 + TAIL_BYTES + scale_bytes + (size_t)nk * A_SLICE + (size_t)R * PAIR_STAGE;
+    const size_t need = 1024 + TAIL_BYTES + scale_bytes + extra + (size_t)nk * A_SLICE + (size_t)R * PAIR_STAGE;
     if (need > (size_t)SMEM_LIMIT) continue;
     *rings = R;
     *smem = need;
@@ -1384,11 +1538,12 @@ static bool plan_pair(int K, int items, size_t scale_bytes, int* rings, size_t* 
   return false;
 }
 
-// Clusters of two that can be resident at once with `smem` bytes per CTA
-// (the occupancy query is cached per host thread, keyed by device, kernel
-// and shared-memory size).
-static int pair_clusters(void (*kern)(const Fc1Args), size_t smem) {
-  thread_local void (*cached_kern)(const Fc1Args) = nullptr;
+// Clusters of two that can be resident at once with `smem` bytes per CTA of
+// `threads` threads (the occupancy query is cached per host thread, keyed by
+// device, kernel and shared-memory size).
+template <class Args>
+static int pair_clusters(void (*kern)(const Args), size_t smem, int threads) {
+  thread_local void (*cached_kern)(const Args) = nullptr;
   thread_local size_t cached_smem = 0;
   thread_local int cached_dev = -1, cached = 0;
   int dev = -1;
@@ -1396,7 +1551,7 @@ static int pair_clusters(void (*kern)(const Fc1Args), size_t smem) {
   if (kern == cached_kern && smem == cached_smem && dev == cached_dev) return cached;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(Roles<FC1_NE>::THREADS);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1427,10 +1582,10 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
   const bool allow_pairs = !(env && env[0] == '0');
   size_t smem;
   int pair_rings = 0;
-  if (allow_pairs && plan_pair(a.d, a.d_ff / BN, (size_t)2 * a.d_ff * 4, &pair_rings, &smem)) {
+  if (allow_pairs && plan_pair(a.d, a.d_ff / BN, (size_t)2 * a.d_ff * 4, 0, &pair_rings, &smem)) {
     void (*kern)(const Fc1Args) = dbg ? fc1_swiglu_kernel<true, true> : fc1_swiglu_kernel<false, true>;
     if (set_smem((const void*)kern, smem) != 0) return -1;
-    int clusters = pair_clusters(kern, smem);
+    int clusters = pair_clusters(kern, smem, Roles<FC1_NE>::THREADS);
     const int sms = gemm_num_ctas();
     if (sms > 0 && clusters > sms / 2) clusters = sms / 2;
     // every pair unit holds at least one of the m_cap / 128 tiles (the device
@@ -1467,8 +1622,44 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
   return 0;
 }
 
+// FC2 runs on CTA pairs (clusters of two) for the forward where the pair
+// plan fits, d is a multiple of 256 and clusters of two can be resident;
+// the backward's recomputation (dw set) runs on single CTAs.
+// MOE_FC2_CTA_PAIRS=0 in the environment selects single CTAs throughout.
 int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream) {
   size_t smem;
+  const char* env = std::getenv("MOE_FC2_CTA_PAIRS");
+  const bool allow_pairs = !(env && env[0] == '0') && a.dw == nullptr && a.d % (2 * BN) == 0;
+  int pair_rings = 0;
+  if (allow_pairs && plan_pair(a.d_ff, a.d / (2 * BN), (size_t)2 * a.d * 4, (size_t)FC2P_NE * 32 * FC2_STAGE_ROW,
+                               &pair_rings, &smem)) {
+    void (*kern)(const Fc2Args) = a.dbg_y != nullptr ? fc2_pair_kernel<true> : fc2_pair_kernel<false>;
+    if (set_smem((const void*)kern, smem) != 0) return -1;
+    int clusters = pair_clusters(kern, smem, Roles<FC2P_NE>::THREADS);
+    const int sms = gemm_num_ctas();
+    if (sms > 0 && clusters > sms / 2) clusters = sms / 2;
+    const int64_t pair_units = m_cap / BM;
+    if (pair_units < clusters) clusters = (int)pair_units;
+    if (clusters >= 1) {
+      a.rings = pair_rings;
+      a.nb = 1;
+      a.resident = 1;
+      a.na = (a.d_ff + 255) / 256;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(2 * clusters));
+      cfg.blockDim = dim3(Roles<FC2P_NE>::THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? 0 : -1;
+    }
+  }
   if (!plan(a.d_ff, a.d / BN, (size_t)2 * a.d * 4, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident,
             &smem))
     return -1;

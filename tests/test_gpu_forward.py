@@ -119,20 +119,26 @@ def test_forward_against_oracle(orc, name):
     assert rel <= E2E_REL_L2 and ratio <= 1.0
 
 
-@pytest.mark.parametrize("name", ["small", "ragged"])
+@pytest.mark.parametrize("name", ["small", "ragged", "tiny"])
 def test_forward_cta_pairs_equal_single(orc, name, monkeypatch):
-    """The forward with FC1 on CTA pairs (the default at these shapes) and
-    with FC1 on single CTAs: identical h codes and output, bit for bit."""
+    """The forward with FC1 and FC2 on CTA pairs (the default where their
+    shapes allow it) and with either GEMM on single CTAs: identical h codes
+    and output, bit for bit."""
     lay = layer_of(name)
     x, lg, W1, W2 = lay.x(), lay.logits(), lay.w1(), lay.w2()
     r2, w1q, w2q = gpu_forward(lay, x, lg, W1, W2)
-    monkeypatch.setenv("MOE_FC1_CTA_PAIRS", "0")
-    r1, _, _ = gpu_forward(lay, x, lg, w1q=w1q, w2q=w2q)
-    assert r1["status"] == 0 and r2["status"] == 0
-    mp = int(r1["offsets"][-1])
-    assert np.array_equal(r2["h_codes"][:mp], r1["h_codes"][:mp])
-    assert np.array_equal(r2["h_g"][:mp].view(np.uint32), r1["h_g"][:mp].view(np.uint32))
-    assert np.array_equal(r2["out"], r1["out"])
+    runs = []
+    for var in ("MOE_FC1_CTA_PAIRS", "MOE_FC2_CTA_PAIRS"):
+        monkeypatch.setenv(var, "0")
+        runs.append(gpu_forward(lay, x, lg, w1q=w1q, w2q=w2q)[0])
+        monkeypatch.delenv(var)
+    assert r2["status"] == 0 and all(r["status"] == 0 for r in runs)
+    mp = int(r2["offsets"][-1])
+    for r1 in runs:
+        assert np.array_equal(r2["h_codes"][:mp], r1["h_codes"][:mp])
+        assert np.array_equal(r2["h_g"][:mp].view(np.uint32), r1["h_g"][:mp].view(np.uint32))
+        assert np.array_equal(r2["slots"][:mp], r1["slots"][:mp])
+        assert np.array_equal(r2["out"], r1["out"])
 
 
 def test_forward_equals_modular_composition(orc):

@@ -95,7 +95,10 @@ constexpr int FC2_NSLOT = 2;                           // FC2: double buffering
 // columns each, 80 registers per thread); FC2's light epilogue keeps 8 warps
 // of 64 columns at 128 registers.
 constexpr int FC1_NE = 16, FC2_NE = 8;
-constexpr int FC2P_NE = 16;  // FC2 on CTA pairs: 4 column parts of 64 of the 256-column accumulator
+constexpr int FC2P_NE = 16;
+// Register split of the 24-warp kernels (launched at 80 per thread)
+constexpr int REG_EPI = 96, REG_SFW = 56, REG_PROD = 40;
+static_assert(4 * REG_EPI + REG_SFW + REG_PROD == 6 * 80, "register split");  // FC2 on CTA pairs: 4 column parts of 64 of the 256-column accumulator
 static_assert(FC1_NE * 32 <= kFc1EpiThreads, "FC1 epilogue threads");
 constexpr int FC1_PARTS = FC1_NE / 4, FC1_PART_COLS = BN / FC1_PARTS;  // column parts of a chunk, one per warp
 // h is staged and requantised in 32-column sub-parts (two 16-element blocks,
@@ -852,7 +855,12 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
   const AbortFlag abort_flag{smem_u32(&tl->abort_flag)};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   using RL = Roles<NE>;
+  // 24 warps (16 epilogue) launch at 80 registers a thread; the epilogue's
+  // four warpgroups take registers from the scale writers' group and from
+  // the producers' and MMA issuer's group (sums: 4 x 96 + 56 + 40 = 6 x 80)
+  constexpr bool SPLIT = NE == 16;
   if (warp >= RL::PROD && warp < RL::MMA) {
+    if constexpr (SPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_PROD));
     if (lane == 0) {
       prefetch_tmap(tmap_a);
       prefetch_tmap(tmap_b);
@@ -867,15 +875,18 @@ __device__ __forceinline__ bool run_pipeline_roles(const CUtensorMap* tmap_a, co
     return false;
   }
   if (warp == RL::MMA) {
+    if constexpr (SPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_PROD));
     if (lane == 0 && (!PAIR || G.rank == 0))
       mma_loop<PAIR>(G, off, E, a_base, ring_base, tl, tl->tmem_base, abort_flag, status);
     __syncwarp();
     return false;
   }
   if (warp >= RL::SFW && warp < RL::SFW + 4) {
+    if constexpr (SPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_SFW));
     sf_writer_loop(warp - RL::SFW, G, off, E, ring_base, tl, tl->tmem_base, abort_flag, status);
     return false;
   }
+  if constexpr (SPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_EPI));
   return true;
 }
 

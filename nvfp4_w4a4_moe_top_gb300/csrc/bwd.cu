@@ -191,15 +191,15 @@ __device__ __forceinline__ Plan make_plan(const BwdGemmArgs& a) {
 __device__ void producer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTail* tl, volatile int* abort_flag) {
   const uint32_t stage_bytes = A_TILE + a.bn * 128;
   const uint32_t tx = stage_bytes;
-  uint32_t kc = 0;
+  // stage s and use count of the CTA's running k-step, advanced by increments
+  uint32_t s = 0, use = 0;
   uint32_t last_use[MAX_STAGES];
   for (int i = 0; i < MAX_STAGES; ++i) last_use[i] = 0xFFFFFFFFu;
   bool aborted = false;
   for (int u = blockIdx.x; u < P.units && !aborted; u += gridDim.x) {
     const Unit U = P.unit(a, u);
     const int brow0 = a.mode == BWD_WGRAD ? U.k0 : U.e * a.K;
-    for (int ks = 0; ks < U.nk; ++ks, ++kc) {
-      const uint32_t s = kc % (uint32_t)a.stages, use = kc / (uint32_t)a.stages;
+    for (int ks = 0; ks < U.nk; ++ks) {
       if (!bwait(smem_u32(&tl->empty[s]), (use & 1u) ^ 1u, abort_flag, a.status)) { aborted = true; break; }
       const uint32_t st = ring + s * stage_bytes;
       const uint32_t fb = smem_u32(&tl->full[s]);
@@ -213,6 +213,10 @@ __device__ void producer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTa
       for (int c = 0; c < a.bn / 64; ++c)
         tma_load_2d(st + A_TILE + c * CHUNK, &a.tmap_b, U.nt * a.bn + c * 64, brow0 + ks * BK, fb);
       last_use[s] = use;
+      if (++s == (uint32_t)a.stages) {
+        s = 0;
+        ++use;
+      }
     }
   }
   if (aborted) {
@@ -230,7 +234,17 @@ __device__ void mma_issuer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, B
   const uint32_t stage_bytes = A_TILE + a.bn * 128;
   const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((a.a_mn ? 1u : 0u) << 15) | (1u << 16) |
                          ((uint32_t)(a.bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-  uint32_t kc = 0, it = 0;
+  // The single issuing thread's per-k-step work is what the tensor pipe
+  // waits on: descriptors and barrier addresses are formed once, and the
+  // stage position advances by increments.  K = 16 per instruction: 32
+  // bytes (2 descriptor units) along a K-major row, or two 8-row groups
+  // (2048 bytes, 128 units) down an MN-major tile.
+  const uint32_t full0 = smem_u32(&tl->full[0]), empty0 = smem_u32(&tl->empty[0]);
+  const uint32_t stage_desc = stage_bytes >> 4;
+  const uint64_t adesc0 = a.a_mn ? sdesc_mn_sw128(ring, CHUNK) : sdesc_k_sw128(ring);
+  const uint64_t bdesc0 = sdesc_mn_sw128(ring + A_TILE, CHUNK);
+  const uint32_t astep = a.a_mn ? 128u : 2u;
+  uint32_t s = 0, use = 0, it = 0;
   bool aborted = false;
   for (int u = blockIdx.x; u < P.units && !aborted; u += gridDim.x) {
     const Unit U = P.unit(a, u);
@@ -239,20 +253,19 @@ __device__ void mma_issuer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, B
     if (!bwait(smem_u32(&tl->tempty[acc]), (ause & 1u) ^ 1u, abort_flag, a.status)) { aborted = true; break; }
     tc_fence_after();
     const uint32_t d = tmem + acc * (uint32_t)a.bn;
-    for (int ks = 0; ks < U.nk; ++ks, ++kc) {
-      const uint32_t s = kc % (uint32_t)a.stages, use = kc / (uint32_t)a.stages;
-      if (!bwait(smem_u32(&tl->full[s]), use & 1u, abort_flag, a.status)) { aborted = true; break; }
+    for (int ks = 0; ks < U.nk; ++ks) {
+      if (!bwait(full0 + 8u * s, use & 1u, abort_flag, a.status)) { aborted = true; break; }
       tc_fence_after();
-      const uint32_t st = ring + s * stage_bytes;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        // K = 16 per instruction: 32 bytes along a K-major row, or two
-        // 8-row groups (2048 bytes) down an MN-major tile
-        const uint64_t ad = a.a_mn ? sdesc_mn_sw128(st + i * 2048, CHUNK) : sdesc_k_sw128(st + i * 32);
-        const uint64_t bd = sdesc_mn_sw128(st + A_TILE + i * 2048, CHUNK);
-        bf16_mma(d, ad, bd, idesc, (ks | i) != 0 ? 1u : 0u);
+      const uint64_t ad = adesc0 + s * stage_desc, bd = bdesc0 + s * stage_desc;
+      bf16_mma(d, ad, bd, idesc, ks != 0 ? 1u : 0u);
+      bf16_mma(d, ad + astep, bd + 128u, idesc, 1u);
+      bf16_mma(d, ad + 2u * astep, bd + 256u, idesc, 1u);
+      bf16_mma(d, ad + 3u * astep, bd + 384u, idesc, 1u);
+      bcommit(empty0 + 8u * s);
+      if (++s == (uint32_t)a.stages) {
+        s = 0;
+        ++use;
       }
-      bcommit(smem_u32(&tl->empty[s]));
     }
     if (aborted) break;
     bcommit(smem_u32(&tl->tfull[acc]));

@@ -41,6 +41,8 @@
 //
 // Every wait is bounded; on expiry the kernel raises MOE_STATUS_TIMEOUT,
 // lets its own copies and MMAs land, frees tensor memory and returns.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -153,6 +155,7 @@ __device__ __forceinline__ int expert_of_tile(const int32_t* off, int E, int mt)
 struct Unit {
   int e, mt, nt;  // expert, 128-row output tile, N tile
   int k0, nk;     // first contraction row (wgrad) and number of 64-deep k-steps
+  bool ghost;     // CTA pairs: a repeated tile that stores nothing
 };
 
 struct Plan {
@@ -174,9 +177,129 @@ struct Plan {
       U.k0 = __ldg(a.offsets + U.e);
       U.nk = (__ldg(a.offsets + U.e + 1) - U.k0) / BK;
     }
+    U.ghost = false;
     return U;
   }
 };
+
+// CTA pairs (cta_group::2 MMAs of M = 256, N = 256): a unit is a pair of
+// 128-row output tiles and one 256-column N tile; rank r of the pair takes
+// row tile r of the pair and loads N columns 128 r .. of the tile's B.
+// dgrad: the pairs are consecutive row tiles of one expert, numbered expert
+// by expert (an expert with n tiles owns ceil(n / 2) pairs; when n is odd,
+// rank 1's tile of the last pair repeats tile 0's rows and stores nothing);
+// wgrad: the expert's Mo / 128 output row tiles in pairs (Mo % 256 == 0).
+// The cursor walks the experts forward, so successive calls of one CTA
+// (increasing u) continue where the previous one stopped.
+struct PairCursor {
+  int e = 0, p0 = 0;
+};
+__device__ __forceinline__ bool pair_unit(const BwdGemmArgs& a, int ntn, int u, int rank, PairCursor& cur, Unit& U) {
+  const int p = u / ntn;
+  U.nt = u - p * ntn;
+  U.ghost = false;
+  if (a.mode == BWD_WGRAD) {
+    const int per_e = a.Mo / (2 * BM);
+    U.e = p / per_e;
+    if (U.e >= a.E) return false;
+    U.mt = 2 * (p - U.e * per_e) + rank;
+    U.k0 = __ldg(a.offsets + U.e);
+    U.nk = (__ldg(a.offsets + U.e + 1) - U.k0) / BK;
+    return true;
+  }
+  while (cur.e < a.E) {
+    const int t0 = __ldg(a.offsets + cur.e) / BM, t1 = __ldg(a.offsets + cur.e + 1) / BM;
+    const int np = (t1 - t0 + 1) >> 1;
+    if (p < cur.p0 + np) {
+      U.e = cur.e;
+      U.mt = t0 + 2 * (p - cur.p0) + rank;
+      if (U.mt >= t1) {
+        U.ghost = true;
+        U.mt -= 1;
+      }
+      U.k0 = 0;
+      U.nk = a.K / BK;
+      return true;
+    }
+    cur.p0 += np;
+    ++cur.e;
+  }
+  return false;
+}
+
+// The CTA's units in order: single CTAs take u = blockIdx.x, + gridDim.x,
+// ...; pairs take pair units u = cluster, + clusters, ...
+template <bool PAIR>
+struct UnitWalk {
+  const BwdGemmArgs& a;
+  const Plan& P;
+  int u, step, rank;
+  PairCursor cur;
+  __device__ UnitWalk(const BwdGemmArgs& a_, const Plan& P_, int start, int step_, int rank_)
+      : a(a_), P(P_), u(start), step(step_), rank(rank_) {}
+  __device__ bool next(Unit& U) {
+    if constexpr (PAIR) {
+      const bool ok = pair_unit(a, P.ntn, u, rank, cur, U);
+      u += step;
+      return ok;
+    } else {
+      if (u >= P.units) return false;
+      U = P.unit(a, u);
+      u += step;
+      return true;
+    }
+  }
+};
+
+__device__ __forceinline__ uint32_t b_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t b_cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t b_cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t b_map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// 2D tiled TMA load whose completion is signalled on a barrier of either CTA
+// of the pair (rank 1's loads complete on rank 0's barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bf16_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void bcommit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void b_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void b_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 __device__ __forceinline__ Plan make_plan(const BwdGemmArgs& a) {
   Plan p;
@@ -188,30 +311,43 @@ __device__ __forceinline__ Plan make_plan(const BwdGemmArgs& a) {
   return p;
 }
 
-__device__ void producer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTail* tl, volatile int* abort_flag) {
-  const uint32_t stage_bytes = A_TILE + a.bn * 128;
-  const uint32_t tx = stage_bytes;
+// PAIR: each CTA loads its A tile and its 128 columns of B; rank 0's
+// full[s] counts both CTAs' bytes (rank 1's loads complete on it), and each
+// CTA waits for its own empty[s], which the MMAs' commits reach in both.
+template <bool PAIR>
+__device__ void producer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTail* tl, volatile int* abort_flag,
+                         UnitWalk<PAIR> walk, uint32_t rank) {
+  const int bcols = PAIR ? a.bn / 2 : a.bn;  // B columns this CTA loads per stage
+  const uint32_t stage_bytes = A_TILE + bcols * 128;
+  const uint32_t tx = PAIR ? 2 * stage_bytes : stage_bytes;
   // stage s and use count of the CTA's running k-step, advanced by increments
   uint32_t s = 0, use = 0;
   uint32_t last_use[MAX_STAGES];
   for (int i = 0; i < MAX_STAGES; ++i) last_use[i] = 0xFFFFFFFFu;
   bool aborted = false;
-  for (int u = blockIdx.x; u < P.units && !aborted; u += gridDim.x) {
-    const Unit U = P.unit(a, u);
+  Unit U;
+  while (!aborted && walk.next(U)) {
     const int brow0 = a.mode == BWD_WGRAD ? U.k0 : U.e * a.K;
+    const int bcol0 = U.nt * a.bn + (PAIR ? (int)rank * bcols : 0);
     for (int ks = 0; ks < U.nk; ++ks) {
       if (!bwait(smem_u32(&tl->empty[s]), (use & 1u) ^ 1u, abort_flag, a.status)) { aborted = true; break; }
       const uint32_t st = ring + s * stage_bytes;
-      const uint32_t fb = smem_u32(&tl->full[s]);
-      mbar_arrive_expect_tx(fb, tx);
+      const uint32_t fb_own = smem_u32(&tl->full[s]);
+      const uint32_t fb = PAIR ? b_map_to_rank(fb_own, 0) : fb_own;
+      if (!PAIR || rank == 0) mbar_arrive_expect_tx(fb_own, tx);
+      auto load = [&](uint32_t dst, const CUtensorMap* map, int x, int y) {
+        if (PAIR)
+          tma_load_2d_pair(dst, map, x, y, fb);
+        else
+          tma_load_2d(dst, map, x, y, fb);
+      };
       if (a.a_mn) {
-        tma_load_2d(st, &a.tmap_a, U.mt * BM, U.k0 + ks * BK, fb);
-        tma_load_2d(st + CHUNK, &a.tmap_a, U.mt * BM + 64, U.k0 + ks * BK, fb);
+        load(st, &a.tmap_a, U.mt * BM, U.k0 + ks * BK);
+        load(st + CHUNK, &a.tmap_a, U.mt * BM + 64, U.k0 + ks * BK);
       } else {
-        tma_load_2d(st, &a.tmap_a, ks * BK, U.mt * BM, fb);
+        load(st, &a.tmap_a, ks * BK, U.mt * BM);
       }
-      for (int c = 0; c < a.bn / 64; ++c)
-        tma_load_2d(st + A_TILE + c * CHUNK, &a.tmap_b, U.nt * a.bn + c * 64, brow0 + ks * BK, fb);
+      for (int c = 0; c < bcols / 64; ++c) load(st + A_TILE + c * CHUNK, &a.tmap_b, bcol0 + c * 64, brow0 + ks * BK);
       last_use[s] = use;
       if (++s == (uint32_t)a.stages) {
         s = 0;
@@ -220,20 +356,30 @@ __device__ void producer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTa
     }
   }
   if (aborted) {
-    for (int s = 0; s < MAX_STAGES; ++s)
-      if (last_use[s] != 0xFFFFFFFFu) {
+    // let the copies this thread issued land before the CTA can exit (a
+    // pair's rank 1 waits on its own barrier's phase too: its copies have
+    // landed once rank 0's phase completed, which the cluster barrier at
+    // exit covers)
+    for (int s2 = 0; s2 < MAX_STAGES; ++s2)
+      if (last_use[s2] != 0xFFFFFFFFu && (!PAIR || rank == 0)) {
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(smem_u32(&tl->full[s]), last_use[s] & 1u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
+        while (!mbar_try_wait(smem_u32(&tl->full[s2]), last_use[s2] & 1u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
         }
       }
   }
 }
 
+// PAIR: run by rank 0 alone; cta_group::2 MMAs of M = 256 (each CTA's 128
+// rows from its A tile) and N = 256 (each CTA's 128 columns of B), commits
+// reaching both CTAs.
+template <bool PAIR>
 __device__ void mma_issuer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, BTail* tl, uint32_t tmem,
-                           volatile int* abort_flag) {
-  const uint32_t stage_bytes = A_TILE + a.bn * 128;
+                           volatile int* abort_flag, UnitWalk<PAIR> walk) {
+  const int bcols = PAIR ? a.bn / 2 : a.bn;
+  const uint32_t stage_bytes = A_TILE + bcols * 128;
+  const uint32_t m = PAIR ? 2 * BM : BM;
   const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((a.a_mn ? 1u : 0u) << 15) | (1u << 16) |
-                         ((uint32_t)(a.bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+                         ((uint32_t)(a.bn >> 3) << 17) | ((m >> 4) << 24);
   // The single issuing thread's per-k-step work is what the tensor pipe
   // waits on: descriptors and barrier addresses are formed once, and the
   // stage position advances by increments.  K = 16 per instruction: 32
@@ -244,10 +390,22 @@ __device__ void mma_issuer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, B
   const uint64_t adesc0 = a.a_mn ? sdesc_mn_sw128(ring, CHUNK) : sdesc_k_sw128(ring);
   const uint64_t bdesc0 = sdesc_mn_sw128(ring + A_TILE, CHUNK);
   const uint32_t astep = a.a_mn ? 128u : 2u;
+  auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t acc) {
+    if constexpr (PAIR)
+      bf16_mma_pair(d, ad, bd, idesc, acc);
+    else
+      bf16_mma(d, ad, bd, idesc, acc);
+  };
+  auto commit = [&](uint32_t bar) {
+    if constexpr (PAIR)
+      bcommit_pair(bar);
+    else
+      bcommit(bar);
+  };
   uint32_t s = 0, use = 0, it = 0;
   bool aborted = false;
-  for (int u = blockIdx.x; u < P.units && !aborted; u += gridDim.x) {
-    const Unit U = P.unit(a, u);
+  Unit U;
+  while (!aborted && walk.next(U)) {
     if (U.nk == 0) continue;
     const uint32_t acc = it & 1u, ause = it >> 1;
     if (!bwait(smem_u32(&tl->tempty[acc]), (ause & 1u) ^ 1u, abort_flag, a.status)) { aborted = true; break; }
@@ -257,21 +415,21 @@ __device__ void mma_issuer(const BwdGemmArgs& a, const Plan& P, uint32_t ring, B
       if (!bwait(full0 + 8u * s, use & 1u, abort_flag, a.status)) { aborted = true; break; }
       tc_fence_after();
       const uint64_t ad = adesc0 + s * stage_desc, bd = bdesc0 + s * stage_desc;
-      bf16_mma(d, ad, bd, idesc, ks != 0 ? 1u : 0u);
-      bf16_mma(d, ad + astep, bd + 128u, idesc, 1u);
-      bf16_mma(d, ad + 2u * astep, bd + 256u, idesc, 1u);
-      bf16_mma(d, ad + 3u * astep, bd + 384u, idesc, 1u);
-      bcommit(empty0 + 8u * s);
+      mma(d, ad, bd, ks != 0 ? 1u : 0u);
+      mma(d, ad + astep, bd + 128u, 1u);
+      mma(d, ad + 2u * astep, bd + 256u, 1u);
+      mma(d, ad + 3u * astep, bd + 384u, 1u);
+      commit(empty0 + 8u * s);
       if (++s == (uint32_t)a.stages) {
         s = 0;
         ++use;
       }
     }
     if (aborted) break;
-    bcommit(smem_u32(&tl->tfull[acc]));
+    commit(smem_u32(&tl->tfull[acc]));
     ++it;
   }
-  bcommit(smem_u32(&tl->done));
+  commit(smem_u32(&tl->done));
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(smem_u32(&tl->done), 0u) && global_timer_ns() - t0 < WAIT_LIMIT_NS) {
   }
@@ -344,8 +502,12 @@ __device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint
 // 16-byte chunk j of row r at chunk j ^ (r % 8), the 128-byte swizzle of the
 // output tensor map) and one TMA store per 32 x 32 chunk, instead of each
 // lane writing its own row.
+// PAIR: each CTA drains its own 128 rows (all a.bn columns of the pair's
+// accumulator) and releases the accumulator to rank 0's barrier; a ghost
+// tile stores nothing.
+template <bool PAIR>
 __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_t tmem, uint32_t staging,
-                         volatile int* abort_flag) {
+                         volatile int* abort_flag, UnitWalk<PAIR> walk) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q4 = warp & 3, part = warp >> 2;
   const int rl = q4 * 32 + lane;
@@ -353,8 +515,9 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
   const uint32_t stg = staging + (uint32_t)warp * STAGE_TILE;
   bool pending = false;  // lane 0: a store from stg may still be reading it
   uint32_t it = 0;
-  for (int u = blockIdx.x; u < P.units; u += gridDim.x) {
-    const Unit U = P.unit(a, u);
+  const uint32_t tempty0 = PAIR ? b_map_to_rank(smem_u32(&tl->tempty[0]), 0) : smem_u32(&tl->tempty[0]);
+  Unit U;
+  while (walk.next(U)) {
     const int c0 = U.nt * a.bn + part * half;  // first output column of this thread
     if (U.nk == 0) {  // wgrad of an expert without rows: zero gradient
       float4* o = reinterpret_cast<float4*>(a.out + ((int64_t)U.e * a.Mo + U.mt * BM + rl) * a.N + c0);
@@ -366,7 +529,7 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
     if (!bwarp_wait(smem_u32(&tl->tfull[acc]), ause & 1u, abort_flag, a.status)) break;
     tc_fence_after();
     const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + acc * (uint32_t)a.bn + part * half;
-    for (int c = 0; c < half; c += 32) {
+    for (int c = 0; c < half && !U.ghost; c += 32) {
       uint32_t v[32];
       tld32(tbase + c, v);
       if (a.mode == BWD_DGRAD_SWIGLU) {
@@ -389,7 +552,12 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&tl->tempty[acc]));
+    if (lane == 0) {
+      if constexpr (PAIR)
+        b_arrive_cluster(tempty0 + 8u * acc);
+      else
+        mbar_arrive(tempty0 + 8u * acc);
+    }
   }
   if (lane == 0 && pending) bulk_wait0();  // the last stores complete before the CTA exits
   __syncwarp();
@@ -397,13 +565,21 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
 
 }  // namespace
 
+// PAIR: clusters of two CTAs (cta_group::2 MMAs issued by rank 0); the
+// barriers rank 0's MMA thread waits on count both CTAs (full: both CTAs'
+// bytes; tempty: both CTAs' epilogue warps); the cluster barrier at entry
+// orders the barrier initialisation before any remote arrival, and the one
+// at exit holds both CTAs until rank 0 has seen all MMAs complete.
+template <bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_constant__ BwdGemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t stage_bytes = A_TILE + a.bn * 128;
+  const int bcols = PAIR ? a.bn / 2 : a.bn;
+  const uint32_t stage_bytes = A_TILE + bcols * 128;
   uint8_t* staging = smem + (size_t)a.stages * stage_bytes;
   BTail* tl = reinterpret_cast<BTail*>(staging + NEPI * STAGE_TILE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? b_cluster_rank() : 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(smem_u32(&tl->full[s]), 1);
@@ -411,44 +587,65 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&tl->tfull[s]), 1);
-      mbar_init(smem_u32(&tl->tempty[s]), NEPI);
+      mbar_init(smem_u32(&tl->tempty[s]), PAIR ? 2 * NEPI : NEPI);
     }
     mbar_init(smem_u32(&tl->done), 1);
     tl->abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == MMA_WARP) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl->tmem_base)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    b_cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const Plan P = make_plan(a);
   volatile int* abort_flag = &tl->abort_flag;
   const uint32_t ring = smem_u32(smem);
+  const int start = PAIR ? (int)b_cluster_id() : (int)blockIdx.x;
+  const int step = PAIR ? (int)b_cluster_count() : (int)gridDim.x;
+  const UnitWalk<PAIR> walk(a, P, start, step, (int)rank);
   if (warp == PROD_WARP) {
     if (lane == 0) {
       prefetch_tmap(&a.tmap_a);
       prefetch_tmap(&a.tmap_b);
       if (a.mode != BWD_DGRAD_SWIGLU) prefetch_tmap(&a.tmap_out);
-      producer(a, P, ring, tl, abort_flag);
+      producer<PAIR>(a, P, ring, tl, abort_flag, walk, rank);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    if (lane == 0) mma_issuer(a, P, ring, tl, tl->tmem_base, abort_flag);
+    if (lane == 0 && (!PAIR || rank == 0)) mma_issuer<PAIR>(a, P, ring, tl, tl->tmem_base, abort_flag, walk);
     __syncwarp();
   } else {
-    epilogue(a, P, tl, tl->tmem_base, smem_u32(staging), abort_flag);
+    epilogue<PAIR>(a, P, tl, tl->tmem_base, smem_u32(staging), abort_flag, walk);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    b_cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
-  if (warp == MMA_WARP)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
-                 : "memory");
+  if (warp == MMA_WARP) {
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tl->tmem_base), "r"(TMEM_COLS)
+                   : "memory");
+  }
 }
 
 int bwd_gemm_smem_bytes(int bn, int stages) {
@@ -457,19 +654,57 @@ int bwd_gemm_smem_bytes(int bn, int stages) {
 
 // max_row_tiles: for dgrad, an upper bound of offsets[E] / 128 (the number
 // of units is read on the device); ignored for wgrad.
+// The GEMMs with N % 256 == 0 (and, for wgrad, Mo % 256 == 0) run on CTA
+// pairs, six 32 KB stages per CTA; the rest on single CTAs with four 48 KB
+// (N tile 256) or six 32 KB (N tile 128) stages.  MOE_BWD_CTA_PAIRS=0 in the
+// environment selects single CTAs throughout.
 int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream) {
   a.bn = a.N % 256 == 0 ? 256 : 128;
-  a.stages = a.bn == 256 ? 4 : 6;
   const int ntn = a.N / a.bn;
+  const char* env = std::getenv("MOE_BWD_CTA_PAIRS");
+  const bool pairs = !(env && env[0] == '0') && a.bn == 256 && (a.mode != BWD_WGRAD || a.Mo % 256 == 0);
+  int sms = gemm_num_ctas();
+  if (sms <= 0) return -1;
+  if (pairs) {
+    a.stages = 6;
+    const int smem = bwd_gemm_smem_bytes(a.bn / 2, a.stages);
+    if (cudaFuncSetAttribute(bwd_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, bwd_gemm_kernel<true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      clusters = 0;
+    }
+    if (clusters > sms / 2) clusters = sms / 2;
+    const int64_t max_units = a.mode == BWD_WGRAD ? (int64_t)a.E * (a.Mo / (2 * BM)) * ntn
+                                                  : ((int64_t)max_row_tiles / 2 + a.E) * ntn;
+    if (max_units < clusters) clusters = (int)max_units;
+    if (clusters >= 1) {
+      cfg.gridDim = dim3((unsigned)(2 * clusters));
+      return cudaLaunchKernelEx(&cfg, bwd_gemm_kernel<true>, a) == cudaSuccess ? 0 : -1;
+    }
+  }
+  a.stages = a.bn == 256 ? 4 : 6;
   const int64_t max_units = a.mode == BWD_WGRAD ? (int64_t)a.E * (a.Mo / BM) * ntn : (int64_t)max_row_tiles * ntn;
   const int smem = bwd_gemm_smem_bytes(a.bn, a.stages);
-  if (cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(bwd_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return -1;
-  int grid = gemm_num_ctas();
-  if (grid <= 0) return -1;
+  int grid = sms;
   if (max_units < grid) grid = (int)max_units;
   if (grid < 1) return 0;
-  bwd_gemm_kernel<<<grid, THREADS, smem, stream>>>(a);
+  bwd_gemm_kernel<false><<<grid, THREADS, smem, stream>>>(a);
   return 0;
 }
 

@@ -145,6 +145,21 @@ def test_backward_against_oracle(orc, name):
         assert e2e[key] <= 1e-3, key
 
 
+@pytest.mark.parametrize("name", ["small", "tiny"])
+def test_backward_cta_pairs_equal_single(orc, name, monkeypatch):
+    """The backward GEMMs on CTA pairs (where N, and for the weight
+    gradients Mo, are multiples of 256) and on single CTAs: every gradient
+    bit for bit."""
+    lay = layer_of(name)
+    x, lg, W1, W2, dY = lay.x(), lay.logits(), lay.w1(), lay.w2(), lay.grad_out()
+    r2 = gpu_train_step(lay, x, lg, W1, W2, dY)
+    monkeypatch.setenv("MOE_BWD_CTA_PAIRS", "0")
+    r1 = gpu_train_step(lay, x, lg, W1, W2, dY)
+    assert r1["status"] == 0 and r2["status"] == 0
+    for key in ("du", "dx", "dW1", "dW2", "dw", "dlogits"):
+        assert np.array_equal(r1[key].view(np.uint8), r2[key].view(np.uint8)), key
+
+
 def test_empty_experts_get_zero_weight_gradients(orc):
     lay = layer_of("ragged")
     x, lg, W1, W2, dY = lay.x(), lay.logits(), lay.w1(), lay.w2(), lay.grad_out()

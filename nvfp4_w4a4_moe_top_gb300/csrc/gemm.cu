@@ -815,7 +815,9 @@ __device__ __forceinline__ void stage_scales(float* dst, const float* src, int n
 // two blocks of 16) of row `row`, read back from the scratch vectors this
 // thread staged: per block the E4M3 scale s_b = E4M3(a_b / (6 g)) and the
 // E2M1 codes of h / (g s_b).  The two scale bytes are bytes 2*(vp % 2)
-// and +1 of scale word 2c + vp/2.
+// and +1 of scale word 2c + vp/2.  Called by all 32 lanes of the warp: the
+// scratch lines it has read are then dropped from L2 without a write-back
+// (the buffer is rewritten before it is read again).
 __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int vp, int rl, int64_t row, float g,
                                               float den, uint8_t* h_codes, uint8_t* h_sf, int d_ff) {
   uint4 cur[4];
@@ -842,6 +844,13 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int vp, i
   const int kgh = d_ff / 64;
   *reinterpret_cast<uint16_t*>(h_sf + ((row >> 7) * kgh + 2 * c + (vp >> 1)) * 512 + (row & 31) * 16 +
                                ((row >> 5) & 3) * 4 + 2 * (vp & 1)) = (uint16_t)sb2;
+  // each 128-byte line holds 8 rows' 16 bytes: discarded once all 32 lanes
+  // have used what they read
+  __syncwarp();
+  if ((rl & 7) == 0) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) discard_l2_line(scr + (size_t)((c * FC1_VPARTS + vp) * 4 + v) * BM + rl);
+  }
 }
 
 // Shared roles of both GEMMs.  Returns true for the epilogue warps, which
@@ -1086,12 +1095,14 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
               dh[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
               dh[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
             }
+            // staged h stays in L2 until it is requantised (evict last)
             uint4* sv = scratch_buf(uc & 1) + (size_t)((c * FC1_VPARTS + part * FC1_SUB) * 4 + 2 * hh) * BM + rl;
-            sv[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-            sv[BM] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+            const uint64_t pol = l2_evict_last();
+            st_global_hint(sv, make_uint4(hp[0], hp[1], hp[2], hp[3]), pol);
+            st_global_hint(sv + BM, make_uint4(hp[4], hp[5], hp[6], hp[7]), pol);
           }
         }
-        if (have_prev && !ghost_prev && !abort_flag.raised())
+        if (__all_sync(0xFFFFFFFFu, have_prev && !ghost_prev && !abort_flag.raised()))
 #pragma unroll
           for (int sp = 0; sp < FC1_SUB; ++sp)
             requant_chunk(scratch_buf((uc - 1) & 1), c, part * FC1_SUB + sp, rl, (int64_t)u_prev * BM + rl, g_prev,
@@ -1126,7 +1137,7 @@ __global__ void __launch_bounds__(Roles<FC1_NE>::THREADS, 1) fc1_swiglu_kernel(c
     }
     // the last unit
     if (have_prev && !ghost_prev) {
-      if (!abort_flag.raised())
+      if (__all_sync(0xFFFFFFFFu, !abort_flag.raised()))
         for (int c = 0; c < nch; ++c)
           for (int sp = 0; sp < FC1_SUB; ++sp)
             requant_chunk(scratch_buf((uc - 1) & 1), c, part * FC1_SUB + sp, rl, (int64_t)u_prev * BM + rl, g_prev,

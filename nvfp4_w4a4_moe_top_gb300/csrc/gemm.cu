@@ -825,6 +825,7 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int vp, i
   for (int v = 0; v < 4; ++v) cur[v] = scr[(size_t)((c * FC1_VPARTS + vp) * 4 + v) * BM + rl];
   uint32_t sb2 = 0;
   uint32_t cw[4];
+  const float rden = block_scale_rden(den);
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
     const uint32_t wb[8] = {cur[2 * b].x, cur[2 * b].y, cur[2 * b].z, cur[2 * b].w,
@@ -832,8 +833,8 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int vp, i
     uint32_t sb = 0;
     uint2 p = make_uint2(0u, 0u);
     if (g != 0.0f) {
-      sb = e4m3_encode(__fdiv_rn(amax16_bf16(wb), den));
-      const float S = __fmul_rn(g, e4m3_decode(sb));
+      sb = block_scale_code(amax16_bf16(wb), den, rden);
+      const float S = __fmul_rn(g, e4m3_decode_hw(sb));
       if (S != 0.0f) p = e2m1_block16(wb, S);
     }
     cw[2 * b] = p.x;

@@ -63,6 +63,7 @@ __device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32
   const int64_t sf_row = (r >> 7) * kg * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
   const float gs = __fdiv_rn(a, 2688.0f);
   const float den = __fmul_rn(6.0f, gs);
+  const float rden = block_scale_rden(den);
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int e8 = g * 128 + 4 * lane;
@@ -73,8 +74,8 @@ __device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32
       for (int b = 0; b < 2; ++b) {  // the lane's two blocks of 16
         const uint4 p0 = v[g][2 * b], p1 = v[g][2 * b + 1];
         const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w}, w1[4] = {p1.x, p1.y, p1.z, p1.w};
-        const uint32_t sb = e4m3_encode(__fdiv_rn(__uint_as_float(bm[g][b] << 16), den));
-        const float S = __fmul_rn(gs, e4m3_decode(sb));
+        const uint32_t sb = block_scale_code(__uint_as_float(bm[g][b] << 16), den, rden);
+        const float S = __fmul_rn(gs, e4m3_decode_hw(sb));
         if (S != 0.0f) {
           const uint2 cc = e2m1_codes16(w0, w1, S);
           c[2 * b] = cc.x;

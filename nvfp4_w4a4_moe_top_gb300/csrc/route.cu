@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
   if (lane == 0 && amax_tok) amax_tok[t] = a;
   const float gs = __fdiv_rn(a, 2688.0f);
   const float den = __fmul_rn(6.0f, gs);
+  const float rden = block_scale_rden(den);
   const int kg = d / 64;
   uint4 cw[NG];
   uint32_t sfw[NG];
@@ -368,8 +369,8 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
       const float ab = __uint_as_float(bm[g][b] << 16);
       uint32_t sb = 0;
       if (gs != 0.0f) {
-        sb = e4m3_encode(__fdiv_rn(ab, den));
-        const float S = __fmul_rn(gs, e4m3_decode(sb));
+        sb = block_scale_code(ab, den, rden);
+        const float S = __fmul_rn(gs, e4m3_decode_hw(sb));
         if (S != 0.0f) {
           const uint2 cc = e2m1_codes16(w0, w1, S);
           c[2 * b] = cc.x;

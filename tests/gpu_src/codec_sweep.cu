@@ -88,3 +88,103 @@ extern "C" int run_codec_sweeps(unsigned int* e4m3_first, unsigned long long* e4
   cudaFree(d_f4); cudaFree(d_f2); cudaFree(d_v); cudaFree(d_val);
   return rc;
 }
+
+// ---- the quantisers' fast paths against their exact definitions ----
+
+// The hardware E4M3 conversion of two values at once against e4m3_encode on
+// every non-negative finite float (in either position), and the hardware
+// decode against e4m3_decode on every code.
+__global__ void e4m3_hw_sweep(unsigned long long* viol) {
+  const unsigned int stride = gridDim.x * blockDim.x;
+  unsigned long long bad = 0;
+  for (unsigned int p = blockIdx.x * blockDim.x + threadIdx.x; p < 0x7F800000u; p += stride) {
+    const float t = __uint_as_float(p);
+    const unsigned int c = moe::e4m3_encode(t);
+    if (moe::e4m3x2_hw(t, 0.0f) != c || moe::e4m3x2_hw(0.0f, t) != (c << 8)) ++bad;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < 0x7F)
+    if (__float_as_uint(moe::e4m3_decode_hw(threadIdx.x)) != __float_as_uint(moe::e4m3_decode(threadIdx.x))) ++bad;
+  if (bad) atomicAdd(viol, bad);
+}
+
+// A positive float spread over [2^-126, 2^126) in exponent, from an index.
+__device__ __forceinline__ float spread(unsigned int i) {
+  const unsigned int e = 1u + (i % 252u);                    // biased exponents 1 .. 252
+  const unsigned int m = (i * 2654435761u) & 0x007FFFFFu;    // mixed mantissa
+  return __uint_as_float((e << 23) | m);
+}
+
+// block_scale_code against the exact definition E4M3(RN(a / den)) for every
+// finite non-negative BF16 amax a and 65536 divisors den spread over the
+// float range (including den below 2^-120, where the exact path serves).
+__global__ void block_scale_sweep(unsigned long long* viol) {
+  const float den = spread(blockIdx.x * blockDim.x + threadIdx.x);
+  const float rden = moe::block_scale_rden(den);
+  unsigned long long bad = 0;
+  for (unsigned int b = 0; b < 0x7F80u; ++b) {
+    const float a = __uint_as_float(b << 16);
+    if (moe::block_scale_code(a, den, rden) != moe::e4m3_encode(__fdiv_rn(a, den))) ++bad;
+  }
+  if (bad) atomicAdd(viol, bad);
+}
+
+// The E2M1 codes of 8 values through the bracket against the exact
+// definition Q(RN(v / S)) for every finite BF16 v (either sign) and 65536
+// scales S spread over the float range.
+__global__ void e2m1_bracket_sweep(unsigned long long* viol) {
+  const float S = spread(blockIdx.x * blockDim.x + threadIdx.x);
+  const moe::E2m1Bracket br = moe::e2m1_bracket(S);
+  unsigned long long bad = 0;
+  for (unsigned int b0 = 0; b0 < 0x10000u; b0 += 8) {
+    uint32_t w[4];
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t lo = b0 + 2 * i, hi = b0 + 2 * i + 1;
+      if ((lo & 0x7F80u) == 0x7F80u) lo = 0;  // non-finite patterns: zero instead
+      if ((hi & 0x7F80u) == 0x7F80u) hi = 0;
+      w[i] = lo | (hi << 16);
+      q[2 * i] = __fdiv_rn(moe::bf16_lo(w[i]), S);
+      q[2 * i + 1] = __fdiv_rn(moe::bf16_hi(w[i]), S);
+    }
+    if (moe::e2m1_codes8(w, S, br) != moe::e2m1x8(q)) ++bad;
+  }
+  if (bad) atomicAdd(viol, bad);
+}
+
+// Largest relative error of the hardware reciprocal over every float in
+// [2^-120, 2^120] (the bracket's domain), as float bits.
+__global__ void rcp_error(unsigned int* out) {
+  const unsigned int stride = gridDim.x * blockDim.x;
+  float e = 0.0f;
+  for (unsigned int p = 0x03800000u + blockIdx.x * blockDim.x + threadIdx.x; p <= 0x7B800000u; p += stride) {
+    const float x = __uint_as_float(p);
+    // y = (1 + err) / x, so x * y - 1 = err, formed exactly inside the fma
+    e = fmaxf(e, fabsf(fmaf(x, moe::rcp_approx(x), -1.0f)));
+  }
+  atomicMax(out, __float_as_uint(e));
+}
+
+extern "C" int run_fast_path_sweeps(unsigned long long* viol_e4m3, unsigned long long* viol_scale,
+                                    unsigned long long* viol_e2m1, float* rcp_max_rel) {
+  unsigned long long* d_v;
+  unsigned int* d_e;
+  if (cudaMalloc(&d_v, 3 * 8) || cudaMalloc(&d_e, 4)) return -1;
+  cudaMemset(d_v, 0, 3 * 8);
+  cudaMemset(d_e, 0, 4);
+  e4m3_hw_sweep<<<152 * 8, 256>>>(d_v);
+  block_scale_sweep<<<256, 256>>>(d_v + 1);
+  e2m1_bracket_sweep<<<256, 256>>>(d_v + 2);
+  rcp_error<<<152 * 8, 256>>>(d_e);
+  unsigned long long v[3];
+  unsigned int e = 0;
+  int rc = 0;
+  if (cudaMemcpy(v, d_v, 3 * 8, cudaMemcpyDeviceToHost) || cudaMemcpy(&e, d_e, 4, cudaMemcpyDeviceToHost)) rc = -2;
+  *viol_e4m3 = v[0];
+  *viol_scale = v[1];
+  *viol_e2m1 = v[2];
+  memcpy(rcp_max_rel, &e, 4);
+  cudaFree(d_v);
+  cudaFree(d_e);
+  return rc;
+}

@@ -1195,6 +1195,9 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
   // per epilogue warp: 32 rows x 64 BF16 columns, 16-byte chunks XOR-swizzled by row
   const uint32_t stg = smem_u32(smem + a_bytes + ring_bytes + TAIL_BYTES + (size_t)2 * d * 4) +
                        (uint32_t)(warp < FC2_NE ? warp : 0) * 32 * FC2_STAGE_ROW;
+  // DW: a second tile per warp, after all output tiles, for the copied-in
+  // output gradient
+  const uint32_t dyb = stg + FC2_STAGING_BYTES;
 
   if (run_pipeline_roles<FC2_NE>(&args.tmap_a, &args.tmap_b, args.a_sf, args.w_sf, G, rows, args.offsets, args.E, a_base,
                          ring_base, tl, args.status)) {
@@ -1229,6 +1232,26 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
       epi_barrier<FC2_NE>();
       const uint16_t* dy_row = DW ? args.dY + (int64_t)(t < 0 ? 0 : t) * d : nullptr;
       float dot = 0.0f;
+      // DW: an item's 32 output-gradient row segments (64 columns each) are
+      // copied asynchronously into the warp's input tile (8 lanes per row, 4
+      // rows per instruction) while the item before is processed
+      auto issue_dy = [&](int nt) {
+        const unsigned long long my_src =
+            t >= 0 ? reinterpret_cast<unsigned long long>(dy_row + nt * BN + part * 64) : 0ull;
+        const int sub = lane >> 3, ch = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + sub;
+          const unsigned long long sp = __shfl_sync(0xFFFFFFFFu, my_src, rr);
+          cp_async16(dyb + rr * FC2_STAGE_ROW + 16 * (ch ^ (rr & 7)),
+                     sp ? reinterpret_cast<const uint4*>(sp) + ch : reinterpret_cast<const uint4*>(args.dY), sp != 0);
+        }
+        cp_async_commit();
+      };
+      if (DW) {
+        __syncwarp();  // every lane is done with the previous unit's input tile
+        issue_dy(0);
+      }
       for (int nt = 0; nt < G.items; ++nt, ++it) {
         const uint32_t slot = it % FC2_NSLOT;
         bool ok = __all_sync(0xFFFFFFFFu, !abort_flag.raised());
@@ -1249,20 +1272,8 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
           // the staging tile is free once the previous store has read it
           if (lane == 0 && stores) bulk_wait_read0();
           __syncwarp();
-          if (DW) {
-            // the warp's 32 output-gradient row segments (64 columns each)
-            // into the staging tile, 8 lanes per row, 4 rows per load
-            const unsigned long long my_src =
-                t >= 0 ? reinterpret_cast<unsigned long long>(dy_row + nt * BN + part * 64) : 0ull;
-            const int sub = lane >> 3, ch = lane & 7;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int rr = i * 4 + sub;
-              const unsigned long long sp = __shfl_sync(0xFFFFFFFFu, my_src, rr);
-              uint4 g = make_uint4(0u, 0u, 0u, 0u);
-              if (sp) g = __ldg(reinterpret_cast<const uint4*>(sp) + ch);
-              sts128(stg + rr * FC2_STAGE_ROW + 16 * (ch ^ (rr & 7)), g.x, g.y, g.z, g.w);
-            }
+          if (DW) {  // this item's output-gradient segments have landed
+            cp_async_wait_all();
             __syncwarp();
           }
           // scale and weight into the staging tile (the 128-byte-swizzled
@@ -1288,8 +1299,8 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
               }
             }
             if (DW) {  // this row's 16 output-gradient columns, from the staging tile
-              const uint4 g0 = lds128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf) ^ (lane & 7)));
-              const uint4 g1 = lds128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf + 1) ^ (lane & 7)));
+              const uint4 g0 = lds128(dyb + lane * FC2_STAGE_ROW + 16 * ((2 * hf) ^ (lane & 7)));
+              const uint4 g1 = lds128(dyb + lane * FC2_STAGE_ROW + 16 * ((2 * hf + 1) ^ (lane & 7)));
               const uint32_t gw4[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
@@ -1307,6 +1318,10 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
             sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf) ^ (lane & 7)), zp[0], zp[1], zp[2], zp[3]);
             sts128(stg + lane * FC2_STAGE_ROW + 16 * ((2 * hf + 1) ^ (lane & 7)), zp[4], zp[5], zp[6], zp[7]);
           }
+          if (DW && nt + 1 < G.items) {  // the input tile is free again
+            __syncwarp();
+            issue_dy(nt + 1);
+          }
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
@@ -1321,6 +1336,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
         if (part == 0 && t >= 0) args.dw[(int64_t)t * k + j] = dot + tl->rowmax[1][rl];
       }
     }
+    if (DW) cp_async_wait_all();  // no copy into shared memory outlives the CTA
     if (lane == 0 && stores) bulk_wait0();  // the stores complete before the CTA exits
     __syncwarp();
   }
@@ -1683,7 +1699,8 @@ int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream) {
       return cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess ? 0 : -1;
     }
   }
-  if (!plan(a.d_ff, a.d / BN, (size_t)2 * a.d * 4, FC2_NSLOT, FC2_STAGING_BYTES, &a.rings, &a.na, &a.nb, &a.resident,
+  const size_t staging = (a.dw != nullptr ? 2 : 1) * (size_t)FC2_STAGING_BYTES;
+  if (!plan(a.d_ff, a.d / BN, (size_t)2 * a.d * 4, FC2_NSLOT, staging, &a.rings, &a.na, &a.nb, &a.resident,
             &smem))
     return -1;
   void (*kern)(const Fc2Args) = a.dw != nullptr      ? fc2_scatter_kernel<2>

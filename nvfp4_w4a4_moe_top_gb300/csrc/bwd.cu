@@ -453,14 +453,21 @@ __device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint
                                              int F, int f0, uint32_t stg, int lane) {
   const int64_t ld = 2 * (int64_t)F;  // elements per row of u and du
   const int cj = lane & 3;
+  // all eight loads first (a shared-memory store between them would make
+  // each wait for the one before)
+  uint4 g[4], x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rr = i * 8 + (lane >> 2);
+    g[i] = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + f0) + cj);
+    x[i] = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + F + f0) + cj);
+  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int rr = i * 8 + (lane >> 2);
     const uint32_t off = rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4);
-    const uint4 g = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + f0) + cj);
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + F + f0) + cj);
-    sts128(stg + off, g.x, g.y, g.z, g.w);
-    sts128(stg + 2048 + off, x.x, x.y, x.z, x.w);
+    sts128(stg + off, g[i].x, g[i].y, g[i].z, g[i].w);
+    sts128(stg + 2048 + off, x[i].x, x[i].y, x[i].z, x[i].w);
   }
   __syncwarp();
 #pragma unroll

@@ -1482,7 +1482,9 @@ __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(co
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&args.tmap_out, stg, nt * 2 * BN + part * 64, u * BM + q4 * 32);
+            // evict-first: the 2.15 GB of z rows pass through L2 once, and
+            // should not push out the W2 tiles other clusters still read
+            tma_store_2d_hint(&args.tmap_out, stg, nt * 2 * BN + part * 64, u * BM + q4 * 32, l2_evict_first());
             stores = true;
           }
         }

@@ -59,6 +59,10 @@ constexpr int THREADS = 320;
 constexpr int MAX_STAGES = 8;
 constexpr int TMEM_COLS = 512;
 constexpr int STAGE_TILE = 32 * 128;             // FP32 output staging per epilogue warp
+
+// Staging tiles per epilogue warp: two for the SwiGLU backward (saved u in
+// and du out, double-buffered), one otherwise.
+__host__ __device__ constexpr int stage_tiles(int mode) { return mode == BWD_DGRAD_SWIGLU ? 2 : 1; }
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 struct BTail {
@@ -444,36 +448,37 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 
 // SwiGLU backward of the 32 columns f0.. of a warp's 32 rows (FP32 dh of the
 // lane's row in v).  The rows' gate and up segments (64 bytes each) pass
-// through the warp's staging tile both ways: gate of row r at stg + 64 r,
-// up at stg + 2048 + 64 r, 16-byte chunk j at chunk j ^ ((r / 2) % 4) (eight
-// consecutive rows cover all eight 16-byte bank groups).  Loads and stores
-// go four lanes per row, eight rows per instruction, instead of one row per
-// lane.
-__device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint16_t* u_row0, uint16_t* du_row0,
-                                             int F, int f0, uint32_t stg, int lane) {
-  const int64_t ld = 2 * (int64_t)F;  // elements per row of u and du
+// through one of the warp's two staging tiles both ways: gate of row r at
+// tile + 64 r, up at tile + 2048 + 64 r, 16-byte chunk j at chunk
+// j ^ ((r / 2) % 4) (eight consecutive rows cover all eight 16-byte bank
+// groups).  Copies and stores go four lanes per row, eight rows per
+// instruction, instead of one row per lane.  The segments of the next chunk
+// are copied in (cp.async, one group per chunk) while this one is computed.
+__device__ __forceinline__ void swiglu_u_fetch(const uint16_t* u_row0, int F, int f0, uint32_t tile, int lane) {
+  const int64_t ld = 2 * (int64_t)F;  // elements per row of u
   const int cj = lane & 3;
-  // all eight loads first (a shared-memory store between them would make
-  // each wait for the one before)
-  uint4 g[4], x[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int rr = i * 8 + (lane >> 2);
-    g[i] = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + f0) + cj);
-    x[i] = __ldg(reinterpret_cast<const uint4*>(u_row0 + rr * ld + F + f0) + cj);
-  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int rr = i * 8 + (lane >> 2);
     const uint32_t off = rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4);
-    sts128(stg + off, g[i].x, g[i].y, g[i].z, g[i].w);
-    sts128(stg + 2048 + off, x[i].x, x[i].y, x[i].z, x[i].w);
+    cp_async16(tile + off, reinterpret_cast<const uint4*>(u_row0 + rr * ld + f0) + cj, true);
+    cp_async16(tile + 2048 + off, reinterpret_cast<const uint4*>(u_row0 + rr * ld + F + f0) + cj, true);
   }
+  cp_async_commit();
+}
+
+// PENDING: copy groups issued after this chunk's (0 or 1).
+template <int PENDING>
+__device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], uint16_t* du_row0, int F, int f0, uint32_t tile,
+                                             int lane) {
+  const int64_t ld = 2 * (int64_t)F;  // elements per row of du
+  const int cj = lane & 3;
+  asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
   __syncwarp();
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t off = lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
-    const uint4 g4 = lds128(stg + off), u4 = lds128(stg + 2048 + off);
+    const uint4 g4 = lds128(tile + off), u4 = lds128(tile + 2048 + off);
     const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
     uint32_t og[4], ou[4];
 #pragma unroll
@@ -491,16 +496,16 @@ __device__ __forceinline__ void swiglu_bwd32(const uint32_t (&v)[32], const uint
       og[p] = pack2_rn(rg[0], rg[1]);
       ou[p] = pack2_rn(ru[0], ru[1]);
     }
-    sts128(stg + off, og[0], og[1], og[2], og[3]);
-    sts128(stg + 2048 + off, ou[0], ou[1], ou[2], ou[3]);
+    sts128(tile + off, og[0], og[1], og[2], og[3]);
+    sts128(tile + 2048 + off, ou[0], ou[1], ou[2], ou[3]);
   }
   __syncwarp();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int rr = i * 8 + (lane >> 2);
     const uint32_t off = rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4);
-    reinterpret_cast<uint4*>(du_row0 + rr * ld + f0)[cj] = lds128(stg + off);
-    reinterpret_cast<uint4*>(du_row0 + rr * ld + F + f0)[cj] = lds128(stg + 2048 + off);
+    reinterpret_cast<uint4*>(du_row0 + rr * ld + f0)[cj] = lds128(tile + off);
+    reinterpret_cast<uint4*>(du_row0 + rr * ld + F + f0)[cj] = lds128(tile + 2048 + off);
   }
   __syncwarp();
 }
@@ -519,7 +524,8 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
   const int q4 = warp & 3, part = warp >> 2;
   const int rl = q4 * 32 + lane;
   const int half = a.bn / 2;
-  const uint32_t stg = staging + (uint32_t)warp * STAGE_TILE;
+  const bool sw = a.mode == BWD_DGRAD_SWIGLU;
+  const uint32_t stg = staging + (uint32_t)warp * (uint32_t)stage_tiles(a.mode) * STAGE_TILE;
   bool pending = false;  // lane 0: a store from stg may still be reading it
   uint32_t it = 0;
   const uint32_t tempty0 = PAIR ? b_map_to_rank(smem_u32(&tl->tempty[0]), 0) : smem_u32(&tl->tempty[0]);
@@ -533,15 +539,24 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
     }
     const uint32_t acc = it & 1u, ause = it >> 1;
     ++it;
+    const int64_t row0 = (int64_t)U.mt * BM + q4 * 32;  // DGRAD_SWIGLU: the warp's first row
+    // DGRAD_SWIGLU: the first chunk's saved u is copied in before the wait
+    if (sw && !U.ghost) swiglu_u_fetch(a.u + row0 * 2 * a.F, a.F, c0, stg, lane);
     if (!bwarp_wait(smem_u32(&tl->tfull[acc]), ause & 1u, abort_flag, a.status)) break;
     tc_fence_after();
     const uint32_t tbase = tmem + ((uint32_t)(q4 * 32) << 16) + acc * (uint32_t)a.bn + part * half;
     for (int c = 0; c < half && !U.ghost; c += 32) {
       uint32_t v[32];
       tld32(tbase + c, v);
-      if (a.mode == BWD_DGRAD_SWIGLU) {
-        const int64_t row0 = (int64_t)U.mt * BM + q4 * 32;
-        swiglu_bwd32(v, a.u + row0 * 2 * a.F, a.du + row0 * 2 * a.F, a.F, c0 + c, stg, lane);
+      if (sw) {
+        const uint32_t tile = stg + (uint32_t)((c >> 5) & 1) * STAGE_TILE;
+        if (c + 32 < half) {
+          swiglu_u_fetch(a.u + row0 * 2 * a.F, a.F, c0 + c + 32, stg + (uint32_t)(((c >> 5) + 1) & 1) * STAGE_TILE,
+                         lane);
+          swiglu_bwd32<1>(v, a.du + row0 * 2 * a.F, a.F, c0 + c, tile, lane);
+        } else {
+          swiglu_bwd32<0>(v, a.du + row0 * 2 * a.F, a.F, c0 + c, tile, lane);
+        }
       } else {
         const int orow0 = a.mode == BWD_WGRAD ? U.e * a.Mo + U.mt * BM + q4 * 32 : U.mt * BM + q4 * 32;
         if (lane == 0 && pending) bulk_wait_read0();
@@ -566,6 +581,7 @@ __device__ void epilogue(const BwdGemmArgs& a, const Plan& P, BTail* tl, uint32_
         mbar_arrive(tempty0 + 8u * acc);
     }
   }
+  if (sw) cp_async_wait_all();  // no copy into shared memory outlives the CTA
   if (lane == 0 && pending) bulk_wait0();  // the last stores complete before the CTA exits
   __syncwarp();
 }
@@ -584,7 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
   const int bcols = PAIR ? a.bn / 2 : a.bn;
   const uint32_t stage_bytes = A_TILE + bcols * 128;
   uint8_t* staging = smem + (size_t)a.stages * stage_bytes;
-  BTail* tl = reinterpret_cast<BTail*>(staging + NEPI * STAGE_TILE);
+  BTail* tl = reinterpret_cast<BTail*>(staging + NEPI * stage_tiles(a.mode) * STAGE_TILE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? b_cluster_rank() : 0u;
   if (threadIdx.x == 0) {
@@ -655,16 +671,26 @@ __global__ void __launch_bounds__(THREADS, 1) bwd_gemm_kernel(const __grid_const
   }
 }
 
-int bwd_gemm_smem_bytes(int bn, int stages) {
-  return 1024 + stages * (A_TILE + bn * 128) + NEPI * STAGE_TILE + (int)sizeof(BTail);
+int bwd_gemm_smem_bytes(int mode, int bn, int stages) {
+  return 1024 + stages * (A_TILE + bn * 128) + NEPI * stage_tiles(mode) * STAGE_TILE + (int)sizeof(BTail);
+}
+
+// The most stages, up to `most`, whose shared memory fits one CTA (B tiles of
+// `bcols` columns).
+static int fit_stages(int mode, int bcols, int most) {
+  int s = most;
+  while (s > 2 && bwd_gemm_smem_bytes(mode, bcols, s) > 232448) --s;
+  return s;
 }
 
 // max_row_tiles: for dgrad, an upper bound of offsets[E] / 128 (the number
 // of units is read on the device); ignored for wgrad.
 // The GEMMs with N % 256 == 0 (and, for wgrad, Mo % 256 == 0) run on CTA
 // pairs, six 32 KB stages per CTA; the rest on single CTAs with four 48 KB
-// (N tile 256) or six 32 KB (N tile 128) stages.  MOE_BWD_CTA_PAIRS=0 in the
-// environment selects single CTAs throughout.
+// (N tile 256) or six 32 KB (N tile 128) stages.  The SwiGLU backward's
+// second staging tile per warp takes one stage's room where they do not all
+// fit.  MOE_BWD_CTA_PAIRS=0 in the environment selects single CTAs
+// throughout.
 int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream) {
   a.bn = a.N % 256 == 0 ? 256 : 128;
   const int ntn = a.N / a.bn;
@@ -673,8 +699,8 @@ int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream) {
   int sms = gemm_num_ctas();
   if (sms <= 0) return -1;
   if (pairs) {
-    a.stages = 6;
-    const int smem = bwd_gemm_smem_bytes(a.bn / 2, a.stages);
+    a.stages = fit_stages(a.mode, a.bn / 2, 6);
+    const int smem = bwd_gemm_smem_bytes(a.mode, a.bn / 2, a.stages);
     if (cudaFuncSetAttribute(bwd_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return -1;
     cudaLaunchConfig_t cfg = {};
@@ -703,9 +729,9 @@ int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream) {
       return cudaLaunchKernelEx(&cfg, bwd_gemm_kernel<true>, a) == cudaSuccess ? 0 : -1;
     }
   }
-  a.stages = a.bn == 256 ? 4 : 6;
+  a.stages = fit_stages(a.mode, a.bn, a.bn == 256 ? 4 : 6);
   const int64_t max_units = a.mode == BWD_WGRAD ? (int64_t)a.E * (a.Mo / BM) * ntn : (int64_t)max_row_tiles * ntn;
-  const int smem = bwd_gemm_smem_bytes(a.bn, a.stages);
+  const int smem = bwd_gemm_smem_bytes(a.mode, a.bn, a.stages);
   if (cudaFuncSetAttribute(bwd_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return -1;
   int grid = sms;

@@ -392,9 +392,15 @@ int moe_expert_forward_train(const uint16_t* x, const float* logits, int T,
  *   dx f32 [T][d], dW1 f32 [E][2 d_ff][d], dW2 f32 [E][d][d_ff],
  *   dw f32 [T][k] (out); dlogits f32 [T][E] (out, or NULL to skip)
  *   ws        moe_expert_backward_workspace_bytes(...) bytes
- * Eight launches on `stream` (FC2 recomputation with dw and dy2, x rows,
- * logits, four tcgen05 BF16 grouped GEMMs, dx reduce), no host
- * synchronisation.  Experts without rows get zero weight gradients.
+ * Eight launches (FC2 recomputation with dw and dy2, x rows, logits, four
+ * tcgen05 BF16 grouped GEMMs, dx reduce), no host synchronisation.  All run
+ * on `stream` but the x-row copy, which runs on a second stream the library
+ * owns (one per host thread and device, created on first use), forked from
+ * `stream` after the FC2 recomputation and joined back before the dW1 GEMM
+ * by events, so that it overlaps the GEMMs before it; MOE_BWD_SIDE_STREAM=0
+ * in the environment keeps it on `stream` (same results bit for bit).  The
+ * call is complete, for `stream`, when its last launch is.  Experts without
+ * rows get zero weight gradients.
  * Errors: MOE_ERR_SHAPE as moe_expert_forward, MOE_ERR_POINTER,
  * MOE_ERR_WORKSPACE, MOE_ERR_DEVICE, MOE_ERR_CUDA; a wait that runs out sets
  * MOE_STATUS_TIMEOUT. */

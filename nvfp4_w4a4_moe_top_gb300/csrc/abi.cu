@@ -1,6 +1,7 @@
 // C ABI of libmoe_nvfp4.so (declared in include/moe_nvfp4.h): argument
 // validation on the host, TMA tensor-map encoding, workspace layout and the
 // launch sequence of each entry point.  No allocation, no synchronisation.
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -64,6 +65,34 @@ int check_device() {
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
   return MOE_OK;
+}
+
+// A second stream per host thread and device, with its fork and join
+// events, on which the backward copies the permuted x rows while the GEMMs
+// before the one that reads them run (created on first use, kept for the
+// thread's life).  Returns false where it cannot be created; the caller then
+// stays on its own stream.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false;
+};
+bool side_stream(SideStream*& out) {
+  thread_local SideStream side[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  SideStream& ss = side[dev];
+  if (!ss.tried) {
+    ss.tried = true;
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+      (void)cudaGetLastError();
+      ss.s = nullptr;
+    }
+  }
+  out = &ss;
+  return ss.s != nullptr;
 }
 
 // 2-D byte tensor of `rows` rows of `row_bytes` bytes, read in boxes of
@@ -446,41 +475,62 @@ int moe_expert_backward(const uint16_t* dY, const uint16_t* x, int T, int E, int
   a2.dY = dY; a2.dw = dw; a2.status = status;
   if (encode_bf16(&a2.tmap_out, dy2, mc, d, 32) != MOE_OK) return MOE_ERR_CUDA;
   if (moe::launch_fc2(a2, mc, s) != 0) return MOE_ERR_CUDA;
-  moe::launch_bwd_xrows(x, row_to_token, offsets, E, T, d, mc, xp, s);
   if (dlogits) moe::launch_bwd_logits(dw, topk_w, topk_ids, T, E, k, dlogits, s);
+  // The permuted x rows (read only by the dW1 GEMM) are copied on a second
+  // stream, by one block per SM, beside the three GEMMs before dW1: both fit
+  // on an SM together, and the copy's HBM traffic fills what the GEMMs leave.
+  // (MOE_BWD_SIDE_STREAM=0 in the environment keeps it on the caller's stream.)
+  const char* side_env = std::getenv("MOE_BWD_SIDE_STREAM");
+  SideStream* side = nullptr;
+  const bool forked = !(side_env && side_env[0] == '0') && side_stream(side) &&
+                      cudaEventRecord(side->fork, s) == cudaSuccess &&
+                      cudaStreamWaitEvent(side->s, side->fork, 0) == cudaSuccess;
+  if (forked) {
+    moe::launch_bwd_xrows(x, row_to_token, offsets, E, T, d, mc, xp, moe::gemm_num_ctas(), side->s);
+    if (cudaEventRecord(side->join, side->s) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    (void)cudaGetLastError();
+    moe::launch_bwd_xrows(x, row_to_token, offsets, E, T, d, mc, xp, 0, s);
+  }
+  // an early return still leaves the caller's stream waiting for the copy
+  auto fail = [&]() {
+    if (forked) (void)cudaStreamWaitEvent(s, side->join, 0);
+    return MOE_ERR_CUDA;
+  };
 
   moe::BwdGemmArgs g;
   // dh = dy2 . W2_e, SwiGLU backward -> du
   std::memset(&g, 0, sizeof(g));
   if (encode_bf16(&g.tmap_a, dy2, mc, d, 128) != MOE_OK || encode_bf16(&g.tmap_b, W2, (int64_t)E * d, F, 64) != MOE_OK)
-    return MOE_ERR_CUDA;
+    return fail();
   g.mode = moe::BWD_DGRAD_SWIGLU; g.a_mn = 0; g.E = E; g.offsets = offsets; g.N = F; g.K = d; g.F = F;
   g.u = u; g.du = du; g.status = status;
-  if (moe::launch_bwd_gemm(g, (int)(mc / 128), s) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_bwd_gemm(g, (int)(mc / 128), s) != 0) return fail();
   // dW2_e = dy2_e^T . h_e
   std::memset(&g, 0, sizeof(g));
   if (encode_bf16(&g.tmap_a, dy2, mc, d, 64) != MOE_OK || encode_bf16(&g.tmap_b, h, mc, F, 64) != MOE_OK)
-    return MOE_ERR_CUDA;
-  if (encode_f32_out(&g.tmap_out, dW2, (int64_t)E * d, F) != MOE_OK) return MOE_ERR_CUDA;
+    return fail();
+  if (encode_f32_out(&g.tmap_out, dW2, (int64_t)E * d, F) != MOE_OK) return fail();
   g.mode = moe::BWD_WGRAD; g.a_mn = 1; g.E = E; g.offsets = offsets; g.N = F; g.Mo = d; g.out = dW2; g.status = status;
-  if (moe::launch_bwd_gemm(g, 0, s) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_bwd_gemm(g, 0, s) != 0) return fail();
   // dxr = du . W1_e
   std::memset(&g, 0, sizeof(g));
   if (encode_bf16(&g.tmap_a, du, mc, 2 * F, 128) != MOE_OK ||
       encode_bf16(&g.tmap_b, W1, (int64_t)E * 2 * F, d, 64) != MOE_OK)
-    return MOE_ERR_CUDA;
-  if (encode_f32_out(&g.tmap_out, dxr, mc, d) != MOE_OK) return MOE_ERR_CUDA;
+    return fail();
+  if (encode_f32_out(&g.tmap_out, dxr, mc, d) != MOE_OK) return fail();
   g.mode = moe::BWD_DGRAD; g.a_mn = 0; g.E = E; g.offsets = offsets; g.N = d; g.K = 2 * F; g.out = dxr;
   g.status = status;
-  if (moe::launch_bwd_gemm(g, (int)(mc / 128), s) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_bwd_gemm(g, (int)(mc / 128), s) != 0) return fail();
   // dW1_e = du_e^T . xp_e
+  if (forked && cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess) return fail();
   std::memset(&g, 0, sizeof(g));
   if (encode_bf16(&g.tmap_a, du, mc, 2 * F, 64) != MOE_OK || encode_bf16(&g.tmap_b, xp, mc, d, 64) != MOE_OK)
-    return MOE_ERR_CUDA;
-  if (encode_f32_out(&g.tmap_out, dW1, (int64_t)E * 2 * F, d) != MOE_OK) return MOE_ERR_CUDA;
+    return fail();
+  if (encode_f32_out(&g.tmap_out, dW1, (int64_t)E * 2 * F, d) != MOE_OK) return fail();
   g.mode = moe::BWD_WGRAD; g.a_mn = 1; g.E = E; g.offsets = offsets; g.N = d; g.Mo = 2 * F; g.out = dW1;
   g.status = status;
-  if (moe::launch_bwd_gemm(g, 0, s) != 0) return MOE_ERR_CUDA;
+  if (moe::launch_bwd_gemm(g, 0, s) != 0) return fail();
   moe::launch_bwd_dx(dxr, token_slot_row, T, k, d, dx, s);
   return finish();
 }

@@ -745,24 +745,25 @@ int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream) {
 // Row, logit and dx kernels (HBM-bound, one warp per row or token)
 // ---------------------------------------------------------------------------
 // xp[r] = x[row_to_token[r]] (the wgrad operand of FC1), zero on pad rows;
-// rows at or past offsets[E] are left alone.  d % 8 == 0.
+// rows at or past offsets[E] are left alone.  d % 8 == 0.  One warp per row,
+// the warps of the grid striding over the rows.
 __global__ void __launch_bounds__(256) bwd_xrows_kernel(const uint16_t* __restrict__ x,
                                                         const int32_t* __restrict__ row_to_token,
                                                         const int32_t* __restrict__ offsets, int E, int T, int d,
                                                         int64_t m_rows, uint16_t* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= m_rows) return;
-  if (r >= __ldg(offsets + E)) return;  // past the padded rows: never read
+  const int64_t end = min(m_rows, (int64_t)__ldg(offsets + E));  // past the padded rows: never read
   const int n8 = d / 8;
-  uint4* xrow = reinterpret_cast<uint4*>(xp + r * d);
-  const int t = __ldg(row_to_token + r);
-  if (t < 0 || t >= T) {
-    for (int i = lane; i < n8; i += 32) xrow[i] = make_uint4(0u, 0u, 0u, 0u);
-    return;
+  for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < end; r += (int64_t)gridDim.x * 8) {
+    uint4* xrow = reinterpret_cast<uint4*>(xp + r * d);
+    const int t = __ldg(row_to_token + r);
+    if (t < 0 || t >= T) {
+      for (int i = lane; i < n8; i += 32) xrow[i] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const uint4* xsrc = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
+    for (int i = lane; i < n8; i += 32) xrow[i] = __ldg(xsrc + i);
   }
-  const uint4* xsrc = reinterpret_cast<const uint4*>(x + (int64_t)t * d);
-  for (int i = lane; i < n8; i += 32) xrow[i] = __ldg(xsrc + i);
 }
 
 // dlogits[t][:] = 0, then w_j (dw_j - sum_i w_i dw_i) at the selected ids.
@@ -811,10 +812,14 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(const float* __restrict__ d
   }
 }
 
+// blocks > 0: that many blocks stride over the rows (a grid small enough to
+// run beside a persistent GEMM); else one block per eight rows.
 int launch_bwd_xrows(const uint16_t* x, const int32_t* row_to_token, const int32_t* offsets, int E, int T, int d,
-                     int64_t m_rows, uint16_t* xp, cudaStream_t stream) {
+                     int64_t m_rows, uint16_t* xp, int blocks, cudaStream_t stream) {
   if (m_rows <= 0) return 0;
-  bwd_xrows_kernel<<<(unsigned)((m_rows + 7) / 8), 256, 0, stream>>>(x, row_to_token, offsets, E, T, d, m_rows, xp);
+  const int64_t all = (m_rows + 7) / 8;
+  const unsigned grid = (unsigned)(blocks > 0 && blocks < all ? blocks : all);
+  bwd_xrows_kernel<<<grid, 256, 0, stream>>>(x, row_to_token, offsets, E, T, d, m_rows, xp);
   return 0;
 }
 

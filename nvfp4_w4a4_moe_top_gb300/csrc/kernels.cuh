@@ -124,7 +124,7 @@ struct BwdGemmArgs {
 };
 int launch_bwd_gemm(BwdGemmArgs& a, int max_row_tiles, cudaStream_t stream);
 int launch_bwd_xrows(const uint16_t* x, const int32_t* row_to_token, const int32_t* offsets, int E, int T, int d,
-                     int64_t m_rows, uint16_t* xp, cudaStream_t stream);
+                     int64_t m_rows, uint16_t* xp, int blocks, cudaStream_t stream);
 int launch_bwd_logits(const float* dw, const float* topk_w, const int32_t* topk_ids, int T, int E, int k,
                       float* dlogits, cudaStream_t stream);
 int launch_bwd_dx(const float* dxr, const int32_t* token_slot_row, int T, int k, int d, float* dx, cudaStream_t stream);

@@ -160,6 +160,20 @@ def test_backward_cta_pairs_equal_single(orc, name, monkeypatch):
         assert np.array_equal(r1[key].view(np.uint8), r2[key].view(np.uint8)), key
 
 
+@pytest.mark.parametrize("name", ["small", "ragged"])
+def test_backward_side_stream_equals_one_stream(orc, name, monkeypatch):
+    """The permuted-row copy on the second stream (beside the GEMMs) and on
+    the caller's stream: every gradient bit for bit."""
+    lay = layer_of(name)
+    x, lg, W1, W2, dY = lay.x(), lay.logits(), lay.w1(), lay.w2(), lay.grad_out()
+    r2 = gpu_train_step(lay, x, lg, W1, W2, dY)
+    monkeypatch.setenv("MOE_BWD_SIDE_STREAM", "0")
+    r1 = gpu_train_step(lay, x, lg, W1, W2, dY)
+    assert r1["status"] == 0 and r2["status"] == 0
+    for key in ("xp", "du", "dx", "dW1", "dW2", "dw", "dlogits"):
+        assert np.array_equal(r1[key].view(np.uint8), r2[key].view(np.uint8)), key
+
+
 def test_empty_experts_get_zero_weight_gradients(orc):
     lay = layer_of("ragged")
     x, lg, W1, W2, dY = lay.x(), lay.logits(), lay.w1(), lay.w2(), lay.grad_out()

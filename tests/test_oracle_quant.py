@@ -169,6 +169,29 @@ def test_sf_layout_is_a_bijection_of_128x4_tiles(orc):
         assert len(np.unique(rr)) == 128 and len(np.unique(cc)) == 4
 
 
+def test_sf_layout_matches_tile_reshape(orc):
+    """The block-scale layout built another way: a tile holds the scales of
+    128 rows x 4 columns (4 blocks of 16 elements along K, one scale each)
+    as a 32 x 16-byte array whose row i carries, for each of
+    the row groups j = 0..3, the 4 column scales of row 32 j + i (the
+    tensor core's block-scale tile: each of the 32 lanes of a 32-row quadrant
+    reads one 16-byte row).  Tiles follow row block by row block, column
+    group fastest.  Built here by reshaping the logical [rows][K/16] array,
+    not from the oracle's offset formula, and compared through the oracle's
+    unswizzle."""
+    rng = np.random.default_rng(21)
+    rows, K = 256, 192
+    logical = rng.integers(0, 256, size=(rows, K // 16), dtype=np.uint8)
+    tiles = []
+    for b in range(rows // 128):
+        for g in range(K // 64):
+            t = logical[128 * b:128 * (b + 1), 4 * g:4 * (g + 1)]  # [128 rows][4 columns]
+            tiles.append(t.reshape(4, 32, 4).transpose(1, 0, 2).reshape(512))  # [lane i][group j][column c]
+    buf = np.concatenate(tiles)
+    assert buf.size == orc.sf_bytes(rows, K)
+    assert np.array_equal(orc.unswizzle_sf(buf, rows, K), logical)
+
+
 def test_context_swap_invariance(orc):
     """Per-token scales: a row's codes, scales and outer scale do not depend on
     the other rows of the batch (the context-swap property of the AI summary's

@@ -1344,7 +1344,7 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
 }
 
 
-// FC2 on CTA pairs (the forward; MODE 0 and 1): clusters of two CTAs, a
+// FC2 on CTA pairs (MODE as fc2_scatter_kernel's): clusters of two CTAs, a
 // unit being two 128-row tiles of one expert, walked as FC1's pair units
 // (ghost tile included).  An item is 256 output columns: rank 0's B tile
 // holds W2 rows nt*256 .. +127, rank 1's the next 128; one cta_group::2 MMA
@@ -1355,8 +1355,14 @@ __global__ void __launch_bounds__(Roles<FC2_NE>::THREADS, 1) fc2_scatter_kernel(
 // second round trip has landed; z = BF16(w * acc * (g_h * g_w2)) goes
 // through the warp's swizzled 32 x 64 staging tile to one TMA tensor store,
 // as in the single-CTA kernel.  A ghost tile computes but stores nothing.
-template <bool DBG>
+// MODE 2: the staging tile first receives the item's output-gradient
+// segments (cp.async, issued before the accumulator wait); each row's dY
+// values are read back for dw and replaced by dy2 = BF16(w dY) in place,
+// which then leaves by the tile's TMA store.  dw of a row: the four column
+// parts' sums, ((p0 + p1) + p2) + p3.
+template <int MODE>
 __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(const __grid_constant__ Fc2Args args) {
+  constexpr bool DBG = MODE == 1, DW = MODE == 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int d = args.d, k = args.k;
@@ -1406,10 +1412,10 @@ __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(co
       const int64_t row = (int64_t)u * BM + rl;
       const int t = args.row_to_token[row];
       float w = 0.0f;
+      int j = 0;
       if (t >= 0) {
         // slot of this row among the token's k (loads issued eight at a time)
         const int32_t* ts = args.token_slot_row + (int64_t)t * k;
-        int j = 0;
         for (int j0 = 0; j0 < k; j0 += 8) {
           int v8[8];
 #pragma unroll
@@ -1424,7 +1430,29 @@ __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(co
       float* gws = gw_s + (uc & 1) * d;
       stage_scales<FC2P_NE>(gws, args.w_g + (int64_t)e * d, d, threadIdx.x);
       epi_barrier<FC2P_NE>();
+      // DW: the row's output gradient, and its partial dot product with y2
+      const uint16_t* dy_row = DW ? args.dY + (int64_t)(t < 0 ? 0 : t) * d : nullptr;
+      float dot = 0.0f;
       for (int nt = 0; nt < G.items; ++nt, ++it) {
+        if (DW && !ghost) {
+          // the staging tile receives this item's 32 output-gradient row
+          // segments (64 columns each; 8 lanes per row, 4 rows per
+          // instruction, zeros for pad rows) once the previous store has
+          // read it
+          if (lane == 0 && stores) bulk_wait_read0();
+          __syncwarp();
+          const unsigned long long my_src =
+              t >= 0 ? reinterpret_cast<unsigned long long>(dy_row + nt * 2 * BN + part * 64) : 0ull;
+          const int sub = lane >> 3, ch = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + sub;
+            const unsigned long long sp = __shfl_sync(0xFFFFFFFFu, my_src, rr);
+            cp_async16(stg + rr * FC2_STAGE_ROW + 16 * (ch ^ (rr & 7)),
+                       sp ? reinterpret_cast<const uint4*>(sp) + ch : reinterpret_cast<const uint4*>(args.dY), sp != 0);
+          }
+          cp_async_commit();
+        }
         bool ok = __all_sync(0xFFFFFFFFu, !abort_flag.raised());
         if (ok) ok = warp_wait(smem_u32(&tl->tfull[0]), it & 1u, abort_flag, args.status);
         auto release = [&]() {
@@ -1432,9 +1460,13 @@ __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(co
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(tempty0);
         };
-        uint32_t zp[32];  // the row's 64 z values, packed pairs
+        uint32_t zp[32];  // the row's 64 z (DW: dy2) values, packed pairs
         if (ok) {
           tc_fence_after();
+          if (DW && !ghost) {  // this item's output-gradient segments have landed
+            cp_async_wait_all();
+            __syncwarp();
+          }
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t R[2][16];
@@ -1456,9 +1488,22 @@ __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(co
                   const int m = i + jj;
                   const float y0 = __fmul_rn(__uint_as_float(R[hf][m]), __fmul_rn(gh, f[jj]));
                   const float y1 = __fmul_rn(__uint_as_float(R[hf][m + 1]), __fmul_rn(gh, f[jj + 1]));
-                  zp[(c0 + m) >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
+                  if (!DW) zp[(c0 + m) >> 1] = bf16x2_rn(__fmul_rn(w, y0), __fmul_rn(w, y1));
                   yv[m] = y0;
                   yv[m + 1] = y1;
+                }
+              }
+              if (DW && !ghost) {  // this row's 16 output-gradient columns, from the staging tile
+                const int c8 = c0 >> 3;  // 16-byte chunk of the row
+                const uint4 g0 = lds128(stg + lane * FC2_STAGE_ROW + 16 * (c8 ^ (lane & 7)));
+                const uint4 g1 = lds128(stg + lane * FC2_STAGE_ROW + 16 * ((c8 + 1) ^ (lane & 7)));
+                const uint32_t gw4[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float d0 = bf16_lo(gw4[q]), d1 = bf16_hi(gw4[q]);
+                  dot = fmaf(d0, yv[2 * q], dot);
+                  dot = fmaf(d1, yv[2 * q + 1], dot);
+                  zp[(c0 >> 1) + q] = bf16x2_rn(__fmul_rn(w, d0), __fmul_rn(w, d1));
                 }
               }
               if (DBG && args.dbg_y && t >= 0 && !ghost) {
@@ -1473,7 +1518,9 @@ __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(co
         }
         if (ok && !ghost) {
           // the staging tile is free once the previous store has read it
-          if (lane == 0 && stores) bulk_wait_read0();
+          // (DW: that was waited for before the output gradient came in, and
+          // each lane overwrites only its own row, which it has read)
+          if (!DW && lane == 0 && stores) bulk_wait_read0();
           __syncwarp();
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch)
@@ -1484,14 +1531,25 @@ __global__ void __launch_bounds__(Roles<FC2P_NE>::THREADS, 1) fc2_pair_kernel(co
           if (lane == 0) {
             // evict-first: the 2.15 GB of z rows pass through L2 once, and
             // should not push out the W2 tiles other clusters still read
-            tma_store_2d_hint(&args.tmap_out, stg, nt * 2 * BN + part * 64, u * BM + q4 * 32, l2_evict_first());
+            // (DW: dy2, which the next GEMM reads, keeps the default policy)
+            if (DW)
+              tma_store_2d(&args.tmap_out, stg, nt * 2 * BN + part * 64, u * BM + q4 * 32);
+            else
+              tma_store_2d_hint(&args.tmap_out, stg, nt * 2 * BN + part * 64, u * BM + q4 * 32, l2_evict_first());
             stores = true;
           }
         }
       }
+      if (DW) {  // dw of the row: the four column parts' sums in a fixed order
+        tl->rowmax[part][rl] = dot;
+        epi_barrier<FC2P_NE>();
+        if (part == 0 && t >= 0 && !ghost)
+          args.dw[(int64_t)t * k + j] = ((dot + tl->rowmax[1][rl]) + tl->rowmax[2][rl]) + tl->rowmax[3][rl];
+      }
       // every read of this unit's scale buffer precedes the barrier that
       // precedes the staging of the unit after next into it
     }
+    if (DW) cp_async_wait_all();  // no copy into shared memory outlives the CTA
     if (lane == 0 && stores) bulk_wait0();  // the stores complete before the CTA exits
     __syncwarp();
   }
@@ -1663,18 +1721,20 @@ int launch_fc1(Fc1Args& a, int64_t m_cap, cudaStream_t stream) {
   return 0;
 }
 
-// FC2 runs on CTA pairs (clusters of two) for the forward where the pair
-// plan fits, d is a multiple of 256 and clusters of two can be resident;
-// the backward's recomputation (dw set) runs on single CTAs.
+// FC2 runs on CTA pairs (clusters of two) where the pair plan fits, d is a
+// multiple of 256 and clusters of two can be resident, the forward and the
+// backward's recomputation (dw set) alike; elsewhere on single CTAs.
 // MOE_FC2_CTA_PAIRS=0 in the environment selects single CTAs throughout.
 int launch_fc2(Fc2Args& a, int64_t m_cap, cudaStream_t stream) {
   size_t smem;
   const char* env = std::getenv("MOE_FC2_CTA_PAIRS");
-  const bool allow_pairs = !(env && env[0] == '0') && a.dw == nullptr && a.d % (2 * BN) == 0;
+  const bool allow_pairs = !(env && env[0] == '0') && a.d % (2 * BN) == 0;
   int pair_rings = 0;
   if (allow_pairs && plan_pair(a.d_ff, a.d / (2 * BN), (size_t)2 * a.d * 4, (size_t)FC2P_NE * 32 * FC2_STAGE_ROW,
                                &pair_rings, &smem)) {
-    void (*kern)(const Fc2Args) = a.dbg_y != nullptr ? fc2_pair_kernel<true> : fc2_pair_kernel<false>;
+    void (*kern)(const Fc2Args) = a.dw != nullptr      ? fc2_pair_kernel<2>
+                                   : a.dbg_y != nullptr ? fc2_pair_kernel<1>
+                                                        : fc2_pair_kernel<0>;
     if (set_smem((const void*)kern, smem) != 0) return -1;
     int clusters = pair_clusters(kern, smem, Roles<FC2P_NE>::THREADS);
     const int sms = gemm_num_ctas();

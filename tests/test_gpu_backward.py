@@ -160,6 +160,24 @@ def test_backward_cta_pairs_equal_single(orc, name, monkeypatch):
         assert np.array_equal(r1[key].view(np.uint8), r2[key].view(np.uint8)), key
 
 
+@pytest.mark.parametrize("name", ["small", "tiny", "ragged"])
+def test_backward_fc2_pairs_equal_single(orc, name, monkeypatch):
+    """The backward's FC2 recomputation on CTA pairs and on single CTAs: dy2
+    and every gradient that flows from it bit for bit; dw (a dot product
+    over d, summed in four column parts on pairs and two on single CTAs)
+    and the logit gradient within FP32 reassociation."""
+    lay = layer_of(name)
+    x, lg, W1, W2, dY = lay.x(), lay.logits(), lay.w1(), lay.w2(), lay.grad_out()
+    r2 = gpu_train_step(lay, x, lg, W1, W2, dY)
+    monkeypatch.setenv("MOE_FC2_CTA_PAIRS", "0")
+    r1 = gpu_train_step(lay, x, lg, W1, W2, dY)
+    assert r1["status"] == 0 and r2["status"] == 0
+    for key in ("dy2", "du", "dx", "dW1", "dW2"):
+        assert np.array_equal(r1[key].view(np.uint8), r2[key].view(np.uint8)), key
+    for key in ("dw", "dlogits"):
+        assert rel(r2[key], r1[key]) <= 1e-6, key
+
+
 @pytest.mark.parametrize("name", ["small", "ragged"])
 def test_backward_side_stream_equals_one_stream(orc, name, monkeypatch):
     """The permuted-row copy on the second stream (beside the GEMMs) and on

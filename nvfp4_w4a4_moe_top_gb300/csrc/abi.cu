@@ -320,7 +320,7 @@ int moe_permute_amax(const float* logits, const int32_t* ext_ids, const float* e
     return finish();
   }
   moe::launch_route(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, token_slot_row, hist, status, s);
-  moe::launch_scan(hist, C, E, counts, offsets, s);
+  moe::launch_scan(hist, C, E, counts, s);
   moe::launch_pad_rows(offsets, counts, E, mc, row_to_token, x ? amax_row : nullptr, nullptr, 64, nullptr, nullptr, s);
   moe::launch_permute_amax(topk_ids, token_slot_row, hist, offsets, T, E, k, x, d, row_to_token,
                            x ? amax_tok : nullptr, x ? amax_row : nullptr, status, s);
@@ -581,7 +581,7 @@ int forward_impl(const uint16_t* x, const float* logits, int T, int E, int k, in
   mark(0);
   moe::launch_route(logits, nullptr, nullptr, T, E, k, topk_ids, topk_w, tsr, hist, status, s);
   mark(1);
-  moe::launch_scan(hist, C, E, counts, offsets, s);
+  moe::launch_scan(hist, C, E, counts, s);
   mark(2);
   // gather: x_codes holds the codes once per token (rows 0..T-1) and a zero
   // row T, which the pad rows gather; otherwise one copy per routed row

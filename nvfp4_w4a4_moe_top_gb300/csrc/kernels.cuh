@@ -24,8 +24,9 @@ int launch_route(const float* logits, const int32_t* ext_ids, const float* ext_w
                  int32_t* topk_ids, float* topk_w, int32_t* token_slot_row, int32_t* hist, int* status,
                  cudaStream_t stream);
 
-// Chunk histograms -> exclusive chunk bases (in place), counts, padded offsets.
-int launch_scan(int32_t* hist, int C, int E, int32_t* counts, int32_t* offsets, cudaStream_t stream);
+// Chunk histograms -> exclusive chunk bases (in place) and counts; the
+// padded offsets come from launch_pad_rows, which runs next.
+int launch_scan(int32_t* hist, int C, int E, int32_t* counts, cudaStream_t stream);
 
 // Final rows of the slots, row_to_token, and (when x != NULL) per-token amax
 // gathered in the same pass.
@@ -33,9 +34,10 @@ int launch_permute_amax(const int32_t* topk_ids, int32_t* token_slot_row, const 
                         int T, int E, int k, const uint16_t* x, int d, int32_t* row_to_token, float* amax_tok,
                         float* amax_row, int* status, cudaStream_t stream);
 
-// Pad rows of every group (and rows >= M_pad up to m_cap): row_to_token = -1,
-// amax_row = 0, and when codes != NULL zero codes / block scales / g.
-int launch_pad_rows(const int32_t* offsets, const int32_t* counts, int E, int64_t m_cap, int32_t* row_to_token,
+// Padded offsets [E+1] from the counts, then the pad rows of every group
+// (and rows >= M_pad up to m_cap): row_to_token = -1, amax_row = 0, and when
+// codes != NULL zero codes / block scales / g.
+int launch_pad_rows(int32_t* offsets, const int32_t* counts, int E, int64_t m_cap, int32_t* row_to_token,
                     float* amax_row, uint8_t* codes, int K, uint8_t* sf, float* g, cudaStream_t stream);
 
 // Fused permute + amax + quantise of the forward: x read once, codes written

@@ -164,53 +164,45 @@ int launch_route(const float* logits, const int32_t* ext_ids, const float* ext_w
   return 0;
 }
 
-// One CTA of 1024 threads: G = 1024/E threads per expert sum the expert's
-// chunk counts, write exclusive chunk bases in place, then a block scan of
-// the 128-padded counts gives the offsets.
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int C, int E,
-                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  __shared__ int part[1024];
-  __shared__ int scan_a[1024], scan_b[1024];
-  const int G = max(1, 1024 / E);
-  const int e = threadIdx.x / G, gi = threadIdx.x % G;
-  const int per = (C + G - 1) / G;
-  const int c0 = min(C, gi * per), c1 = min(C, c0 + per);
-  int s = 0;
-  if (e < E)
-    for (int c = c0; c < c1; ++c) s += hist[(int64_t)c * E + e];
-  part[threadIdx.x] = s;
-  __syncthreads();
-  if (e < E) {
-    int run = 0;
-    for (int g2 = 0; g2 < gi; ++g2) run += part[e * G + g2];
-    for (int c = c0; c < c1; ++c) {
-      const int h = hist[(int64_t)c * E + e];
-      hist[(int64_t)c * E + e] = run;
-      run += h;
+// One CTA of 256 threads per expert e: the exclusive scan of the expert's
+// chunk counts over the chunks (written back in place as chunk bases) and
+// the expert's total (counts[e]).  The padded offsets follow in
+// pad_rows_kernel, which needs them first.
+__global__ void __launch_bounds__(256) scan_kernel(int32_t* __restrict__ hist, int C, int E,
+                                                   int32_t* __restrict__ counts) {
+  __shared__ int warp_sum[8];
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int run = 0;
+  for (int base = 0; base < C; base += 256) {
+    const int c = base + threadIdx.x;
+    const int v = c < C ? hist[(int64_t)c * E + e] : 0;
+    // inclusive scan within the warp, then across the 8 warps
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
     }
-  }
-  // padded counts, inclusive scan over experts (Hillis-Steele)
-  const int x = threadIdx.x;
-  int tot = 0;
-  if (x < E) {
-    for (int g2 = 0; g2 < G; ++g2) tot += part[x * G + g2];
-    counts[x] = tot;
-  }
-  scan_a[x] = (x < E) ? ((tot + 127) & ~127) : 0;
-  __syncthreads();
-  int* in = scan_a;
-  int* out = scan_b;
-  for (int o = 1; o < 1024; o <<= 1) {
-    out[x] = in[x] + (x >= o ? in[x - o] : 0);
+    if (lane == 31) warp_sum[wid] = x;
     __syncthreads();
-    int* tmp = in; in = out; out = tmp;
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int ws = warp_sum[w];
+      before += w < wid ? ws : 0;
+      total += ws;
+    }
+    if (c < C) hist[(int64_t)c * E + e] = run + before + x - v;
+    run += total;
+    __syncthreads();  // warp_sum is rewritten by the next round
   }
-  if (x < E) offsets[x + 1] = in[x];
-  if (x == 0) offsets[0] = 0;
+  if (threadIdx.x == 0) counts[e] = run;
 }
 
-int launch_scan(int32_t* hist, int C, int E, int32_t* counts, int32_t* offsets, cudaStream_t stream) {
-  scan_kernel<<<1, 1024, 0, stream>>>(hist, C, E, counts, offsets);
+int launch_scan(int32_t* hist, int C, int E, int32_t* counts, cudaStream_t stream) {
+  if (E < 1) return 0;
+  scan_kernel<<<E, 256, 0, stream>>>(hist, C, E, counts);
   return 0;
 }
 
@@ -264,17 +256,46 @@ int launch_permute_amax(const int32_t* topk_ids, int32_t* token_slot_row, const 
   return 0;
 }
 
-// Blocks [0, E): the pad rows of group e (fewer than 128); blocks >= E: rows
-// from the padded total up to m_cap (maps only; the GEMMs never read them).
-__global__ void __launch_bounds__(128) pad_rows_kernel(const int32_t* __restrict__ offsets,
+// First the padded offsets, which every block computes for itself from the
+// counts: off_e = sum over e' < e of ceil(count_e' / 128) * 128 (block e
+// writes offsets[e + 1], block 0 also offsets[0] = 0).  Then blocks [0, E):
+// the pad rows of group e (fewer than 128); blocks >= E: rows from the
+// padded total up to m_cap (maps only; the GEMMs never read them).
+__global__ void __launch_bounds__(128) pad_rows_kernel(int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ counts, int E, int64_t m_cap,
                                                        int32_t* __restrict__ row_to_token, float* __restrict__ amax_row,
                                                        uint8_t* __restrict__ codes, int K, uint8_t* __restrict__ sf,
                                                        float* __restrict__ g) {
+  __shared__ int part_before[4], part_all[4];
+  const int me = (int)blockIdx.x < E ? (int)blockIdx.x : E;  // the group whose start this block needs
+  int before = 0, all = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    const int pc = (counts[i] + 127) & ~127;
+    all += pc;
+    if (i < me) before += pc;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xFFFFFFFFu, before, o);
+    all += __shfl_xor_sync(0xFFFFFFFFu, all, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    part_before[threadIdx.x >> 5] = before;
+    part_all[threadIdx.x >> 5] = all;
+  }
+  __syncthreads();
+  const int64_t off_me = (int64_t)part_before[0] + part_before[1] + part_before[2] + part_before[3];
+  const int64_t total = (int64_t)part_all[0] + part_all[1] + part_all[2] + part_all[3];
   if ((int)blockIdx.x < E) {
     const int e = blockIdx.x;
-    const int64_t r = (int64_t)offsets[e] + counts[e] + threadIdx.x;
-    if (r >= offsets[e + 1]) return;
+    const int cnt = counts[e];
+    const int64_t end = off_me + ((cnt + 127) & ~127);
+    if (threadIdx.x == 0) {
+      offsets[e + 1] = (int32_t)end;
+      if (e == 0) offsets[0] = 0;
+    }
+    const int64_t r = off_me + cnt + threadIdx.x;
+    if (r >= end) return;
     row_to_token[r] = -1;
     if (amax_row) amax_row[r] = 0.0f;
     if (codes) {
@@ -288,8 +309,7 @@ __global__ void __launch_bounds__(128) pad_rows_kernel(const int32_t* __restrict
       g[r] = 0.0f;
     }
   } else {
-    const int64_t start = offsets[E];
-    for (int64_t r = start + (int64_t)(blockIdx.x - E) * blockDim.x + threadIdx.x; r < m_cap;
+    for (int64_t r = total + (int64_t)(blockIdx.x - E) * blockDim.x + threadIdx.x; r < m_cap;
          r += (int64_t)(gridDim.x - E) * blockDim.x) {
       row_to_token[r] = -1;
       if (amax_row) amax_row[r] = 0.0f;
@@ -297,7 +317,7 @@ __global__ void __launch_bounds__(128) pad_rows_kernel(const int32_t* __restrict
   }
 }
 
-int launch_pad_rows(const int32_t* offsets, const int32_t* counts, int E, int64_t m_cap, int32_t* row_to_token,
+int launch_pad_rows(int32_t* offsets, const int32_t* counts, int E, int64_t m_cap, int32_t* row_to_token,
                     float* amax_row, uint8_t* codes, int K, uint8_t* sf, float* g, cudaStream_t stream) {
   pad_rows_kernel<<<E + 64, 128, 0, stream>>>(offsets, counts, E, m_cap, row_to_token, amax_row, codes, K, sf, g);
   return 0;

@@ -206,7 +206,7 @@ int moe_permute_amax(const float* logits, const int32_t* ext_ids,
  * the library, held on every GPU that loads the library until the process
  * exits; nothing is allocated or freed.  Shapes whose scratch,
  * moe_permute_workspace_bytes(T, E), exceeds that size return
- * MOE_ERR_WORKSPACE before any CUDA call (with 1 MiB: T up to 524288 tokens
+ * MOE_ERR_WORKSPACE before any CUDA call (with 4 MiB: T up to 524288 tokens
  * at E = 128, 65536 at E = 1024).
  *
  * Every call looks up the array's device address on the current device
@@ -217,7 +217,7 @@ int moe_permute_amax(const float* logits, const int32_t* ext_ids,
  * calls share the one array, so calls whose GPU work overlaps (other streams
  * or host threads at the same time) race and give wrong results: serialise
  * them.  The array needs no clearing between calls. */
-#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1 << 20)
+#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1 << 22)
 int moe_permute_amax_noalloc(const float* logits, const int32_t* ext_ids,
                              const float* ext_w, const uint16_t* x, int T,
                              int E, int k, int d, int32_t* topk_ids,

@@ -6,7 +6,7 @@
 
 namespace moe {
 
-constexpr int kRouteChunk = 256;  // tokens per routing chunk (one CTA)
+constexpr int kRouteChunk = 64;  // tokens per routing chunk (one CTA); a multiple of 32
 
 // amax (optional) holds one entry per amax_rows consecutive source rows.
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,

@@ -10,7 +10,7 @@
 // with the same kernels, but takes no workspace argument.
 //
 // The array is a file-scope device variable of MOE_PERMUTE_NOALLOC_SCRATCH_BYTES
-// (1 MiB): every GPU on which the library is loaded keeps it until the process
+// (4 MiB): every GPU on which the library is loaded keeps it until the process
 // exits.  Host code cannot use the array's name as a device address, so every
 // call looks the address up on the current device with cudaGetSymbolAddress
 // (a table lookup once the device code is loaded).  The address is not kept

@@ -5,7 +5,7 @@
 // statistics, device-side expert offsets).
 //
 // The permutation is a deterministic stable counting sort with no
-// arrival-order atomics: per 256-token chunk, a bitmask per expert records
+// arrival-order atomics: per 64-token chunk, a bitmask per expert records
 // which tokens chose it (atomicOr is order-independent), a token's rank in
 // its expert is a popcount of the lower bits, chunk histograms are scanned
 // once, and a row is offsets[e] + chunk base + rank.
@@ -27,9 +27,12 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// One CTA per chunk of 256 tokens, 32 warps, one warp per token at a time.
+// One CTA per chunk of kChunk tokens, kChunk / 8 warps (8 tokens each), one
+// warp per token at a time.  Small chunks spread the tokens evenly over the
+// SMs (1024 CTAs for 64k tokens).
+constexpr int kRouteThreads = kChunk * 4;
 template <int NPL>
-__global__ void __launch_bounds__(1024) route_kernel(const float* __restrict__ logits,
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits,
                                                    const int32_t* __restrict__ ext_ids,
                                                    const float* __restrict__ ext_w, int T, int E, int k,
                                                    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
@@ -152,7 +155,7 @@ int launch_route(const float* logits, const int32_t* ext_ids, const float* ext_w
   const size_t smem = (size_t)E * (kChunk / 32) * sizeof(uint32_t);
   const int npl = (E + 31) / 32;
 #define MOE_ROUTE(N)                                                                                 \
-  route_kernel<N><<<C, 1024, smem, stream>>>(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, \
+  route_kernel<N><<<C, kRouteThreads, smem, stream>>>(logits, ext_ids, ext_w, T, E, k, topk_ids, topk_w, \
                                            token_slot_row, hist, status)
   if (npl <= 1) MOE_ROUTE(1);
   else if (npl <= 2) MOE_ROUTE(2);

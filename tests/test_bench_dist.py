@@ -98,3 +98,27 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     base = sha_of("int f(int x) {\n  return x + 1;\n}\n")
     assert sha_of("// a comment\nint f(int x) {  // trailing\n\n  return x + 1;   \n}\n") == base
     assert sha_of("int f(int x) {\n  return x + 2;\n}\n") != base
+
+
+def test_reference_arm_line(capsys, monkeypatch):
+    """The reference arm (the oracle on the host cores) on one process: one
+    JSON line with the native arm's metric, unit and config, its own
+    cpu_baseline and an e2e entry without copies; with no explicit sample
+    size it takes whole 256-token samples of the tiny layer."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    for v in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(v, raising=False)
+    args = argparse.Namespace(workload="tiny", seed=0, ref_tokens=None, warmup=3, steps=1)
+    bench.reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    lay = synth.layer("tiny")
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["config"] == bench.config_of("tiny", lay, 1)
+    assert line["steps"] == 1 and line["warmup"] == 3 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["sample"].startswith("256 consecutive tokens")
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+

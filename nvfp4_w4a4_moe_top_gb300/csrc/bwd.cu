@@ -6,13 +6,16 @@
 // the table: the layer bypass saves the original BF16 operands).
 //
 // Launch sequence of moe_expert_backward:
-//   fc2_scatter_kernel<2> (gemm.cu) recomputes the forward's expert outputs
-//                       y2 from the saved FP4 operands (bit-identical) and,
-//                       per permuted row r of token t, slot j:
+//   FC2 in MODE 2 (gemm.cu: fc2_pair_kernel<2> on CTA pairs, else
+//                       fc2_scatter_kernel<2>) recomputes the forward's
+//                       expert outputs y2 from the saved FP4 operands
+//                       (bit-identical) and, per permuted row r of token t,
+//                       slot j:
 //                         dw[t][j] = <dY[t], y2[r]>            (FP32)
 //                         dy2[r] = BF16(RN_f32(w_tj * dY[t]))  (GEMM operand)
 //                       with dy2 zero on pad rows.
-//   bwd_xrows_kernel    xp[r] = x[t] (GEMM operand), zero on pad rows.
+//   bwd_xrows_kernel    xp[r] = x[t] (GEMM operand), zero on pad rows; on a
+//                       second stream, beside the next three GEMMs.
 //   bwd_logits_kernel   dlogits[t][e_j] = w_j (dw_j - sum_i w_i dw_i).
 //   bwd_gemm (DGRAD_SWIGLU)  dh = dy2 . W2_e (FP32 in tensor memory), then
 //                       SwiGLU backward in the epilogue against the saved u:
@@ -24,8 +27,10 @@
 //   bwd_dx_kernel       dx[t] = sum_j dxr[row(t,j)], ascending j, FP32.
 //
 // bwd_gemm is one persistent kernel (one CTA per SM, 10 warps) running
-// tcgen05.mma kind::f16 (BF16 x BF16 -> FP32, M = 128, N = 128 or 256,
-// K = 16 per instruction) from 128-byte-swizzled TMA tiles:
+// tcgen05.mma kind::f16 (BF16 x BF16 -> FP32, K = 16 per instruction) from
+// 128-byte-swizzled TMA tiles: on CTA pairs (cta_group::2, M = 256, N = 256)
+// where N and, for the wgrads, the output rows per expert are multiples of
+// 256, else on single CTAs (M = 128, N = 128 or 256):
 //   warp 8   TMA producer: per 64-deep k-step one A tile (128 rows) and one B
 //            tile (N columns) into a ring of stages;
 //   warp 9   MMA issuer: four MMAs per k-step into one of two accumulators

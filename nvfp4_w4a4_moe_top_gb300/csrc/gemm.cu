@@ -4,8 +4,9 @@
 // AI summary methodology: outer factors applied in FP32 after the native
 // block-scaled multiply, no decoded BF16 operand).
 //
-// Design (one persistent CTA per SM; NE epilogue warps, NE = 16 in FC1 and 8
-// in FC2, then 4 scale writers, 3 producers and the MMA issuer):
+// Design (one persistent CTA per SM; NE epilogue warps, NE = 16 in FC1 and in
+// FC2 on CTA pairs, 8 in FC2 on single CTAs, then 4 scale writers, 3
+// producers and the MMA issuer):
 //   warps NE+4 .. NE+6  TMA producers.  A work unit is one 128-row tile of
 //            the routed rows (one expert).  Its A operand (128 rows x K FP4,
 //            128-byte swizzle) is loaded once into resident shared memory, one
@@ -54,6 +55,16 @@
 // on rank 0's sf_full / tempty barriers.  Each CTA runs the epilogue of its
 // own rows, and releases the accumulator once u is formed, before the SwiGLU.
 //
+// FC2 on CTA pairs (where d is a multiple of 256): the same pair units; an
+// item is 256 output columns, W2 rows nt*256.. in rank 0's B tile and the
+// next 128 in rank 1's, one 256-column accumulator per CTA, 16 epilogue
+// warps of 64 columns.  The backward's recomputation of FC2 (dw, dy2) runs
+// on the same kernel.
+//
+// The 24-warp kernels (FC1, FC2 on pairs) launch at 80 registers a thread and
+// move registers to the epilogue with setmaxnreg (96 for the epilogue, 56 for
+// the scale writers, 40 for the producers and the MMA issuer).
+//
 // Every wait is bounded (a few seconds of wall clock); on expiry the kernel
 // raises MOE_STATUS_TIMEOUT, drains its own copies and MMAs, frees tensor
 // memory and returns.
@@ -92,8 +103,9 @@ constexpr int FC2_NSLOT = 2;                           // FC2: double buffering
 // Epilogue warps per kernel: warp w serves TMEM lane quadrant w % 4 and
 // column part w / 4 of each accumulator.  FC1's SwiGLU/requantisation is
 // latency-bound and gains from four warps per scheduler (16 warps, 32
-// columns each, 80 registers per thread); FC2's light epilogue keeps 8 warps
-// of 64 columns at 128 registers.
+// columns each); FC2 on pairs drains 64 columns per warp of its 256-column
+// accumulator with 16 warps; FC2 on single CTAs keeps 8 warps of 64 columns
+// at 128 registers.
 constexpr int FC1_NE = 16, FC2_NE = 8;
 constexpr int FC2P_NE = 16;
 // Register split of the 24-warp kernels (launched at 80 per thread)

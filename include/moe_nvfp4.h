@@ -279,7 +279,14 @@ int nvfp4_grouped_gemm_fc1_swiglu(
  *   slots      bf16 [M_cap][d] (workspace, also an output): z by routed
  *              row; pad rows are written as zeros
  *   out        bf16 [T][d] (out)
- *   dbg_y_f32  f32 [M_cap][d] pre-weighting expert outputs y2, or NULL */
+ *   dbg_y_f32  f32 [M_cap][d] pre-weighting expert outputs y2, or NULL
+ * Launch: where d is a multiple of 256 the GEMM runs on pairs of CTAs
+ * (clusters of two, cta_group::2 MMAs covering two 128-row tiles and 256
+ * output columns); elsewhere on single CTAs.  Both give the same bits.  The
+ * environment variable MOE_FC2_CTA_PAIRS=0, read at each launch, selects
+ * single CTAs throughout (this entry point, the forwards and the backward's
+ * recomputation of FC2, whose dw then sums its columns in another grouping:
+ * equal within FP32 reassociation, dy2 bit for bit). */
 int nvfp4_grouped_gemm_fc2_unpermute(
     const uint8_t* h_codes, const uint8_t* h_sf, const float* h_g,
     const int32_t* offsets, int E, int64_t M_cap, int d_ff, int d,

@@ -101,10 +101,16 @@ def layer_of(name):
                             n_forced_empty=3)
     if name == "k1":
         return synth.custom(T=130, d=256, E=4, k=1, d_ff=128, seed=2)
+    if name == "ragged_pairs":
+        # d a multiple of 256, so the FC2 recomputation runs on CTA pairs (three
+        # rings, scale buffers on their own ring), with empty experts and odd
+        # tile counts (ghost tiles)
+        return synth.custom(T=1500, d=512, E=12, k=3, d_ff=256, seed=13, logits="bias", bias_std=2.0,
+                            n_forced_empty=3)
     return synth.layer(name)
 
 
-@pytest.mark.parametrize("name", ["tiny", "small", "ragged", "k1"])
+@pytest.mark.parametrize("name", ["tiny", "small", "ragged", "k1", "ragged_pairs"])
 def test_backward_against_oracle(orc, name):
     lay = layer_of(name)
     x, lg, W1, W2, dY = lay.x(), lay.logits(), lay.w1(), lay.w2(), lay.grad_out()
@@ -160,7 +166,7 @@ def test_backward_cta_pairs_equal_single(orc, name, monkeypatch):
         assert np.array_equal(r1[key].view(np.uint8), r2[key].view(np.uint8)), key
 
 
-@pytest.mark.parametrize("name", ["small", "tiny", "ragged"])
+@pytest.mark.parametrize("name", ["small", "tiny", "ragged_pairs"])
 def test_backward_fc2_pairs_equal_single(orc, name, monkeypatch):
     """The backward's FC2 recomputation on CTA pairs and on single CTAs: dy2
     and every gradient that flows from it bit for bit; dw (a dot product

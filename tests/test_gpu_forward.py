@@ -89,6 +89,9 @@ def layer_of(name):
         return synth.custom(T=64, d=128, E=1024, k=32, d_ff=128, seed=13)
     if name == "max_width":  # d and d_ff at their limits: A streams through the stages in both GEMMs
         return synth.custom(T=160, d=4096, E=2, k=1, d_ff=4096, seed=14)
+    if name == "ragged_pairs":  # FC2 on CTA pairs (three rings) with empty experts and odd tile counts
+        return synth.custom(T=1500, d=512, E=12, k=3, d_ff=256, seed=13, logits="bias", bias_std=2.0,
+                            n_forced_empty=3)
     return synth.layer(name)
 
 
@@ -119,7 +122,7 @@ def test_forward_against_oracle(orc, name):
     assert rel <= E2E_REL_L2 and ratio <= 1.0
 
 
-@pytest.mark.parametrize("name", ["small", "ragged", "tiny"])
+@pytest.mark.parametrize("name", ["small", "ragged", "tiny", "ragged_pairs"])
 def test_forward_cta_pairs_equal_single(orc, name, monkeypatch):
     """The forward with FC1 and FC2 on CTA pairs (the default where their
     shapes allow it) and with either GEMM on single CTAs: identical h codes

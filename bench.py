@@ -695,7 +695,33 @@ def cpu_baseline(lay, args, tokens=None):
     sec = time.perf_counter() - t0
     return {"value": round(tokens / sec, 2), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "first %d tokens of the %s workload, one oracle forward (weights quantised beforehand)"
-                      % (tokens, args.workload)}
+                      % (tokens, args.workload),
+            "single_thread": oracle_single_thread(args)}
+
+
+def oracle_single_thread(args, tokens=256):
+    """The oracle on one host thread, on the tiny and small layers (the first
+    `tokens` tokens of each, weights quantised beforehand): the per-core
+    figure beside the all-cores baseline."""
+    import oracle
+    import synth
+    out = {}
+    n0 = oracle.num_threads()
+    for name in ("tiny", "small"):
+        lay = synth.layer(name, seed=args.seed)
+        w1q, w2q = oracle_weights(lay)
+        n = min(tokens, lay.T)
+        x, lg = lay.x_rows(range(n)), lay.logits_rows(range(n))
+        oracle.set_num_threads(1)
+        try:
+            t0 = time.perf_counter()
+            oracle.moe_forward(x, lg, w1q, w2q, lay.k, lay.d_ff)
+            sec = time.perf_counter() - t0
+        finally:
+            oracle.set_num_threads(n0)
+        out[name] = {"value": round(n / sec, 2), "unit": UNIT, "cores": 1,
+                     "sample": "first %d tokens of the %s workload" % (n, name)}
+    return out
 
 
 def reference(args):

@@ -79,6 +79,7 @@ def lib():
                 "orc_e4m3_first_input_of_code": (I64, [ctypes.c_uint8]),
                 "orc_e2m1_first_input_of_code": (I64, [ctypes.c_uint8]),
                 "orc_num_threads": (I32, []),
+                "orc_set_num_threads": (None, [I32]),
                 "orc_rht16_rows": (None, [P, I64, I32, P, P]),
                 "orc_quantize_tensor": (None, [P, I64, I32, P, P, P]),
                 "orc_quantize_weights_per_expert": (None, [P, I32, I32, I32, P, P, P]),
@@ -359,6 +360,12 @@ class TokenOracle:
 
 def num_threads():
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n):
+    """Threads of the oracle's parallel loops from now on; results do not
+    depend on it."""
+    lib().orc_set_num_threads(int(n))
 
 
 # --------------------------------------------------------------------------

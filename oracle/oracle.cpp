@@ -463,6 +463,16 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads of the parallel loops from now on (n >= 1); the results do not
+   depend on it (each output is summed in a fixed order by one thread). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 }  // extern "C"
 
 /* ---- contrast recipes ---- */

@@ -96,6 +96,7 @@ void orc_reduce(const uint16_t* slots, int64_t T, int k, int d, uint16_t* out);
 int64_t orc_e4m3_first_input_of_code(uint8_t code);
 int64_t orc_e2m1_first_input_of_code(uint8_t code);
 int     orc_num_threads(void);
+void    orc_set_num_threads(int n);
 
 /* ---- contrast recipes (not the hot path's recipe) ---- */
 

@@ -29,6 +29,22 @@ def test_token_oracle_equals_full_forward(orc, tiny):
             assert np.array_equal(r["y2"][j], res["y2"][row])
 
 
+def test_results_do_not_depend_on_thread_count(orc, tiny):
+    """The oracle's parallel loops give every output to one thread, summed in
+    a fixed order: one thread and all threads give the same bits."""
+    lay, x, lg, W1, W2, w1q, w2q, res = tiny
+    n0 = orc.num_threads()
+    orc.set_num_threads(1)
+    try:
+        assert orc.num_threads() == 1 or n0 == 1
+        one = orc.moe_forward(x, lg, w1q, w2q, lay.k, lay.d_ff)
+    finally:
+        orc.set_num_threads(n0)
+    assert orc.num_threads() == n0
+    for key in ("out", "y2", "h", "slots"):
+        assert np.array_equal(one[key], res[key]), key
+
+
 def test_context_swap_invariance_end_to_end(orc, tiny):
     """Replacing and reordering the other tokens leaves a token's codes and
     output bitwise unchanged (per-token scales, RHT and stochastic rounding

@@ -4,7 +4,8 @@ column of the Technical Report's section 4.3 table) with the oracle.
 moe_nvfp4_quantize_weights_per_expert: codes, block scales, the replicated
 g and amax_e bit-exact with oracle.quantize_weights_per_expert, on small and
 ragged shapes, an all-zero expert, a single expert, rows spanning several
-decades, and sampled experts of the full Qwen-shaped W1 and W2.  The forward
+decades, replays of a CUDA graph that captured the call, and sampled
+experts of the full Qwen-shaped W1 and W2.  The forward
 on per-expert weights (same GEMM kernels, per-expert g in the epilogue)
 against the oracle forward on the oracle's per-expert weights.
 """
@@ -58,7 +59,8 @@ def test_small_layer_weights_bitexact(orc):
         check_equal(orc, W, gpu_per_expert(W))
 
 
-@pytest.mark.parametrize("E,N,K", [(3, 128, 192), (1, 256, 64), (5, 384, 4096), (2, 128, 1024)])
+@pytest.mark.parametrize("E,N,K", [(3, 128, 192), (1, 256, 64), (5, 384, 4096), (2, 128, 1024), (13, 128, 256),
+                                   (17, 256, 128)])
 def test_wide_range_and_zero_expert(orc, E, N, K):
     W = wide_range_weights(E, N, K, seed=E * 7 + K)
     if E > 1:
@@ -99,6 +101,40 @@ def test_nonfinite_weight_sets_status(orc):
     assert int(st.item()) & M.STATUS_NONFINITE_WEIGHT
     a = host(am)
     assert a[0] == np.float32(0.5) and a[1] == 0.0  # NaN does not win the maximum
+
+
+def test_replays_in_a_cuda_graph(orc):
+    """Captured on a stream in a CUDA graph (the memset of amax_e and both
+    launches), then replayed on new weights copied into the captured buffer:
+    every replay equals the oracle, so the maxima restart from zero on each
+    replay."""
+    import torch
+    from gpu_util import dev, host
+    E, N, K = 11, 128, 256
+    W = dev(wide_range_weights(E, N, K, seed=5))
+    q = M.empty_quantized(E * N, K)
+    am = torch.empty(E, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def call():
+        M.moe_nvfp4_quantize_weights_per_expert(W, q["codes"], q["sf"], q["g"], am, st)
+
+    with torch.cuda.stream(s):  # first call outside the capture: device checks
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for seed in [6, 7]:
+        Wn = wide_range_weights(E, N, K, seed=seed)
+        Wn[seed % E] = 0
+        W.copy_(dev(Wn))
+        g.replay()
+        torch.cuda.synchronize()
+        got = (host(q["codes"]).reshape(E, N, K // 2), host(q["sf"]), host(q["g"]).reshape(E, N), host(am))
+        check_equal(orc, Wn, got)
+    assert int(st.item()) == 0
 
 
 @pytest.mark.parametrize("which", ["w1", "w2"])

@@ -808,10 +808,11 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   return r;
 }
 
-// Codes of 16 BF16 values (8 packed words) for block scale S > 0.
+// Codes of 16 BF16 values (8 packed words) for block scale S > 0 (the
+// exact path out of line, which measured faster here).
 __device__ __forceinline__ uint2 e2m1_block16(const uint32_t (&w)[8], float S) {
   const uint32_t w0[4] = {w[0], w[1], w[2], w[3]}, w1[4] = {w[4], w[5], w[6], w[7]};
-  return e2m1_codes16(w0, w1, S);
+  return e2m1_codes16<true>(w0, w1, S);
 }
 
 // Largest BF16 magnitude of 16 values (8 packed words), as a float.

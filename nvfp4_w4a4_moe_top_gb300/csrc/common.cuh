@@ -206,78 +206,75 @@ __device__ __forceinline__ uint32_t e2m1x8_pairs(const uint64_t (&p)[4]) {
   return r;
 }
 
-// Codes of 8 BF16 values (4 packed words) for block scale S > 0:
-// c = Q_E2M1(RN(v / S)).  With R the hardware reciprocal of S (relative error
-// below 2^-23, measured over every input by the tests), the products
-// v*RN(R*(1-2^-21)) and v*RN(R*(1+2^-21)) bracket RN(v/S): each is within
-// 2^-23 + 2*2^-24 (relative) of v/S*(1 -+ 2^-21), while RN(v/S) is within
-// 2^-24 of v/S.  The encoder is monotone, so when both brackets give the same
-// codes those are the codes of RN(v/S).  Otherwise (a quotient within about
-// 2^-21 of a rounding boundary, e.g. an exact tie) the codes are recomputed
-// from the correctly rounded division.  Quotients far below 0.25 encode to
-// zero on both sides, so subnormal products do not break the argument.  The
-// bracket products go two at a time through the packed f32x2 multiply.
-// The two bracket factors depend on S only: a 16-element block computes
-// them once for both of its halves.
-struct E2m1Bracket {
-  uint64_t rl, rh;  // RN(R(1 - 2^-21)), RN(R(1 + 2^-21)), each in both halves
-  bool ok;          // 2^-120 <= S <= 2^120: R normal, the products finite
+// Element-wise fused multiply-add of two FP32 pairs, a * b + c rounded once
+// to nearest even per element: the same two results as two fmaf.
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Exact E2M1 codes with no fallback path: RN(v / S) by Markstein's
+// correctly rounded division (P. W. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34,
+// 1990; in FMA form also in Cornea, Harrison and Tang, "Scientific
+// Computing on Itanium-based Systems", 2002):
+//   y  = RN(1/S)                     the IEEE reciprocal, once per block
+//   q0 = RN(v y)                     within 1.5 ulp of v/S
+//   q1 = RN(q0 + RN(v - S q0) y)     within 0.5 ulp + 2^-45 relative: faithful
+//   q2 = RN(q1 + (v - S q1) y)       Markstein: with y the correctly rounded
+//                                    reciprocal and q1 faithful, the residual
+//                                    is exact and q2 = RN(v / S).
+// Domain: 2^-96 <= S <= 2^120 and |v| <= 16 S.  The residual of a quotient
+// of at least 2^-3 is then a multiple of 2^-145 or coarser, so it stays
+// exact; smaller quotients encode to zero whatever their last bits.  y is
+// normal and no step overflows.  The quantisers meet |v| <= 16 S by
+// construction: a block's scale is E4M3(RN(a_b / (6 g))) of the block's own
+// largest magnitude a_b, at most a factor 1.5 below a_b / (6 g) (the E4M3
+// subnormal step), so |v| / S <= 9.  The sign of v is ORed into the quotient,
+// which keeps the sign of a zero v.
+//
+// S lies in the domain through a power-of-two factor f per row: v and S are
+// both multiplied by f, which leaves v / S unchanged.  For a row with outer
+// scale g > 0 every block scale is RN(g s_b) with s_b a nonzero E4M3 value
+// (2^-9 .. 448); f = 2^64 below g = 2^-87, 2^-64 above g = 2^111, else 1,
+// puts g f in [2^-87, 2^111] and so S f in [2^-96, 2^120].  S f is exact;
+// v f is exact except, for f = 2^-64, below |v| = 2^-62, where in such a row
+// the quotient is under 2^-164 and encodes to zero (with v's sign) either
+// way.
+__device__ __forceinline__ float e2m1_row_factor(float g) {
+  return g < 0x1p-87f ? 0x1p64f : (g > 0x1p111f ? 0x1p-64f : 1.0f);
+}
+struct E2m1Div {
+  uint64_t f, nS, y;  // (f, f), (-S f, -S f) and (RN(1/(S f)), RN(1/(S f)))
 };
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+__device__ __forceinline__ E2m1Div e2m1_div(float S, float f) {
+  E2m1Div d;
+  const float Sf = S * f;
+  const float y = __frcp_rn(Sf);
+  d.f = f32x2_pack(f, f);
+  d.nS = f32x2_pack(-Sf, -Sf);
+  d.y = f32x2_pack(y, y);
+  return d;
 }
-__device__ __forceinline__ E2m1Bracket e2m1_bracket(float S) {
-  E2m1Bracket b;
-  b.ok = S >= 7.52316384526264e-37f && S <= 1.329227995784916e+36f;  // 2^-120, 2^120
-  const float R = b.ok ? rcp_approx(S) : 0.0f;
-  const float Rl = __fmul_rn(R, 0.99999952316284180f);  // 1 - 2^-21
-  const float Rh = __fmul_rn(R, 1.00000047683715820f);  // 1 + 2^-21
-  b.rl = f32x2_pack(Rl, Rl);
-  b.rh = f32x2_pack(Rh, Rh);
-  return b;
-}
-// The exact path: codes from the correctly rounded divisions.
-__device__ __forceinline__ uint32_t e2m1_codes8_exact(const uint32_t (&w)[4], float S) {
-  float q[8];
+__device__ __forceinline__ uint32_t e2m1_codes8_div(const uint32_t (&w)[4], const E2m1Div& d) {
+  uint64_t q[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    q[2 * i] = __fdiv_rn(bf16_lo(w[i]), S);
-    q[2 * i + 1] = __fdiv_rn(bf16_hi(w[i]), S);
+    const uint64_t v = mul_f32x2(f32x2_pack(bf16_lo(w[i]), bf16_hi(w[i])), d.f);
+    const uint64_t q0 = mul_f32x2(v, d.y);
+    const uint64_t q1 = fma_f32x2(fma_f32x2(d.nS, q0, v), d.y, q0);
+    const uint64_t q2 = fma_f32x2(fma_f32x2(d.nS, q1, v), d.y, q1);
+    const uint64_t sign = ((uint64_t)(w[i] & 0x80000000u) << 32) | (uint64_t)((w[i] & 0x8000u) << 16);
+    q[i] = q2 | sign;
   }
-  return e2m1x8(q);
+  return e2m1x8_pairs(q);
 }
-// The same, as one out-of-line function (see e2m1_codes8).
-static __device__ __noinline__ uint32_t e2m1_codes8_exact_call(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                                               float S) {
-  const uint32_t w[4] = {w0, w1, w2, w3};
-  return e2m1_codes8_exact(w, S);
-}
-// OUTLINE: the exact path is a call instead of inline code.  Measured per
-// caller: FC1's requantisation (inside the epilogue, under its register
-// split) runs 1.4% faster with the call; the row quantiser 2% slower, and
-// permute_quant the same, so those two keep it inline.
-template <bool OUTLINE = false>
-__device__ __forceinline__ uint32_t e2m1_codes8(const uint32_t (&w)[4], float S, const E2m1Bracket& br) {
-  if (br.ok) {
-    uint64_t l[4], h[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint64_t x = f32x2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
-      l[i] = mul_f32x2(x, br.rl);
-      h[i] = mul_f32x2(x, br.rh);
-    }
-    const uint32_t cl = e2m1x8_pairs(l);
-    if (cl == e2m1x8_pairs(h)) return cl;
-  }
-  return OUTLINE ? e2m1_codes8_exact_call(w[0], w[1], w[2], w[3], S) : e2m1_codes8_exact(w, S);
-}
-// Codes of the 16 BF16 values of one block (two groups of 4 packed words).
-template <bool OUTLINE = false>
-__device__ __forceinline__ uint2 e2m1_codes16(const uint32_t (&w0)[4], const uint32_t (&w1)[4], float S) {
-  const E2m1Bracket br = e2m1_bracket(S);
-  return make_uint2(e2m1_codes8<OUTLINE>(w0, S, br), e2m1_codes8<OUTLINE>(w1, S, br));
+// Codes of 16 BF16 values (two groups of 4 packed words) for a block scale
+// S > 0 of a row with factor f = e2m1_row_factor(g): Q_E2M1(RN(v / S)).
+__device__ __forceinline__ uint2 e2m1_codes16_div(const uint32_t (&w0)[4], const uint32_t (&w1)[4], float S, float f) {
+  const E2m1Div d = e2m1_div(S, f);
+  return make_uint2(e2m1_codes8_div(w0, d), e2m1_codes8_div(w1, d));
 }
 
 // ---------------------------------------------------------------------------

@@ -808,11 +808,11 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   return r;
 }
 
-// Codes of 16 BF16 values (8 packed words) for block scale S > 0 (the
-// exact path out of line, which measured faster here).
-__device__ __forceinline__ uint2 e2m1_block16(const uint32_t (&w)[8], float S) {
+// Codes of 16 BF16 values (8 packed words) for block scale S > 0 of a row
+// with factor f = e2m1_row_factor(g).
+__device__ __forceinline__ uint2 e2m1_block16(const uint32_t (&w)[8], float S, float f) {
   const uint32_t w0[4] = {w[0], w[1], w[2], w[3]}, w1[4] = {w[4], w[5], w[6], w[7]};
-  return e2m1_codes16<true>(w0, w1, S);
+  return e2m1_codes16_div(w0, w1, S, f);
 }
 
 // Largest BF16 magnitude of 16 values (8 packed words), as a float.
@@ -846,6 +846,7 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int vp, i
   uint32_t sb2 = 0;
   uint32_t cw[4];
   const float rden = block_scale_rden(den);
+  const float f = e2m1_row_factor(g);
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
     const uint32_t wb[8] = {cur[2 * b].x, cur[2 * b].y, cur[2 * b].z, cur[2 * b].w,
@@ -855,7 +856,7 @@ __device__ __forceinline__ void requant_chunk(const uint4* scr, int c, int vp, i
     if (g != 0.0f) {
       sb = block_scale_code(amax16_bf16(wb), den, rden);
       const float S = __fmul_rn(g, e4m3_decode_hw(sb));
-      if (S != 0.0f) p = e2m1_block16(wb, S);
+      if (S != 0.0f) p = e2m1_block16(wb, S, f);
     }
     cw[2 * b] = p.x;
     cw[2 * b + 1] = p.y;

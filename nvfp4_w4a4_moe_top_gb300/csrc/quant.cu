@@ -52,18 +52,18 @@ __device__ __forceinline__ uint32_t row_amax_bits(const uint4 (&v)[NG][4], uint3
 }
 
 // Codes, block scales and g of destination row r from the row in registers
-// (bm: its blocks' magnitude maxima) and the outer amax a.
+// (bm: its blocks' magnitude maxima) and the row's outer scale gs.
 template <int NG>
-__device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32_t (&bm)[NG][2], float a, int64_t r,
+__device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32_t (&bm)[NG][2], float gs, int64_t r,
                                            int K, int lane, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                            float* __restrict__ gout) {
   const int kg = K / 64;
   const int n8 = K / 8;
   uint4* crow = reinterpret_cast<uint4*>(codes + r * (K / 2));
   const int64_t sf_row = (r >> 7) * kg * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-  const float gs = __fdiv_rn(a, 2688.0f);
   const float den = __fmul_rn(6.0f, gs);
   const float rden = block_scale_rden(den);
+  const float f = e2m1_row_factor(gs);
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int e8 = g * 128 + 4 * lane;
@@ -77,7 +77,7 @@ __device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32
         const uint32_t sb = block_scale_code(__uint_as_float(bm[g][b] << 16), den, rden);
         const float S = __fmul_rn(gs, e4m3_decode_hw(sb));
         if (S != 0.0f) {
-          const uint2 cc = e2m1_codes16(w0, w1, S);
+          const uint2 cc = e2m1_codes16_div(w0, w1, S, f);
           c[2 * b] = cc.x;
           c[2 * b + 1] = cc.y;
         }
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
   uint32_t bm[NG][2];
   const uint32_t ab = row_amax_bits<NG>(v, bm, lane, status, nonfinite_bit);
   const float a = amax ? amax[s / amax_rows] : __uint_as_float(ab << 16);
-  encode_row<NG>(v, bm, a, r, K, lane, codes, sf, gout);
+  encode_row<NG>(v, bm, __fdiv_rn(a, 2688.0f), r, K, lane, codes, sf, gout);
 }
 
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,

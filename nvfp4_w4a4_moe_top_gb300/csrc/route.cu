@@ -334,6 +334,40 @@ int launch_pad_rows(int32_t* offsets, const int32_t* counts, int E, int64_t m_ca
 // of 1024 columns, the 32 consecutive columns from 32*L (two whole 16-element
 // blocks), so a block never spans lanes, its codes go out as one 16-byte
 // store per row, and lanes L, L ^ 1 together form one 32-bit scale word.
+// Codes (cw, one 16-byte word per group of 32 columns) and block-scale
+// words (sfw, the lane pair's four scales) of a token's row held in
+// registers, from its blocks' magnitude maxima bm and outer scale gs.
+template <int NG>
+__device__ __forceinline__ void encode_token(const uint4 (&v)[NG][4], const uint32_t (&bm)[NG][2], float gs,
+                                             uint4 (&cw)[NG], uint32_t (&sfw)[NG]) {
+  const float den = __fmul_rn(6.0f, gs);
+  const float rden = block_scale_rden(den);
+  const float f = e2m1_row_factor(gs);
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    uint32_t c[4] = {0u, 0u, 0u, 0u}, sb2 = 0u;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {  // the lane's two blocks of 16
+      const uint4 p0 = v[g][2 * b], p1 = v[g][2 * b + 1];
+      const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w}, w1[4] = {p1.x, p1.y, p1.z, p1.w};
+      const float ab = __uint_as_float(bm[g][b] << 16);
+      uint32_t sb = 0;
+      if (gs != 0.0f) {
+        sb = block_scale_code(ab, den, rden);
+        const float S = __fmul_rn(gs, e4m3_decode_hw(sb));
+        if (S != 0.0f) {
+          const uint2 cc = e2m1_codes16_div(w0, w1, S, f);
+          c[2 * b] = cc.x;
+          c[2 * b + 1] = cc.y;
+        }
+      }
+      sb2 |= sb << (8 * b);
+    }
+    cw[g] = make_uint4(c[0], c[1], c[2], c[3]);
+    sfw[g] = sb2 | (__shfl_xor_sync(0xFFFFFFFFu, sb2, 1) << 16);
+  }
+}
+
 template <int NG>
 __global__ void __launch_bounds__(256) permute_quant_kernel(
     const int32_t* __restrict__ topk_ids, int32_t* __restrict__ tsr, const int32_t* __restrict__ hist,
@@ -377,34 +411,10 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
       __uint_as_float((rm <= 0x7F80u ? rm : __reduce_max_sync(0xFFFFFFFFu, absmax_bits_no_nan(v))) << 16);
   if (lane == 0 && amax_tok) amax_tok[t] = a;
   const float gs = __fdiv_rn(a, 2688.0f);
-  const float den = __fmul_rn(6.0f, gs);
-  const float rden = block_scale_rden(den);
   const int kg = d / 64;
   uint4 cw[NG];
   uint32_t sfw[NG];
-#pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    uint32_t c[4] = {0u, 0u, 0u, 0u}, sb2 = 0u;
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {  // the lane's two blocks of 16
-      const uint4 p0 = v[g][2 * b], p1 = v[g][2 * b + 1];
-      const uint32_t w0[4] = {p0.x, p0.y, p0.z, p0.w}, w1[4] = {p1.x, p1.y, p1.z, p1.w};
-      const float ab = __uint_as_float(bm[g][b] << 16);
-      uint32_t sb = 0;
-      if (gs != 0.0f) {
-        sb = block_scale_code(ab, den, rden);
-        const float S = __fmul_rn(gs, e4m3_decode_hw(sb));
-        if (S != 0.0f) {
-          const uint2 cc = e2m1_codes16(w0, w1, S);
-          c[2 * b] = cc.x;
-          c[2 * b + 1] = cc.y;
-        }
-      }
-      sb2 |= sb << (8 * b);
-    }
-    cw[g] = make_uint4(c[0], c[1], c[2], c[3]);
-    sfw[g] = sb2 | (__shfl_xor_sync(0xFFFFFFFFu, sb2, 1) << 16);
-  }
+  encode_token<NG>(v, bm, gs, cw, sfw);
   if (tok_codes) {
     uint4* crow = reinterpret_cast<uint4*>(tok_codes + (int64_t)t * (d / 2));
 #pragma unroll

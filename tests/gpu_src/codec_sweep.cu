@@ -128,63 +128,104 @@ __global__ void block_scale_sweep(unsigned long long* viol) {
   if (bad) atomicAdd(viol, bad);
 }
 
-// The E2M1 codes of 8 values through the bracket against the exact
-// definition Q(RN(v / S)) for every finite BF16 v (either sign) and 65536
-// scales S spread over the float range.
-__global__ void e2m1_bracket_sweep(unsigned long long* viol) {
+// The quantisers' E2M1 encoder (e2m1_codes16_div with the row factor of
+// e2m1_row_factor) against the exact definition Q(RN(v / S)) for every
+// finite BF16 v (either sign) with |v| <= 16 S (other v are replaced by
+// zero; the quantisers never exceed 9 S) and 65536 scales S spread over the
+// whole float range, each as the block scale of rows with outer scale
+// g = S / s_b for s_b = 256, 1 and 2^-9 (the factor follows g).
+__global__ void e2m1_row_sweep(unsigned long long* viol) {
   const float S = spread(blockIdx.x * blockDim.x + threadIdx.x);
-  const moe::E2m1Bracket br = moe::e2m1_bracket(S);
   unsigned long long bad = 0;
+  for (int k = 0; k < 3; ++k) {
+    const float g = S * (k == 0 ? 0x1p-8f : (k == 1 ? 1.0f : 0x1p9f));
+    const float f = moe::e2m1_row_factor(g);
+    for (unsigned int b0 = 0; b0 < 0x10000u; b0 += 16) {
+      uint32_t w[2][4];
+      float q[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t lo = b0 + 8 * h + 2 * i, hi = lo + 1;
+          if ((lo & 0x7F80u) == 0x7F80u || fabsf(__uint_as_float(lo << 16)) > 16.0f * S) lo = 0;
+          if ((hi & 0x7F80u) == 0x7F80u || fabsf(__uint_as_float(hi << 16)) > 16.0f * S) hi = 0;
+          w[h][i] = lo | (hi << 16);
+          q[h][2 * i] = __fdiv_rn(moe::bf16_lo(w[h][i]), S);
+          q[h][2 * i + 1] = __fdiv_rn(moe::bf16_hi(w[h][i]), S);
+        }
+      const uint2 c = moe::e2m1_codes16_div(w[0], w[1], S, f);
+      if (c.x != moe::e2m1x8(q[0]) || c.y != moe::e2m1x8(q[1])) ++bad;
+    }
+  }
+  if (bad) atomicAdd(viol, bad);
+}
+
+// The E2M1 codes of 8 values through Markstein's division (e2m1_codes8_div)
+// against the exact definition Q(RN(v / S)) for every finite BF16 v (either
+// sign) within the division's domain |v| <= 16 S, over scales S in
+// [2^-96, 2^120]: threads 0 .. 215 take S with an all-ones significand at
+// each exponent of that range, the others S spread over it.  `checked`
+// counts the (v, S) pairs compared.
+__device__ __forceinline__ float spread_div_domain(unsigned int i) {
+  if (i < 216u) return __uint_as_float(((31u + i) << 23) | 0x007FFFFFu);  // biased exponents 31 .. 246
+  const unsigned int e = 31u + (i % 216u);
+  const unsigned int m = (i * 2654435761u) & 0x007FFFFFu;
+  return __uint_as_float((e << 23) | m);
+}
+__global__ void e2m1_div_sweep(unsigned long long* viol, unsigned long long* checked) {
+  const float S = spread_div_domain(blockIdx.x * blockDim.x + threadIdx.x);
+  const moe::E2m1Div dv = moe::e2m1_div(S, 1.0f);
+  const bool in = S >= 0x1p-96f && S <= 0x1p120f;
+  const float lim = 16.0f * S;
+  unsigned long long bad = 0, n = 0;
   for (unsigned int b0 = 0; b0 < 0x10000u; b0 += 8) {
     uint32_t w[4];
     float q[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t lo = b0 + 2 * i, hi = b0 + 2 * i + 1;
-      if ((lo & 0x7F80u) == 0x7F80u) lo = 0;  // non-finite patterns: zero instead
-      if ((hi & 0x7F80u) == 0x7F80u) hi = 0;
+      // non-finite patterns and values outside the domain: zero instead
+      if ((lo & 0x7F80u) == 0x7F80u || fabsf(__uint_as_float(lo << 16)) > lim) lo = 0;
+      else ++n;
+      if ((hi & 0x7F80u) == 0x7F80u || fabsf(__uint_as_float(hi << 16)) > lim) hi = 0;
+      else ++n;
       w[i] = lo | (hi << 16);
       q[2 * i] = __fdiv_rn(moe::bf16_lo(w[i]), S);
       q[2 * i + 1] = __fdiv_rn(moe::bf16_hi(w[i]), S);
     }
-    if (moe::e2m1_codes8(w, S, br) != moe::e2m1x8(q)) ++bad;
+    if (!in || moe::e2m1_codes8_div(w, dv) != moe::e2m1x8(q)) ++bad;
   }
   if (bad) atomicAdd(viol, bad);
+  atomicAdd(checked, n);
 }
 
-// Largest relative error of the hardware reciprocal over every float in
-// [2^-120, 2^120] (the bracket's domain), as float bits.
-__global__ void rcp_error(unsigned int* out) {
-  const unsigned int stride = gridDim.x * blockDim.x;
-  float e = 0.0f;
-  for (unsigned int p = 0x03800000u + blockIdx.x * blockDim.x + threadIdx.x; p <= 0x7B800000u; p += stride) {
-    const float x = __uint_as_float(p);
-    // y = (1 + err) / x, so x * y - 1 = err, formed exactly inside the fma
-    e = fmaxf(e, fabsf(fmaf(x, moe::rcp_approx(x), -1.0f)));
-  }
-  atomicMax(out, __float_as_uint(e));
+extern "C" int run_div_sweep(unsigned long long* viol, unsigned long long* checked) {
+  unsigned long long* d_v;
+  if (cudaMalloc(&d_v, 2 * 8)) return -1;
+  cudaMemset(d_v, 0, 2 * 8);
+  e2m1_div_sweep<<<256, 256>>>(d_v, d_v + 1);
+  unsigned long long v[2];
+  const int rc = cudaMemcpy(v, d_v, 2 * 8, cudaMemcpyDeviceToHost) ? -2 : 0;
+  *viol = v[0];
+  *checked = v[1];
+  cudaFree(d_v);
+  return rc;
 }
 
 extern "C" int run_fast_path_sweeps(unsigned long long* viol_e4m3, unsigned long long* viol_scale,
-                                    unsigned long long* viol_e2m1, float* rcp_max_rel) {
+                                    unsigned long long* viol_e2m1) {
   unsigned long long* d_v;
-  unsigned int* d_e;
-  if (cudaMalloc(&d_v, 3 * 8) || cudaMalloc(&d_e, 4)) return -1;
+  if (cudaMalloc(&d_v, 3 * 8)) return -1;
   cudaMemset(d_v, 0, 3 * 8);
-  cudaMemset(d_e, 0, 4);
   e4m3_hw_sweep<<<152 * 8, 256>>>(d_v);
   block_scale_sweep<<<256, 256>>>(d_v + 1);
-  e2m1_bracket_sweep<<<256, 256>>>(d_v + 2);
-  rcp_error<<<152 * 8, 256>>>(d_e);
+  e2m1_row_sweep<<<256, 256>>>(d_v + 2);
   unsigned long long v[3];
-  unsigned int e = 0;
-  int rc = 0;
-  if (cudaMemcpy(v, d_v, 3 * 8, cudaMemcpyDeviceToHost) || cudaMemcpy(&e, d_e, 4, cudaMemcpyDeviceToHost)) rc = -2;
+  const int rc = cudaMemcpy(v, d_v, 3 * 8, cudaMemcpyDeviceToHost) ? -2 : 0;
   *viol_e4m3 = v[0];
   *viol_scale = v[1];
   *viol_e2m1 = v[2];
-  memcpy(rcp_max_rel, &e, 4);
   cudaFree(d_v);
-  cudaFree(d_e);
   return rc;
 }

@@ -41,16 +41,32 @@ def test_quantiser_fast_paths_exhaustive():
     """The quantisers' fast paths equal their exact definitions: the
     hardware E4M3 conversion and decode (every non-negative finite float,
     every code); the bracketed block scale E4M3(RN(a / den)) (every finite
-    BF16 amax with 65536 divisors across the float range); the bracketed
-    E2M1 codes Q(RN(v / S)) (every finite BF16 value with 65536 scales); and
-    the hardware reciprocal the E2M1 bracket rests on stays within 2^-23
-    relative over the bracket's domain."""
+    BF16 amax with 65536 divisors across the float range); and the E2M1
+    encoder, Q(RN(v / S)) for every finite BF16 value up to 16 S with 65536
+    scales across the float range, each under three row scales (Markstein's
+    division after the row's power-of-two factor)."""
     from gpu_util import build_test_so
     L = ctypes.CDLL(build_test_so("codec_sweep"))
     v1, v2, v3 = ctypes.c_ulonglong(), ctypes.c_ulonglong(), ctypes.c_ulonglong()
-    e = ctypes.c_float()
-    assert L.run_fast_path_sweeps(ctypes.byref(v1), ctypes.byref(v2), ctypes.byref(v3), ctypes.byref(e)) == 0
-    print("e4m3 hw mismatches %d, block-scale mismatches %d, e2m1 bracket mismatches %d, rcp max rel %.3e"
-          % (v1.value, v2.value, v3.value, e.value))
+    assert L.run_fast_path_sweeps(ctypes.byref(v1), ctypes.byref(v2), ctypes.byref(v3)) == 0
+    print("e4m3 hw mismatches %d, block-scale mismatches %d, e2m1 encoder mismatches %d"
+          % (v1.value, v2.value, v3.value))
     assert v1.value == 0 and v2.value == 0 and v3.value == 0
-    assert 0 < e.value < 2.0 ** -23
+
+
+def test_markstein_division_codes_exhaustive():
+    """The quantisers' E2M1 codes come from Markstein's correctly rounded
+    division (RN(1/S) once per block, then two FMA corrections of v RN(1/S))
+    with no fallback: inside its domain (row factor 1) its codes equal
+    Q(RN(v / S)) from the IEEE division for
+    every finite BF16 v (either sign) within its domain |v| <= 16 S, over
+    65536 scales across [2^-96, 2^120], all-ones significands at every
+    exponent among them."""
+    from gpu_util import build_test_so
+    L = ctypes.CDLL(build_test_so("codec_sweep"))
+    viol, checked = ctypes.c_ulonglong(), ctypes.c_ulonglong()
+    assert L.run_div_sweep(ctypes.byref(viol), ctypes.byref(checked)) == 0
+    print("markstein division: %d (v, S) pairs, %d mismatching 8-value groups" % (checked.value, viol.value))
+    assert checked.value > 2 ** 31  # the domain holds most (v, S) pairs
+    assert viol.value == 0
+

@@ -598,9 +598,12 @@ def native(args):
           "launches": 14, "workload": "forward with saved values + BF16 backward, dY ~ N(0, 1e-3)"}
     wq = lambda t: {"ms": round(t * 1e3, 4), "achieved": round(wq_bytes / t / 1e9, 1), "unit": "GB/s",
                     "frac": round(wq_bytes / t / 1e9 / peaks["hbm_gbs"], 4)}
-    next_rows = {"weight_quant_per_row": dict(wq(t_wq_row), launches=2),
-                 "weight_quant_per_expert": dict(wq(t_wq_exp), launches=4,
-                                                 note="two passes over W: expert amax, then encode"),
+    next_rows = {"weight_quant_per_row": dict(wq(t_wq_row), launches=4,
+                                              note="per tensor: the encode, then the fix-up pass for rows with "
+                                                   "extreme outer scales"),
+                 "weight_quant_per_expert": dict(wq(t_wq_exp), launches=6,
+                                                 note="two passes over W: expert amax, then encode (and the "
+                                                      "fix-up pass)"),
                  "forward_per_expert_weights": {"value": round(T / t_fwd_exp, 1), "unit": UNIT,
                                                 "ms_per_step": round(t_fwd_exp * 1e3, 4)},
                  "forward_gather_on_load": {"value": round(T / t_fwd_gather, 1), "unit": UNIT,

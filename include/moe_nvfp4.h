@@ -142,7 +142,10 @@ int moe_expert_forward_workspace_layout(int T, int E, int k, int d, int d_ff,
  *   sf     u8   nvfp4_sf_bytes(E*N, K), the E*N rows as one matrix (out)
  *   g      f32  [E][N]            (out)
  * Needs N % 128 == 0, K % 64 == 0, 64 <= K <= 4096.  Called for W1
- * (N = 2 d_ff, K = d) and W2 (N = d, K = d_ff). */
+ * (N = 2 d_ff, K = d) and W2 (N = d, K = d_ff).  Two launches on `stream`:
+ * the row quantiser, then a fix-up pass that encodes the rare rows whose
+ * outer scale lies outside [2^-87, 2^111] (row maxima below about 1.7e-23
+ * or above about 7e36), which the first leaves. */
 int moe_nvfp4_quantize_weights(const uint16_t* W, int E, int N, int K,
                                uint8_t* codes, uint8_t* sf, float* g,
                                int* status, void* stream);
@@ -158,9 +161,9 @@ int moe_nvfp4_quantize_weights(const uint16_t* W, int E, int N, int K,
  *   W, codes, sf, g, shapes   as moe_nvfp4_quantize_weights
  *   amax_e f32 [E]  (out) max |W_e| of each expert; also the accumulator of
  *                   the reduction, so it must not alias W, codes, sf or g
- * Two launches and one memset on `stream`: zero amax_e, per-expert maximum
- * (integer atomicMax on the bits of non-negative floats), then the row
- * quantiser.  NaN/Inf weights set MOE_STATUS_NONFINITE_WEIGHT; NaNs do not
+ * Three launches and one memset on `stream`: zero amax_e, per-expert
+ * maximum (integer atomicMax on the bits of non-negative floats), then the
+ * row quantiser and its fix-up pass (as moe_nvfp4_quantize_weights).  NaN/Inf weights set MOE_STATUS_NONFINITE_WEIGHT; NaNs do not
  * enter the maximum.  Errors as moe_nvfp4_quantize_weights, plus
  * MOE_ERR_CUDA if the memset cannot be enqueued. */
 int moe_nvfp4_quantize_weights_per_expert(const uint16_t* W, int E, int N,
@@ -235,7 +238,8 @@ int moe_permute_amax_noalloc(const float* logits, const int32_t* ext_ids,
  *   amax     f32 [src_rows] outer-scale arguments, NULL = computed per row
  *   codes    u8 [dst_rows][K/2], sf nvfp4_sf_bytes(dst_rows, K), g f32
  *            [dst_rows] (out)
- * Needs K % 64 == 0, 64 <= K <= 4096. */
+ * Needs K % 64 == 0, 64 <= K <= 4096.  Two launches on `stream` (the row
+ * quantiser and its fix-up pass, as moe_nvfp4_quantize_weights). */
 int nvfp4_quantize_rows(const uint16_t* src, int src_rows, int K,
                         const int32_t* row_map, const float* amax,
                         int dst_rows, uint8_t* codes, uint8_t* sf, float* g,

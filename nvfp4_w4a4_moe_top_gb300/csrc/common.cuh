@@ -257,11 +257,15 @@ __device__ __forceinline__ E2m1Div e2m1_div(float S, float f) {
   d.y = f32x2_pack(y, y);
   return d;
 }
+// SCALED false: the caller guarantees f = 1 (the row scale within
+// [2^-87, 2^111], e2m1_div_row_scale_ok), and the multiply by f is left out.
+template <bool SCALED = true>
 __device__ __forceinline__ uint32_t e2m1_codes8_div(const uint32_t (&w)[4], const E2m1Div& d) {
   uint64_t q[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint64_t v = mul_f32x2(f32x2_pack(bf16_lo(w[i]), bf16_hi(w[i])), d.f);
+    const uint64_t v0 = f32x2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
+    const uint64_t v = SCALED ? mul_f32x2(v0, d.f) : v0;
     const uint64_t q0 = mul_f32x2(v, d.y);
     const uint64_t q1 = fma_f32x2(fma_f32x2(d.nS, q0, v), d.y, q0);
     const uint64_t q2 = fma_f32x2(fma_f32x2(d.nS, q1, v), d.y, q1);
@@ -272,10 +276,14 @@ __device__ __forceinline__ uint32_t e2m1_codes8_div(const uint32_t (&w)[4], cons
 }
 // Codes of 16 BF16 values (two groups of 4 packed words) for a block scale
 // S > 0 of a row with factor f = e2m1_row_factor(g): Q_E2M1(RN(v / S)).
+// SCALED as e2m1_codes8_div.
+template <bool SCALED = true>
 __device__ __forceinline__ uint2 e2m1_codes16_div(const uint32_t (&w0)[4], const uint32_t (&w1)[4], float S, float f) {
   const E2m1Div d = e2m1_div(S, f);
-  return make_uint2(e2m1_codes8_div(w0, d), e2m1_codes8_div(w1, d));
+  return make_uint2(e2m1_codes8_div<SCALED>(w0, d), e2m1_codes8_div<SCALED>(w1, d));
 }
+// The row scales whose row factor is 1: g in [2^-87, 2^111].
+__device__ __forceinline__ bool e2m1_div_row_scale_ok(float g) { return g >= 0x1p-87f && g <= 0x1p111f; }
 
 // ---------------------------------------------------------------------------
 // PTX wrappers: mbarrier, TMA, tcgen05

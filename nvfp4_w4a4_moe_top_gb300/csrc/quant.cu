@@ -52,8 +52,9 @@ __device__ __forceinline__ uint32_t row_amax_bits(const uint4 (&v)[NG][4], uint3
 }
 
 // Codes, block scales and g of destination row r from the row in registers
-// (bm: its blocks' magnitude maxima) and the row's outer scale gs.
-template <int NG>
+// (bm: its blocks' magnitude maxima) and the row's outer scale gs.  SCALED
+// false: gs passes e2m1_div_row_scale_ok, so the row factor is 1.
+template <int NG, bool SCALED>
 __device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32_t (&bm)[NG][2], float gs, int64_t r,
                                            int K, int lane, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                            float* __restrict__ gout) {
@@ -63,7 +64,7 @@ __device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32
   const int64_t sf_row = (r >> 7) * kg * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
   const float den = __fmul_rn(6.0f, gs);
   const float rden = block_scale_rden(den);
-  const float f = e2m1_row_factor(gs);
+  const float f = SCALED ? e2m1_row_factor(gs) : 1.0f;
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int e8 = g * 128 + 4 * lane;
@@ -77,7 +78,7 @@ __device__ __forceinline__ void encode_row(const uint4 (&v)[NG][4], const uint32
         const uint32_t sb = block_scale_code(__uint_as_float(bm[g][b] << 16), den, rden);
         const float S = __fmul_rn(gs, e4m3_decode_hw(sb));
         if (S != 0.0f) {
-          const uint2 cc = e2m1_codes16_div(w0, w1, S, f);
+          const uint2 cc = e2m1_codes16_div<SCALED>(w0, w1, S, f);
           c[2 * b] = cc.x;
           c[2 * b + 1] = cc.y;
         }
@@ -120,7 +121,46 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(
   uint32_t bm[NG][2];
   const uint32_t ab = row_amax_bits<NG>(v, bm, lane, status, nonfinite_bit);
   const float a = amax ? amax[s / amax_rows] : __uint_as_float(ab << 16);
-  encode_row<NG>(v, bm, __fdiv_rn(a, 2688.0f), r, K, lane, codes, sf, gout);
+  const float gs = __fdiv_rn(a, 2688.0f);
+  if (gs != 0.0f && !e2m1_div_row_scale_ok(gs)) {  // warp-uniform and rare: left to the fix-up pass
+    if (lane == 0) gout[r] = gs;
+    return;
+  }
+  encode_row<NG, false>(v, bm, gs, r, K, lane, codes, sf, gout);
+}
+
+// Fix-up pass after quantize_rows_kernel: the rows it left, whose outer
+// scale g (already in gout) is nonzero and outside [2^-87, 2^111], encoded
+// with the E2M1 division's row factor.  Such rows are rare (row maxima
+// below about 1.7e-23 or above 7e36), so the main pass carries a single
+// copy of the encoder, without the factor; here each warp reads the g of
+// 32 rows at a time and takes the flagged ones one by one.
+template <int NG>
+__global__ void __launch_bounds__(256) quantize_rows_fixup_kernel(
+    const uint16_t* __restrict__ src, int K, const int32_t* __restrict__ row_map, int64_t dst_rows,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ gout) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * 8;
+  for (int64_t r0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * 32; r0 < dst_rows; r0 += nw * 32) {
+    const float gl = r0 + lane < dst_rows ? gout[r0 + lane] : 0.0f;
+    unsigned need = __ballot_sync(0xFFFFFFFFu, gl != 0.0f && !e2m1_div_row_scale_ok(gl));
+    while (need) {
+      const int i = __ffs(need) - 1;
+      need &= need - 1;
+      const int64_t r = r0 + i;
+      const float gs = __shfl_sync(0xFFFFFFFFu, gl, i);
+      // the main pass zeroed the rows of invalid map entries (g = 0), so s is valid
+      const int64_t s = row_map ? (int64_t)row_map[r] : r;
+      uint4 v[NG][4];
+      load_row<NG>(src + s * (int64_t)K, K, lane, v);
+      uint32_t bm[NG][2];
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) bm[g][b] = absmax_bits16(v[g][2 * b], v[g][2 * b + 1]);
+      encode_row<NG, true>(v, bm, gs, r, K, lane, codes, sf, gout);
+    }
+  }
 }
 
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,
@@ -129,12 +169,20 @@ int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int
   if (dst_rows <= 0) return 0;
   const int ng = (K + 1023) / 1024;
   const dim3 grid((unsigned)((dst_rows + 7) / 8));
+  // fix-up pass: 256 rows per block and iteration, at most four blocks per SM
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    sms = 152;
+  const int64_t fix_all = (dst_rows + 255) / 256;
+  const dim3 fix_grid((unsigned)(fix_all < 4 * sms ? fix_all : 4 * sms));
 #define MOE_QR(N)                                                                                            \
   quantize_rows_kernel<N><<<grid, 256, 0, stream>>>(src, src_rows, K, row_map, amax, amax_rows, dst_rows, codes, \
-                                                    sf, g, status, nonfinite_bit)
-  if (ng <= 1) MOE_QR(1);
-  else if (ng <= 2) MOE_QR(2);
-  else MOE_QR(4);
+                                                    sf, g, status, nonfinite_bit);                                \
+  quantize_rows_fixup_kernel<N><<<fix_grid, 256, 0, stream>>>(src, K, row_map, dst_rows, codes, sf, g)
+  if (ng <= 1) { MOE_QR(1); }
+  else if (ng <= 2) { MOE_QR(2); }
+  else { MOE_QR(4); }
 #undef MOE_QR
   return 0;
 }

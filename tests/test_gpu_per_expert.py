@@ -71,6 +71,16 @@ def test_wide_range_and_zero_expert(orc, E, N, K):
         assert got[3][1] == 0 and not got[2][1].any() and not got[0][1].any()
 
 
+def test_extreme_expert_scales(orc):
+    """Experts whose outer scale leaves [2^-87, 2^111] (maxima near 1e-30 and
+    1e37): encoded by the fix-up pass with the E2M1 division's row factor,
+    bit-exact all the same, beside an ordinary expert."""
+    rng = np.random.default_rng(21)
+    W = np.stack([rng.standard_normal((256, 512)) * s for s in (1e-30, 0.02, 1e37)]).astype(np.float32)
+    W = bf16(W)
+    check_equal(orc, W, gpu_per_expert(W))
+
+
 def test_per_expert_differs_from_per_row(orc):
     """The two recipes really differ on the GPU: same codes as the per-row
     call only where a row's amax equals its expert's."""

@@ -25,8 +25,10 @@ def _cmp(orc, got, exp, rows, K):
     assert np.array_equal(orc.unswizzle_sf(gs, rows, K), orc.unswizzle_sf(es, rows, K))
 
 
+# scale 1e36: row maxima near 1e38, outer scales above 2^111, and the row
+# near 1e-38 below 2^-87: rows the main pass leaves to the fix-up pass
 @pytest.mark.parametrize("rows,K,scale", [(1, 64, 1.0), (37, 128, 1.0), (300, 768, 3.0), (129, 2048, 0.02),
-                                          (64, 4096, 1.0), (200, 1024, 1e-3), (50, 256, 1e30)])
+                                          (64, 4096, 1.0), (200, 1024, 1e-3), (50, 256, 1e30), (40, 2048, 1e36)])
 def test_quantize_rows_bitexact(orc, rows, K, scale):
     from gpu_util import dev, host
     import torch

@@ -14,6 +14,7 @@ import pytest
 
 import nvfp4_w4a4_moe_top_gb300 as M
 import synth
+from helpers import bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -120,6 +121,32 @@ def test_forward_against_oracle(orc, name):
           % (name, rel, mx, ratio, row_diff.mean()))
     assert row_diff.mean() <= H_ROWS_DIFFERING, row_diff.mean()
     assert rel <= E2E_REL_L2 and ratio <= 1.0
+
+
+def test_forward_extreme_token_scales(orc):
+    """Tokens whose maxima are 4e-36 and 2e37 (outer scales outside
+    [2^-87, 2^111]): the fused permute/quantise encodes them with the E2M1
+    division's power-of-two row factor, bit-exact with the oracle's
+    quantiser on the permuted rows.  The weights are scaled by 1e-36 (their
+    outer scales also leave the range) so that every GEMM value stays
+    finite; only the quantised x rows are compared."""
+    from helpers import f32
+    lay = layer_of("tiny")
+    xf = f32(lay.x())
+    peak = np.abs(xf).max(axis=1, keepdims=True)
+    xf[0::7] *= 4e-36 / peak[0::7]
+    xf[3::7] *= 2e37 / peak[3::7]
+    x = bf16(xf)
+    assert np.isfinite(f32(x)).all()
+    W1, W2 = bf16(f32(lay.w1()) * 1e-36), bf16(f32(lay.w2()) * 1e-36)
+    r, _, _ = gpu_forward(lay, x, lay.logits(), W1, W2)
+    mp = int(r["offsets"][-1])
+    codes, sf, g = orc.quantize_rows(x, row_map=r["row_to_token"][:mp], dst_rows=mp)
+    assert np.array_equal(r["x_codes"][:mp], codes)
+    assert np.array_equal(r["x_g"][:mp].view(np.uint32), g.view(np.uint32))
+    assert np.array_equal(orc.unswizzle_sf(r["x_sf"], mp, lay.d), orc.unswizzle_sf(sf, mp, lay.d))
+    gx = r["x_g"][:mp][r["row_to_token"][:mp] >= 0]
+    assert (gx < 2.0 ** -87).any() and (gx > 2.0 ** 111).any()  # both sides of the range are exercised
 
 
 @pytest.mark.parametrize("name", ["small", "ragged", "tiny", "ragged_pairs"])

@@ -9,6 +9,9 @@ namespace moe {
 constexpr int kRouteChunk = 64;  // tokens per routing chunk (one CTA); a multiple of 32
 
 // amax (optional) holds one entry per amax_rows consecutive source rows.
+// Two launches: the row quantiser, then its fix-up pass for the rows whose
+// outer scale lies outside [2^-87, 2^111] (encoded with the E2M1 division's
+// row factor).
 int launch_quantize_rows(const uint16_t* src, int64_t src_rows, int K, const int32_t* row_map,
                          const float* amax, int64_t amax_rows, int64_t dst_rows, uint8_t* codes, uint8_t* sf,
                          float* g, int* status, int nonfinite_bit, cudaStream_t stream);

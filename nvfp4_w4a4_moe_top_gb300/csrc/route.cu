@@ -82,21 +82,55 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
       uint32_t key[NPL];
 #pragma unroll
       for (int i = 0; i < NPL; ++i) key[i] = (i * 32 + lane < E) ? order_key(v[i]) : 0u;
-      uint32_t taken = 0u;
       float my_v = NEG_INF, vmax = NEG_INF;
-      for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0u;
-        int bi = -1;
+      if constexpr (NPL <= 4) {
+        // The lane's keys sorted once, largest first and, among equal keys,
+        // smaller id first (ids differ, so the order is total); absent
+        // experts carry key 0, below every logit, and sort last.  Each round
+        // the heads compete and the winning lane pops its head, so a lane's
+        // head is always its best untaken key, as the rescan below finds it.
+        uint32_t sk[NPL];
+        int si[NPL];
 #pragma unroll
-        for (int i = 0; i < NPL; ++i)
-          if (!((taken >> i) & 1u) && (bi < 0 || key[i] > bk) && i * 32 + lane < E) { bk = key[i]; bi = i; }
-        const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bi >= 0 ? bk : 0u);
-        const uint32_t my_inv = (bi >= 0 && bk == mk) ? 0xFFFFFFFFu - (uint32_t)(bi * 32 + lane) : 0u;
-        const int be = (int)(0xFFFFFFFFu - __reduce_max_sync(0xFFFFFFFFu, my_inv));
-        if (bi >= 0 && bi * 32 + lane == be) taken |= 1u << bi;
-        const float bv = key_value(mk);
-        if (lane == j) { my_id = be; my_v = bv; }
-        if (j == 0) vmax = bv;
+        for (int i = 0; i < NPL; ++i) { sk[i] = key[i]; si[i] = i; }
+        auto order = [&](int a, int b) {  // (sk[a], si[a]) before (sk[b], si[b])
+          if (sk[b] > sk[a] || (sk[b] == sk[a] && si[b] < si[a])) {
+            const uint32_t tk = sk[a]; sk[a] = sk[b]; sk[b] = tk;
+            const int ti = si[a]; si[a] = si[b]; si[b] = ti;
+          }
+        };
+        if constexpr (NPL == 2) order(0, 1);
+        if constexpr (NPL == 4) { order(0, 1); order(2, 3); order(0, 2); order(1, 3); order(1, 2); }
+        for (int j = 0; j < k; ++j) {
+          const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, sk[0]);  // a present expert's key: E >= k
+          const uint32_t hid = (uint32_t)(si[0] * 32 + lane);
+          const uint32_t my_inv = sk[0] == mk ? 0xFFFFFFFFu - hid : 0u;
+          const int be = (int)(0xFFFFFFFFu - __reduce_max_sync(0xFFFFFFFFu, my_inv));
+          if (sk[0] == mk && (int)hid == be) {
+#pragma unroll
+            for (int i = 0; i + 1 < NPL; ++i) { sk[i] = sk[i + 1]; si[i] = si[i + 1]; }
+            sk[NPL - 1] = 0u;
+          }
+          const float bv = key_value(mk);
+          if (lane == j) { my_id = be; my_v = bv; }
+          if (j == 0) vmax = bv;
+        }
+      } else {
+        uint32_t taken = 0u;
+        for (int j = 0; j < k; ++j) {
+          uint32_t bk = 0u;
+          int bi = -1;
+#pragma unroll
+          for (int i = 0; i < NPL; ++i)
+            if (!((taken >> i) & 1u) && (bi < 0 || key[i] > bk) && i * 32 + lane < E) { bk = key[i]; bi = i; }
+          const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, bi >= 0 ? bk : 0u);
+          const uint32_t my_inv = (bi >= 0 && bk == mk) ? 0xFFFFFFFFu - (uint32_t)(bi * 32 + lane) : 0u;
+          const int be = (int)(0xFFFFFFFFu - __reduce_max_sync(0xFFFFFFFFu, my_inv));
+          if (bi >= 0 && bi * 32 + lane == be) taken |= 1u << bi;
+          const float bv = key_value(mk);
+          if (lane == j) { my_id = be; my_v = bv; }
+          if (j == 0) vmax = bv;
+        }
       }
       // softmax over the selected logits (FP32)
       float ex = (lane < k) ? expf(my_v - vmax) : 0.0f;

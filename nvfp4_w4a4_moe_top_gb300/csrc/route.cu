@@ -211,11 +211,16 @@ __global__ void __launch_bounds__(256) scan_kernel(int32_t* __restrict__ hist, i
   const int e = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   int run = 0;
-  for (int base = 0; base < C; base += 256) {
-    const int c = base + threadIdx.x;
-    const int v = c < C ? hist[(int64_t)c * E + e] : 0;
-    // inclusive scan within the warp, then across the 8 warps
-    int x = v;
+  // rounds of 1024 chunks: thread i takes chunks 4i .. 4i+3 of the round,
+  // whose four loads go out together
+  for (int base = 0; base < C; base += 1024) {
+    const int c0 = base + 4 * threadIdx.x;
+    int v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = c0 + q < C ? hist[(int64_t)(c0 + q) * E + e] : 0;
+    const int own = v[0] + v[1] + v[2] + v[3];
+    // inclusive scan of the threads' sums within the warp, then across the 8 warps
+    int x = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
@@ -230,7 +235,12 @@ __global__ void __launch_bounds__(256) scan_kernel(int32_t* __restrict__ hist, i
       before += w < wid ? ws : 0;
       total += ws;
     }
-    if (c < C) hist[(int64_t)c * E + e] = run + before + x - v;
+    int ex = run + before + x - own;  // exclusive prefix of chunk c0
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (c0 + q < C) hist[(int64_t)(c0 + q) * E + e] = ex;
+      ex += v[q];
+    }
     run += total;
     __syncthreads();  // warp_sum is rewritten by the next round
   }
@@ -331,19 +341,30 @@ __global__ void __launch_bounds__(128) pad_rows_kernel(int32_t* __restrict__ off
       offsets[e + 1] = (int32_t)end;
       if (e == 0) offsets[0] = 0;
     }
-    const int64_t r = off_me + cnt + threadIdx.x;
-    if (r >= end) return;
-    row_to_token[r] = -1;
-    if (amax_row) amax_row[r] = 0.0f;
-    if (codes) {
-      uint4* cr = reinterpret_cast<uint4*>(codes + r * (K / 2));
-      for (int i = 0; i < K / 32; ++i) cr[i] = make_uint4(0u, 0u, 0u, 0u);
+    // the group's pad rows [p0, end) are contiguous: their codes are zeroed
+    // by the whole block with coalesced 16-byte stores, their scale words
+    // (one per 64 columns, scattered over the 128 x 4 tiles) spread over
+    // the threads
+    const int64_t p0 = off_me + cnt;
+    const int np = (int)(end - p0);
+    if (threadIdx.x < np) {
+      const int64_t r = p0 + threadIdx.x;
+      row_to_token[r] = -1;
+      if (amax_row) amax_row[r] = 0.0f;
+      if (sf) g[r] = 0.0f;
     }
-    if (sf) {
+    if (codes && np > 0) {
+      uint4* cr = reinterpret_cast<uint4*>(codes + p0 * (K / 2));
+      const int n16 = np * (K / 32);
+      for (int i = threadIdx.x; i < n16; i += blockDim.x) cr[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (sf && np > 0) {
       const int kg = K / 64;
-      for (int c4 = 0; c4 < kg; ++c4)
+      for (int i = threadIdx.x; i < np * kg; i += blockDim.x) {
+        const int64_t r = p0 + i / kg;
+        const int c4 = i % kg;
         *reinterpret_cast<uint32_t*>(sf + ((r >> 7) * kg + c4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4) = 0u;
-      g[r] = 0.0f;
+      }
     }
   } else {
     for (int64_t r = total + (int64_t)(blockIdx.x - E) * blockDim.x + threadIdx.x; r < m_cap;
